@@ -1,0 +1,254 @@
+"""CPU oracle for the half-precision GEMM and the BF16 linear layer.
+
+TEST INFRASTRUCTURE ONLY.  The tests, the package smoke check and the
+benchmark's CPU-baseline leg are the only code allowed to import this
+package.  The product library never imports, links or runs it, and it
+shares no code with the CUDA path.
+
+The arithmetic lives in ``oracle.c`` (plain C, FP64 accumulation, own
+FP16/BF16 codecs, one round-to-nearest-even at the end); this module only
+compiles that file with gcc and marshals numpy arrays into it.
+
+Definitions followed:
+
+* "MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 2 (GEMM入门):
+  C(m,n) = sum_k A(m,k) B(k,n), column-major A[m + k*M], B[k + n*K],
+  C[m + n*M]; section 1 (规则分析): FP16 in, FP32 accumulate, FP16 out.
+* DCU decode-GEMV article (forum.sourcefind.cn), sections 6.1-6.2: the
+  linear layer Y = X W^T with X:[n,k], W:[m,k], Y:[n,m].
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+(exhaustive codec checks against numpy/torch and brute force, identity and
+permutation matrices, rank-1 closed forms, exact rational brute force on tiny
+shapes, the transpose identity, GEMV/GEMM consistency).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import shutil
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so with gcc (-O2, OpenMP if available)."""
+    with _lock:
+        if (not force and os.path.exists(_LIB_PATH)
+                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            return _LIB_PATH
+        os.makedirs(_BUILD_DIR, exist_ok=True)
+        cc = shutil.which("gcc") or shutil.which("cc")
+        if cc is None:
+            raise RuntimeError("oracle: no C compiler (gcc) found")
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        base = [cc, "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", tmp]
+        r = subprocess.run(base[:2] + ["-fopenmp"] + base[2:] + ["-lm"],
+                           capture_output=True, text=True)
+        if r.returncode != 0:  # no libgomp: build single-threaded
+            r = subprocess.run(base + ["-lm"], capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError("oracle: gcc failed:\n" + r.stderr)
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    # A test that plants a mistake in a copy of oracle.c points this variable at
+    # the copy's build, to show that the pins catch the mistake.
+    path = os.environ.get("ORACLE_LIB_OVERRIDE") or build()
+    lib = ctypes.CDLL(path)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    lib.orc_f16_decode.argtypes = [ctypes.c_uint16]
+    lib.orc_f16_decode.restype = ctypes.c_double
+    lib.orc_bf16_decode.argtypes = [ctypes.c_uint16]
+    lib.orc_bf16_decode.restype = ctypes.c_double
+    lib.orc_f16_encode_rn.argtypes = [ctypes.c_double]
+    lib.orc_f16_encode_rn.restype = ctypes.c_uint16
+    lib.orc_bf16_encode_rn.argtypes = [ctypes.c_double]
+    lib.orc_bf16_encode_rn.restype = ctypes.c_uint16
+    for name in ("orc_f16_decode_n", "orc_bf16_decode_n"):
+        getattr(lib, name).argtypes = [u16p, f64p, i64]
+        getattr(lib, name).restype = None
+    for name in ("orc_f16_encode_n", "orc_bf16_encode_n"):
+        getattr(lib, name).argtypes = [f64p, u16p, i64]
+        getattr(lib, name).restype = None
+    lib.orc_max_threads.argtypes = []
+    lib.orc_max_threads.restype = ctypes.c_int
+    for name in ("orc_gemm_f16_colmajor_cols", "orc_gemm_f16_colmajor_rows"):
+        getattr(lib, name).argtypes = [u16p, u16p, i64, i64, i64, i64p, i64,
+                                       f64p, u16p, ctypes.c_int]
+        getattr(lib, name).restype = ctypes.c_int
+    for name in ("orc_linear_bf16", "orc_linear_bf16_tokens"):
+        getattr(lib, name).argtypes = [u16p, u16p, i64, i64, i64, i64p, i64,
+                                       f64p, u16p, ctypes.c_int]
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected uint16 bit patterns, got {a.dtype}")
+    return a
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def max_threads() -> int:
+    """Threads an OpenMP region of the oracle uses by default (1 if built without OpenMP)."""
+    return int(_load().orc_max_threads())
+
+
+# --------------------------------------------------------------------------
+# codecs
+# --------------------------------------------------------------------------
+
+def f16_decode(bits) -> np.ndarray:
+    """FP16 bit patterns -> exact float64 values (the oracle's own decoder)."""
+    b = _u16(bits)
+    out = np.empty(b.shape, np.float64)
+    _load().orc_f16_decode_n(_ptr(b, ctypes.c_uint16), _ptr(out, ctypes.c_double), b.size)
+    return out
+
+
+def bf16_decode(bits) -> np.ndarray:
+    """BF16 bit patterns -> exact float64 values (the oracle's own decoder)."""
+    b = _u16(bits)
+    out = np.empty(b.shape, np.float64)
+    _load().orc_bf16_decode_n(_ptr(b, ctypes.c_uint16), _ptr(out, ctypes.c_double), b.size)
+    return out
+
+
+def f16_encode(x) -> np.ndarray:
+    """float64 -> FP16 bits, one round-to-nearest-even straight from double."""
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _load().orc_f16_encode_n(_ptr(v, ctypes.c_double), _ptr(out, ctypes.c_uint16), v.size)
+    return out
+
+
+def bf16_encode(x) -> np.ndarray:
+    """float64 -> BF16 bits, one round-to-nearest-even straight from double."""
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _load().orc_bf16_encode_n(_ptr(v, ctypes.c_double), _ptr(out, ctypes.c_uint16), v.size)
+    return out
+
+
+# --------------------------------------------------------------------------
+# GEMM: C(m,n) = sum_k A(m,k) B(k,n), column-major, FP16 in/out
+# --------------------------------------------------------------------------
+
+def gemm_f16_colmajor(A, B, M: int, N: int, K: int, cols=None, threads: int = 0):
+    """Oracle for the column-major FP16 GEMM.
+
+    ``A`` and ``B`` are flat uint16 arrays holding A[m + k*M] and B[k + n*K].
+    Returns ``(ref, out)``: ``ref`` is the float64 sum (before rounding) and
+    ``out`` the FP16 bits after one round-to-nearest-even, both flat and
+    column-major with shape ``M x ncols`` (``ncols = N`` when ``cols`` is None,
+    else column j holds output column ``cols[j]``).
+    """
+    A = _u16(A).reshape(-1)
+    B = _u16(B).reshape(-1)
+    if A.size != M * K or B.size != N * K:
+        raise ValueError("oracle: operand sizes do not match M, N, K")
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nc = N if c is None else c.size
+    ref = np.empty(M * nc, np.float64)
+    out = np.empty(M * nc, np.uint16)
+    rc = _load().orc_gemm_f16_colmajor_cols(
+        _ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), M, N, K,
+        _ptr(c, ctypes.c_int64), 0 if c is None else c.size,
+        _ptr(ref, ctypes.c_double), _ptr(out, ctypes.c_uint16), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle gemm failed ({rc})")
+    return ref, out
+
+
+def gemm_f16_colmajor_rows(A, B, M: int, N: int, K: int, rows, threads: int = 0):
+    """Oracle GEMM restricted to output rows ``rows``.
+
+    Returns ``(ref, out)`` with shape ``len(rows) x N`` stored column-major:
+    entry (i, n) at ``i + n*len(rows)``.
+    """
+    A = _u16(A).reshape(-1)
+    B = _u16(B).reshape(-1)
+    if A.size != M * K or B.size != N * K:
+        raise ValueError("oracle: operand sizes do not match M, N, K")
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    ref = np.empty(r.size * N, np.float64)
+    out = np.empty(r.size * N, np.uint16)
+    rc = _load().orc_gemm_f16_colmajor_rows(
+        _ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), M, N, K,
+        _ptr(r, ctypes.c_int64), r.size,
+        _ptr(ref, ctypes.c_double), _ptr(out, ctypes.c_uint16), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle gemm rows failed ({rc})")
+    return ref, out
+
+
+# --------------------------------------------------------------------------
+# Linear layer: Y[t,j] = sum_k X[t,k] W[j,k], BF16 in/out
+# --------------------------------------------------------------------------
+
+def linear_bf16(W, X, M: int, K: int, n: int, js=None, threads: int = 0):
+    """Oracle for y = x W^T (decode GEMV when n is small, prefill GEMM when large).
+
+    ``W`` is [M,K] row-major, ``X`` is [n,K] row-major, both uint16 BF16 bits.
+    Returns ``(ref, out)`` of shape ``(n, nj)``: float64 sums and BF16 bits,
+    ``nj = M`` when ``js`` is None, else column i holds output feature ``js[i]``.
+    """
+    W = _u16(W).reshape(-1)
+    X = _u16(X).reshape(-1)
+    if W.size != M * K or X.size != n * K:
+        raise ValueError("oracle: operand sizes do not match M, K, n")
+    j = None if js is None else np.ascontiguousarray(js, dtype=np.int64)
+    nj = M if j is None else j.size
+    ref = np.empty(n * nj, np.float64)
+    out = np.empty(n * nj, np.uint16)
+    rc = _load().orc_linear_bf16(
+        _ptr(W, ctypes.c_uint16), _ptr(X, ctypes.c_uint16), M, K, n,
+        _ptr(j, ctypes.c_int64), 0 if j is None else j.size,
+        _ptr(ref, ctypes.c_double), _ptr(out, ctypes.c_uint16), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle linear failed ({rc})")
+    return ref.reshape(n, nj), out.reshape(n, nj)
+
+
+def linear_bf16_tokens(W, X, M: int, K: int, n: int, ts, threads: int = 0):
+    """Oracle linear layer for the tokens ``ts`` only: returns arrays of shape ``(len(ts), M)``."""
+    W = _u16(W).reshape(-1)
+    X = _u16(X).reshape(-1)
+    if W.size != M * K or X.size != n * K:
+        raise ValueError("oracle: operand sizes do not match M, K, n")
+    t = np.ascontiguousarray(ts, dtype=np.int64)
+    ref = np.empty(t.size * M, np.float64)
+    out = np.empty(t.size * M, np.uint16)
+    rc = _load().orc_linear_bf16_tokens(
+        _ptr(W, ctypes.c_uint16), _ptr(X, ctypes.c_uint16), M, K, n,
+        _ptr(t, ctypes.c_int64), t.size,
+        _ptr(ref, ctypes.c_double), _ptr(out, ctypes.c_uint16), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle linear tokens failed ({rc})")
+    return ref.reshape(t.size, M), out.reshape(t.size, M)

@@ -1,0 +1,345 @@
+/*
+ * oracle.c -- the plain, slow CPU oracle for the half-precision GEMM and
+ * the BF16 linear layer (decode GEMV / prefill GEMM).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * loads this file.  It is used by the tests, by the package smoke check and
+ * by the benchmark's timed CPU baseline, and by nothing else.  It shares no
+ * code, header, table or constant with the CUDA path.
+ *
+ * What it computes, and where that is stated:
+ *
+ *  - "MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 2 (GEMM入门):
+ *    C[m,n] = sum_k A[m,k] * B[k,n], written there as a triple loop with one
+ *    accumulator per output entry that runs over k in increasing order, and
+ *    the column-major addressing A(m,k) = A[m + k*M], B(k,n) = B[k + n*K],
+ *    C(m,n) = C[m + n*M].  Section 1 (规则分析) fixes the precision: FP16
+ *    inputs, FP32 accumulation, FP16 output.
+ *  - DCU decode-GEMV article (forum.sourcefind.cn), section 6.1: the linear
+ *    layer Y = X W^T with X:[n,k], W:[m,k], Y:[n,m] (all row-major), i.e.
+ *    Y[t,j] = sum_k X[t,k] * W[j,k]; section 6.2: each Y[j] is one
+ *    independent dot product over the whole k range.  BF16 in, BF16 out.
+ *
+ * How the oracle evaluates it:
+ *  - Inputs arrive as raw 16-bit patterns and are decoded by this file's own
+ *    IEEE binary16 / bfloat16 decoders (exact in double).
+ *  - Every product of two decoded inputs is exact in double (11+11 or 8+8
+ *    significand bits), and the sum is accumulated in double, k ascending,
+ *    exactly as the definition's loop runs.  The accumulated error is below
+ *    K * 2^-53 * sum|a*b|, far below any FP32 accumulation error.
+ *  - The exact-ish double result is rounded ONCE, round-to-nearest-even,
+ *    straight from double to FP16 (GEMM) or BF16 (linear).  Going through
+ *    float first would round twice; this file never does.  Overflow goes to
+ *    +-Inf; NaN stays NaN.
+ *
+ * The pages state no output rounding mode; this oracle takes the IEEE default
+ * (round to nearest, ties to even).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* IEEE binary16 and bfloat16 codecs, written from the format definitions.   */
+/* ------------------------------------------------------------------------ */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_f16_decode(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);              /* subnormal: f * 2^-24 */
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25);  /* (1.f) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+double orc_bf16_decode(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -133);             /* subnormal: f * 2^-133 */
+    } else if (e == 255) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(128 + f), e - 134);  /* (1.f) * 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+/*
+ * Round a double to a binary format with `frac_bits` fraction bits, exponent
+ * bias `bias` and all-ones exponent `emax_field`, nearest-even.
+ *
+ * |x| is written as n * q where q is the spacing of representable values in
+ * x's binade (or the subnormal spacing below the normal range).  x / q is an
+ * exact power-of-two rescale in double, and rint() in the default rounding
+ * mode rounds it to the nearest integer with ties to even.  n == 2^(frac+1)
+ * means the value rounded up into the next binade.
+ */
+static uint16_t orc_round_to_format(double x, int frac_bits, int bias, int emax_field)
+{
+    uint16_t sign = signbit(x) ? (uint16_t)(1u << 15) : 0;
+    uint16_t inf = (uint16_t)(emax_field << frac_bits);
+    if (isnan(x)) return (uint16_t)(sign | inf | (1u << (frac_bits - 1)));
+    double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | inf);
+    if (a == 0.0) return sign;
+
+    int ex;
+    frexp(a, &ex);             /* a = f * 2^ex, f in [0.5, 1) */
+    int E = ex - 1;            /* a in [2^E, 2^(E+1)) */
+    int emin = 1 - bias;       /* exponent of the smallest normal */
+    if (E < emin) {
+        /* subnormal range: spacing 2^(emin - frac_bits) */
+        double n = rint(ldexp(a, frac_bits - emin));
+        /* n == 2^frac_bits is exactly the smallest normal's encoding */
+        return (uint16_t)(sign | (uint16_t)n);
+    }
+    double n = rint(ldexp(a, frac_bits - E));   /* in [2^frac, 2^(frac+1)] */
+    if (n >= ldexp(1.0, frac_bits + 1)) {
+        n = ldexp(1.0, frac_bits);
+        E += 1;
+    }
+    int field = E + bias;
+    if (field >= emax_field) return (uint16_t)(sign | inf);
+    uint32_t frac = (uint32_t)n - (1u << frac_bits);
+    return (uint16_t)(sign | (uint16_t)(field << frac_bits) | (uint16_t)frac);
+}
+
+uint16_t orc_f16_encode_rn(double x) { return orc_round_to_format(x, 10, 15, 31); }
+uint16_t orc_bf16_encode_rn(double x) { return orc_round_to_format(x, 7, 127, 255); }
+
+/* Bulk versions for the Python side. */
+void orc_f16_decode_n(const uint16_t* in, double* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_decode(in[i]);
+}
+void orc_bf16_decode_n(const uint16_t* in, double* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_decode(in[i]);
+}
+void orc_f16_encode_n(const double* in, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_encode_rn(in[i]);
+}
+void orc_bf16_encode_n(const double* in, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_encode_rn(in[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Helpers                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Decode table for all 65536 patterns, built with the decoder above; a table
+ * lookup is the same value as calling the decoder, just cheaper. */
+static void orc_build_table(double* lut, int bf16)
+{
+    for (uint32_t i = 0; i < 65536u; ++i)
+        lut[i] = bf16 ? orc_bf16_decode((uint16_t)i) : orc_f16_decode((uint16_t)i);
+}
+
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static void orc_set_threads(int threads)
+{
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#else
+    (void)threads;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Column-major FP16 GEMM: C(m,n) = sum_k A(m,k) B(k,n)                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Computes the output columns listed in `cols` (all N columns when cols is
+ * NULL).  Column j of the result goes to ref[m + j*M] (double, before
+ * rounding) and out[m + j*M] (FP16 bits after the one rounding); either
+ * pointer may be NULL.
+ *
+ * Loop order: for each column n, one double accumulator per row m, and k runs
+ * 0..K-1 in the outer loop so that every accumulator sees its terms in the
+ * definition's order (k ascending); the inner loop over m walks A's column k,
+ * which is contiguous in the column-major layout.
+ */
+int orc_gemm_f16_colmajor_cols(const uint16_t* A, const uint16_t* B,
+                               int64_t M, int64_t N, int64_t K,
+                               const int64_t* cols, int64_t ncols,
+                               double* ref, uint16_t* out, int threads)
+{
+    if (M < 0 || N < 0 || K < 0) return 1;
+    int64_t nc = cols ? ncols : N;
+    double* lut = (double*)malloc(65536 * sizeof(double));
+    if (!lut) return 2;
+    orc_build_table(lut, 0);
+    orc_set_threads(threads);
+    int fail = 0;
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc((size_t)(M > 0 ? M : 1) * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            fail = 2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t j = 0; j < nc; ++j) {
+            if (!acc) continue;
+            int64_t n = cols ? cols[j] : j;
+            for (int64_t m = 0; m < M; ++m) acc[m] = 0.0;
+            if (n >= 0 && n < N) {
+                for (int64_t k = 0; k < K; ++k) {
+                    double b = lut[B[k + n * K]];
+                    const uint16_t* a_col = A + k * M;
+                    for (int64_t m = 0; m < M; ++m) acc[m] += lut[a_col[m]] * b;
+                }
+            }
+            for (int64_t m = 0; m < M; ++m) {
+                if (ref) ref[m + j * M] = acc[m];
+                if (out) out[m + j * M] = orc_f16_encode_rn(acc[m]);
+            }
+        }
+        free(acc);
+    }
+    free(lut);
+    return fail;
+}
+
+/*
+ * Computes the output rows listed in `rows`.  Row i of the result goes to
+ * ref[i + n*nrows] / out[i + n*nrows] (column-major over the selected rows).
+ * Each entry is one dot product over k ascending of row m of A (gathered
+ * once, it is strided in memory) and column n of B.
+ */
+int orc_gemm_f16_colmajor_rows(const uint16_t* A, const uint16_t* B,
+                               int64_t M, int64_t N, int64_t K,
+                               const int64_t* rows, int64_t nrows,
+                               double* ref, uint16_t* out, int threads)
+{
+    if (M < 0 || N < 0 || K < 0) return 1;
+    double* lut = (double*)malloc(65536 * sizeof(double));
+    if (!lut) return 2;
+    orc_build_table(lut, 0);
+    orc_set_threads(threads);
+    double* arow = (double*)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+    if (!arow) { free(lut); return 2; }
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t m = rows[i];
+        for (int64_t k = 0; k < K; ++k) arow[k] = (m >= 0 && m < M) ? lut[A[m + k * M]] : 0.0;
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            const uint16_t* b_col = B + n * K;
+            for (int64_t k = 0; k < K; ++k) acc += arow[k] * lut[b_col[k]];
+            if (ref) ref[i + n * nrows] = acc;
+            if (out) out[i + n * nrows] = orc_f16_encode_rn(acc);
+        }
+    }
+    free(arow);
+    free(lut);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* BF16 linear layer: Y[t,j] = sum_k X[t,k] W[j,k]                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * W is [M,K] row-major, X is [n,K] row-major, Y is [n,M] row-major.  Computes
+ * the output features j listed in `js` (all M when js is NULL) for every
+ * token t; entry (t, i) of the selection goes to ref[t*nj + i] / out[t*nj + i].
+ * Each entry is one dot product over k ascending, accumulated in double and
+ * rounded once to BF16.
+ */
+int orc_linear_bf16(const uint16_t* W, const uint16_t* X,
+                    int64_t M, int64_t K, int64_t n,
+                    const int64_t* js, int64_t njs,
+                    double* ref, uint16_t* out, int threads)
+{
+    if (M < 0 || K < 0 || n < 0) return 1;
+    int64_t nj = js ? njs : M;
+    double* lut = (double*)malloc(65536 * sizeof(double));
+    if (!lut) return 2;
+    orc_build_table(lut, 1);
+    orc_set_threads(threads);
+    /* decode X once: n*K doubles (small: X is the activation side) */
+    double* xd = (double*)malloc((size_t)((n * K) > 0 ? n * K : 1) * sizeof(double));
+    if (!xd) { free(lut); return 2; }
+    for (int64_t i = 0; i < n * K; ++i) xd[i] = lut[X[i]];
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < nj; ++i) {
+        int64_t j = js ? js[i] : i;
+        const uint16_t* wrow = W + j * K;
+        for (int64_t t = 0; t < n; ++t) {
+            double acc = 0.0;
+            if (j >= 0 && j < M) {
+                const double* xr = xd + t * K;
+                for (int64_t k = 0; k < K; ++k) acc += xr[k] * lut[wrow[k]];
+            }
+            if (ref) ref[t * nj + i] = acc;
+            if (out) out[t * nj + i] = orc_bf16_encode_rn(acc);
+        }
+    }
+    free(xd);
+    free(lut);
+    return 0;
+}
+
+/*
+ * Same linear layer, restricted to the tokens listed in `ts` (rows of X) for
+ * every output feature j: entry (i, j) goes to ref[i*M + j] / out[i*M + j].
+ */
+int orc_linear_bf16_tokens(const uint16_t* W, const uint16_t* X,
+                           int64_t M, int64_t K, int64_t n,
+                           const int64_t* ts, int64_t nts,
+                           double* ref, uint16_t* out, int threads)
+{
+    if (M < 0 || K < 0 || n < 0) return 1;
+    double* lut = (double*)malloc(65536 * sizeof(double));
+    if (!lut) return 2;
+    orc_build_table(lut, 1);
+    orc_set_threads(threads);
+    double* xd = (double*)malloc((size_t)((nts * K) > 0 ? nts * K : 1) * sizeof(double));
+    if (!xd) { free(lut); return 2; }
+    for (int64_t i = 0; i < nts; ++i)
+        for (int64_t k = 0; k < K; ++k)
+            xd[i * K + k] = (ts[i] >= 0 && ts[i] < n) ? lut[X[ts[i] * K + k]] : 0.0;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t j = 0; j < M; ++j) {
+        const uint16_t* wrow = W + j * K;
+        for (int64_t i = 0; i < nts; ++i) {
+            double acc = 0.0;
+            const double* xr = xd + i * K;
+            for (int64_t k = 0; k < K; ++k) acc += xr[k] * lut[wrow[k]];
+            if (ref) ref[i * M + j] = acc;
+            if (out) out[i * M + j] = orc_bf16_encode_rn(acc);
+        }
+    }
+    free(xd);
+    free(lut);
+    return 0;
+}

@@ -1,0 +1,48 @@
+"""The oracle's pins have teeth: plant one plausible mistake at a time in a
+copy of ``oracle/oracle.c`` (on the CPU), build the copy, and check that the
+pin suite fails against it.  The real oracle is never modified."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+# (name, text to replace, replacement, count) -- each must occur in oracle.c
+MUTANTS = [
+    ("drop_last_k", "for (int64_t k = 0; k < K; ++k) {\n                    double b",
+     "for (int64_t k = 0; k < K - 1; ++k) {\n                    double b", 1),
+    ("transposed_B_index", "lut[B[k + n * K]]", "lut[B[n + k * N]]", 1),
+    ("f16_sign_dropped", "v = ldexp((double)(1024 + f), e - 25);  /* (1.f) * 2^(e-15) */\n    }\n    return sign ? -v : v;",
+     "v = ldexp((double)(1024 + f), e - 25);  /* (1.f) * 2^(e-15) */\n    }\n    return v;", 1),
+    ("truncate_not_round", "double n = rint(ldexp(a, frac_bits - E));",
+     "double n = floor(ldexp(a, frac_bits - E));", 1),
+    ("bf16_wrong_bias", "e - 134", "e - 133", 1),
+    ("bf16_double_rounding", "return orc_round_to_format(x, 7, 127, 255);",
+     "return orc_round_to_format((double)(float)x, 7, 127, 255);", 1),
+    ("linear_reversed_k", "acc += xr[k] * lut[wrow[k]];", "acc += xr[k] * lut[wrow[K - 1 - k]];", 2),
+    ("f32_accumulator", "double* acc = (double*)malloc", "float* acc = (float*)malloc", 1),
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,old,new,count", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new, count):
+    src = open(SRC).read()
+    assert src.count(old) == count, f"mutant {name}: pattern not found as expected"
+    mutated = src.replace(old, new)
+    if name == "f32_accumulator":
+        mutated = mutated.replace("(size_t)(M > 0 ? M : 1) * sizeof(double)", "(size_t)(M > 0 ? M : 1) * sizeof(float)")
+    csrc = tmp_path / "oracle_mutant.c"
+    csrc.write_text(mutated)
+    lib = tmp_path / "liboracle_mutant.so"
+    r = subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", str(csrc), "-o", str(lib), "-lm"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    env = dict(os.environ, ORACLE_LIB_OVERRIDE=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
