@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the hot path: the 8192x8192x16384 column-major FP16 GEMM and
+the 34816x5120 BF16 decode GEMV (n = 1, 4, 8), on one GB300 per process.
+
+One step = one pass of the whole path on one batch of synthetic input:
+    gemm_f16_colmajor(A, B, C, 8192, 8192, 16384)
+    gemv_bf16(W_i, x_n, y_n, 34816, 5120, n)   for n in (1, 4, 8)
+(each GEMV reads its own copy W_i of the weights, so no call finds W in L2;
+the GEMM's operands, 537 MB, are larger than L2 too).  W = warm-up steps are
+run first, then exactly K steps are timed with CUDA events on the launching
+stream, bracketed by a barrier and a device synchronize.
+
+Reported (one JSON line, rank 0):
+  value      GEMM TFLOP/s: 2*M*N*K / mean GEMM kernel time (events around
+             each GEMM launch), times the number of ranks (replicas).
+  gemv       the GEMV's HBM GB/s per n (algorithmic bytes / kernel time).
+  e2e        the same metrics through the blocking C-ABI calls with pinned
+             host buffers: H2D of the step's inputs + call + D2H of the result.
+  roofline   for the dominant kernel (the GEMM) against the measured bf16
+             peak (FP16 and BF16 dense rates are equal on this part), plus
+             roofline_gemv against the measured HBM copy bandwidth.
+  cpu_baseline  the oracle timed on a bounded sample on the host cores.
+
+``--impl reference`` times the oracle (the plain CPU triple loop) on the same
+workload instead, on the host cores, each step a bounded sample of columns.
+Multi-GPU: one process per GPU under torchrun runs an independent replica.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+GEMM_M, GEMM_N, GEMM_K = 8192, 8192, 16384
+GEMV_M, GEMV_K, GEMV_NS = 34816, 5120, (1, 4, 8)
+METRIC = "FP16 GEMM TFLOP/s @8192x8192x16384; BF16 GEMV HBM GB/s (fraction of peak)"
+WORKLOAD = "gemm_f16_colmajor 8192x8192x16384 + gemv_bf16 34816x5120 n=1,4,8"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def gemm_flops() -> int:
+    return 2 * GEMM_M * GEMM_N * GEMM_K
+
+
+def gemv_bytes(n: int) -> int:
+    """Algorithmic bytes of one decode GEMV: W once, x once, y once (BF16)."""
+    return 2 * (GEMV_M * GEMV_K + n * GEMV_K + n * GEMV_M)
+
+
+def roofline(peak: float, bandwidth: float, intensity: float) -> float:
+    """Attainable rate min(P_peak, B * I) of the roofline model (DCU decode-GEMV
+    article, section 3); units follow the arguments (e.g. TFLOP/s, TB/s, FLOP/B)."""
+    return min(peak, bandwidth * intensity)
+
+
+# ---------------------------------------------------------------------------
+# environment: ranks, peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity for one rank)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    """Hash of the kernel sources; a committed traffic figure is only reported
+    while the kernels are unchanged since it was measured."""
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "bf16_gemm_skinny_gb300", "csrc")
+    for name in sorted(os.listdir(cdir)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(cdir, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key: str):
+    """DRAM bytes per launch from profiles/traffic.txt (lines: key digest bytes)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    digest = source_digest()
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key:
+                    return float(parts[2]) if parts[1] == digest else None
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 8]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_gemm_sample(A, B, seconds: float, max_cols: int = 4096):
+    """Runs the oracle on growing batches of output columns of the GEMM until
+    about `seconds` of CPU work; returns (flops, elapsed, cols, threads)."""
+    import oracle
+
+    threads = oracle.max_threads()
+    done, elapsed, batch, col = 0, 0.0, max(1, threads), 0
+    while elapsed < seconds and done < max_cols:
+        cols = [(col + i * 977) % GEMM_N for i in range(batch)]
+        t0 = time.perf_counter()
+        oracle.gemm_f16_colmajor(A, B, GEMM_M, GEMM_N, GEMM_K, cols=cols)
+        elapsed += time.perf_counter() - t0
+        done += batch
+        col += 1
+    return 2 * GEMM_M * GEMM_K * done, elapsed, done, threads
+
+
+def cpu_baseline(A, B, seconds: float):
+    flops, elapsed, cols, threads = oracle_gemm_sample(A, B, seconds)
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{cols} output columns of the 8192x8192x16384 GEMM (each 8192x16384 FMAs, FP64), "
+                      f"{elapsed:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from bf16_gemm_skinny_gb300 import _native as bsk
+    from bf16_gemm_skinny_gb300 import build as bsk_build
+    from bf16_gemm_skinny_gb300 import inputs
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    bsk_build.build()
+    bsk.load()
+
+    # ---- inputs: seeded, synthetic, shaped like the workload ----
+    A_h, B_h = inputs.gemm_operands(GEMM_M, GEMM_N, GEMM_K, "uniform")
+    W_h, _ = inputs.linear_operands(GEMV_M, GEMV_K, 1, "normal0.02", "normal1")
+    xs_h = {n: inputs.linear_operands(1, GEMV_K, n, "normal0.02", "normal1")[1] for n in GEMV_NS}
+
+    def pinned(a):
+        t = torch.from_numpy(a.view(np.int16)).pin_memory()
+        return t
+
+    A_p, B_p, W_p = pinned(A_h), pinned(B_h), pinned(W_h)
+    x_p = {n: pinned(xs_h[n]) for n in GEMV_NS}
+    A = A_p.to(dev)
+    B = B_p.to(dev)
+    C = torch.empty(GEMM_M * GEMM_N, dtype=torch.int16, device=dev)
+    Ws = [W_p.to(dev) for _ in GEMV_NS]           # one weight copy per GEMV call
+    xs = {n: x_p[n].to(dev) for n in GEMV_NS}
+    ys = {n: torch.empty(n * GEMV_M, dtype=torch.int16, device=dev) for n in GEMV_NS}
+    C_p = torch.empty(GEMM_M * GEMM_N, dtype=torch.int16).pin_memory()
+    y_p = {n: torch.empty(n * GEMV_M, dtype=torch.int16).pin_memory() for n in GEMV_NS}
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev["g0"].record(stream)
+        bsk.gemm_f16_colmajor_enqueue(A, B, C, GEMM_M, GEMM_N, GEMM_K, stream)
+        if ev is not None:
+            ev["g1"].record(stream)
+        for i, n in enumerate(GEMV_NS):
+            if ev is not None:
+                ev[f"v0_{n}"].record(stream)
+            bsk.gemv_bf16_enqueue(Ws[i], xs[n], ys[n], GEMV_M, GEMV_K, n, stream)
+            if ev is not None:
+                ev[f"v1_{n}"].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    bsk.stream_check(stream)
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+
+    keys = ["g0", "g1"] + [f"v{j}_{n}" for n in GEMV_NS for j in (0, 1)]
+    evs = [{k: torch.cuda.Event(enable_timing=True) for k in keys} for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    bsk.stream_check(stream)
+    barrier(dist, dev)
+
+    total_ms = t_start.elapsed_time(t_end)
+    gemm_ms = [e["g0"].elapsed_time(e["g1"]) for e in evs]
+    gemv_ms = {n: [e[f"v0_{n}"].elapsed_time(e[f"v1_{n}"]) for e in evs] for n in GEMV_NS}
+    gemm_ms_mean = statistics.fmean(gemm_ms)
+    gemm_ms_max = max_over_ranks(gemm_ms_mean, dist, dev)
+    total_ms_max = max_over_ranks(total_ms, dist, dev)
+    gemv_ms_mean = {n: max_over_ranks(statistics.fmean(v), dist, dev) for n, v in gemv_ms.items()}
+
+    # ---- end to end through the blocking C-ABI calls, host buffers ----
+    e2e_steps = max(2, min(5, args.steps))
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    e2e_gemm, e2e_gemv = [], {n: [] for n in GEMV_NS}
+    for _ in range(e2e_steps):
+        t0 = time.perf_counter()
+        A.copy_(A_p, non_blocking=True)
+        B.copy_(B_p, non_blocking=True)
+        bsk.gemm_f16_colmajor(A, B, C, GEMM_M, GEMM_N, GEMM_K, stream)
+        C_p.copy_(C, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_gemm.append(time.perf_counter() - t0)
+        for i, n in enumerate(GEMV_NS):
+            t0 = time.perf_counter()
+            Ws[i].copy_(W_p, non_blocking=True)
+            xs[n].copy_(x_p[n], non_blocking=True)
+            bsk.gemv_bf16(Ws[i], xs[n], ys[n], GEMV_M, GEMV_K, n, stream)
+            y_p[n].copy_(ys[n], non_blocking=True)
+            torch.cuda.synchronize()
+            e2e_gemv[n].append(time.perf_counter() - t0)
+    e2e_gemm_s = max_over_ranks(statistics.fmean(e2e_gemm), dist, dev)
+    e2e_gemv_s = {n: max_over_ranks(statistics.fmean(v), dist, dev) for n, v in e2e_gemv.items()}
+
+    peaks, peak_src = load_peaks()
+    value = world * gemm_flops() / (gemm_ms_max * 1e-3) / 1e12
+    per_launch_tflops = gemm_flops() / (gemm_ms_mean * 1e-3) / 1e12
+    gemm_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gemv = {}
+    for n in GEMV_NS:
+        gbs = gemv_bytes(n) / (gemv_ms_mean[n] * 1e-3) / 1e9
+        gemv[f"n{n}"] = {"gbs": round(world * gbs, 1), "us": round(gemv_ms_mean[n] * 1e3, 2),
+                         "frac_of_hbm": round(gbs / hbm_peak, 4),
+                         "e2e_gbs": round(world * gemv_bytes(n) / e2e_gemv_s[n] / 1e9, 1)}
+    gemv_n1_gbs = gemv_bytes(1) / (gemv_ms_mean[1] * 1e-3) / 1e9
+
+    h2d = (A.numel() + B.numel() + sum(W.numel() for W in Ws) + sum(x.numel() for x in xs.values())) * 2
+    d2h = (C.numel() + sum(y.numel() for y in ys.values())) * 2
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms_max / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16/bf16 in, f32 accumulate",
+        "data": "synthetic (seeded PCG64: GEMM A,B uniform[-1,1] FP16; W N(0,0.02), x N(0,1) BF16)",
+        "config": {"workload": WORKLOAD, "gemm": [GEMM_M, GEMM_N, GEMM_K], "gemv": [GEMV_M, GEMV_K, list(GEMV_NS)],
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (GEMM operands 537 MB; each GEMV reads its own 356 MB weight copy)"},
+        "gemv": gemv,
+        "e2e": {"value": round(world * gemm_flops() / e2e_gemm_s / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "gemv_gbs": {f"n{n}": gemv[f"n{n}"]["e2e_gbs"] for n in GEMV_NS},
+                "note": "blocking C-ABI calls; H2D of A,B (GEMM) and W,x (GEMV) from pinned memory, D2H of C / y"},
+        "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2), "peak": gemm_peak,
+                     "unit": "TFLOP/s", "frac": round(per_launch_tflops / gemm_peak, 4),
+                     "traffic": committed_traffic("gemm_f16_8192x8192x16384"),
+                     "peak_source": f"{peak_src} bf16_tflops (FP16 dense rate = BF16 on this part)",
+                     "kernel": "gemm_tcgen05_kernel<256,true,false>"},
+        "roofline_gemv": {"bound": "hbm", "achieved": round(gemv_n1_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                          "frac": round(gemv_n1_gbs / hbm_peak, 4),
+                          "traffic": committed_traffic("gemv_bf16_34816x5120_n1"),
+                          "peak_source": f"{peak_src} hbm_gbs", "kernel": "gemv_bf16_kernel<1,...> (n=1)"},
+        "gpu_launches": args.steps * (1 + len(GEMV_NS)),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(A_h, B_h, args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    from bf16_gemm_skinny_gb300 import inputs
+
+    oracle.build()
+    A_h, B_h = inputs.gemm_operands(GEMM_M, GEMM_N, GEMM_K, "uniform")
+    threads = oracle.max_threads()
+    # size each step so that warm-up + timed steps take about `budget` seconds
+    t0 = time.perf_counter()
+    oracle.gemm_f16_colmajor(A_h, B_h, GEMM_M, GEMM_N, GEMM_K, cols=list(range(threads)))
+    per_batch = time.perf_counter() - t0
+    budget = 150.0
+    batches = max(1, int(budget / max(per_batch, 1e-3) / (args.steps + args.warmup)))
+    cols_per_step = batches * threads
+    for w in range(args.warmup):
+        oracle.gemm_f16_colmajor(A_h, B_h, GEMM_M, GEMM_N, GEMM_K, cols=[(w + i) % GEMM_N for i in range(threads)])
+    times = []
+    for s in range(args.steps):
+        cols = [(s * 131 + i * 977) % GEMM_N for i in range(cols_per_step)]
+        t0 = time.perf_counter()
+        oracle.gemm_f16_colmajor(A_h, B_h, GEMM_M, GEMM_N, GEMM_K, cols=cols)
+        times.append(time.perf_counter() - t0)
+    flops_per_step = 2 * GEMM_M * GEMM_K * cols_per_step
+    value = flops_per_step * len(times) / sum(times) / 1e12
+    sample = (f"{cols_per_step} output columns of the 8192x8192x16384 GEMM per step "
+              f"(each 8192x16384 FMAs in FP64)")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.fmean(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded PCG64)",
+        "config": {"workload": WORKLOAD, "gemm": [GEMM_M, GEMM_N, GEMM_K], "gemv": [GEMV_M, GEMV_K, list(GEMV_NS)],
+                   "parallelism": "host cores"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -14,4 +14,6 @@ from ._native import (  # noqa: F401
     gemv_bf16_enqueue,
     last_error,
     library_path,
+    set_option,
+    stream_check,
 )

@@ -1,0 +1,170 @@
+"""ctypes binding of libbsk (argument marshalling only).
+
+Each function takes CUDA tensors (any 16-bit dtype; only ``data_ptr()`` is
+used) or raw device addresses as ints, plus an optional stream (a
+``torch.cuda.Stream``, a raw ``cudaStream_t`` int, or None for torch's current
+stream), and calls the C entry point of the same name.  A non-zero status
+raises :class:`BskError`.  The library is loaded on first use; if it has not
+been built, the call raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {
+    0: "BSK_OK",
+    1: "BSK_ERR_INVALID_ARG",
+    2: "BSK_ERR_UNSUPPORTED_DEVICE",
+    3: "BSK_ERR_CUDA",
+    4: "BSK_ERR_TIMEOUT",
+    5: "BSK_ERR_NO_MEMORY",
+}
+
+OPTIONS = {
+    "group_m": 1,
+    "block_n": 2,
+    "force_pack": 3,
+    "force_direct_store": 4,
+    "gemv_rows": 5,
+    "gemv_warps": 6,
+    "wait_limit_us": 7,
+    "num_sms": 8,
+}
+
+# Every symbol include/bsk.h declares.
+EXPORTS = (
+    "gemm_f16_colmajor", "gemv_bf16", "bsk_gemm_f16_colmajor_enqueue", "bsk_gemv_bf16_enqueue",
+    "bsk_stream_check", "bsk_last_error", "bsk_status_string", "bsk_version", "bsk_tile_coord",
+    "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout",
+)
+
+
+class BskError(RuntimeError):
+    """A libbsk call returned a non-zero status."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load libbsk.so (raises if it is missing: build it with bf16_gemm_skinny_gb300.build.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libbsk.so not built ({path}); run bf16_gemm_skinny_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        p = ctypes.c_void_p
+        i = ctypes.c_int
+        for name in ("gemm_f16_colmajor", "bsk_gemm_f16_colmajor_enqueue"):
+            getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
+            getattr(lib, name).restype = i
+        for name in ("gemv_bf16", "bsk_gemv_bf16_enqueue"):
+            getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
+            getattr(lib, name).restype = i
+        lib.bsk_stream_check.argtypes = [p]
+        lib.bsk_stream_check.restype = i
+        lib.bsk_last_error.argtypes = []
+        lib.bsk_last_error.restype = ctypes.c_char_p
+        lib.bsk_status_string.argtypes = [i]
+        lib.bsk_status_string.restype = ctypes.c_char_p
+        lib.bsk_version.argtypes = []
+        lib.bsk_version.restype = i
+        lib.bsk_tile_coord.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+        lib.bsk_tile_coord.restype = None
+        lib.bsk_set_option.argtypes = [i, ctypes.c_longlong]
+        lib.bsk_set_option.restype = i
+        lib.bsk_get_option.argtypes = [i]
+        lib.bsk_get_option.restype = ctypes.c_longlong
+        lib.bsk_test_wait_timeout.argtypes = [ctypes.c_uint, p]
+        lib.bsk_test_wait_timeout.restype = i
+        _lib = lib
+        return lib
+
+
+def _addr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def last_error() -> str:
+    return load().bsk_last_error().decode(errors="replace")
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise BskError(status, last_error())
+
+
+def gemm_f16_colmajor(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """C(m,n) = sum_k A(m,k) B(k,n), column-major FP16; blocks until done."""
+    _check(load().gemm_f16_colmajor(_addr(A), _addr(B), _addr(C), M, N, K, _stream(stream)))
+
+
+def gemm_f16_colmajor_enqueue(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """Asynchronous variant of gemm_f16_colmajor (check with stream_check)."""
+    _check(load().bsk_gemm_f16_colmajor_enqueue(_addr(A), _addr(B), _addr(C), M, N, K, _stream(stream)))
+
+
+def gemv_bf16(W, x, y, M: int, K: int, n: int, stream=None) -> None:
+    """y[t, j] = sum_k x[t, k] W[j, k], BF16; blocks until done."""
+    _check(load().gemv_bf16(_addr(W), _addr(x), _addr(y), M, K, n, _stream(stream)))
+
+
+def gemv_bf16_enqueue(W, x, y, M: int, K: int, n: int, stream=None) -> None:
+    """Asynchronous variant of gemv_bf16 (check with stream_check)."""
+    _check(load().bsk_gemv_bf16_enqueue(_addr(W), _addr(x), _addr(y), M, K, n, _stream(stream)))
+
+
+def stream_check(stream=None) -> None:
+    _check(load().bsk_stream_check(_stream(stream)))
+
+
+def tile_coord(t: int, num_m: int, num_n: int, group_m: int):
+    pm, pn = ctypes.c_int(), ctypes.c_int()
+    load().bsk_tile_coord(t, num_m, num_n, group_m, ctypes.byref(pm), ctypes.byref(pn))
+    return pm.value, pn.value
+
+
+def set_option(name: str, value: int) -> None:
+    _check(load().bsk_set_option(OPTIONS[name], int(value)))
+
+
+def get_option(name: str) -> int:
+    return int(load().bsk_get_option(OPTIONS[name]))
+
+
+def version() -> int:
+    return int(load().bsk_version())
+
+
+def test_wait_timeout(limit_us: int, stream=None) -> int:
+    """Runs the watchdog probe; returns the raw status (BSK_ERR_TIMEOUT = 4 expected)."""
+    return int(load().bsk_test_wait_timeout(limit_us, _stream(stream)))

@@ -1,0 +1,413 @@
+// api.cu -- the C ABI of libbsk: argument checks, path choice, workspace,
+// launch, completion and error reporting.  No compute happens here.
+//
+// The host side follows the contract of "MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘",
+// section 3.1 (搭代码框架): one exported entry that checks whether the fast
+// path's layout requirements hold and otherwise takes a prepared path, then
+// synchronises before returning.  Here the fast path is the TMA-fed tcgen05
+// kernel; operands whose layout TMA cannot describe are packed into a
+// workspace first (the same kernel then runs), rather than falling back to a
+// second, slower GEMM.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "bsk.h"
+#include "bsk_internal.h"
+
+namespace {
+
+constexpr int kVersion = 100;   // 0.1.0
+
+thread_local char t_err[1024] = "";
+
+int fail(int status, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int fail_cuda(cudaError_t e, const char* what)
+{
+    return fail(BSK_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ----------------------------------------------------------------------------
+// options
+// ----------------------------------------------------------------------------
+constexpr int kNumOpts = 9;
+std::atomic<long long> g_opt[kNumOpts];
+
+long long opt_or(int key, long long dflt)
+{
+    const long long v = g_opt[key].load(std::memory_order_relaxed);
+    return v != 0 ? v : dflt;
+}
+
+constexpr long long kDefaultWaitLimitUs = 2000000;   // 2 s
+
+// ----------------------------------------------------------------------------
+// per-device state and the device status word
+// ----------------------------------------------------------------------------
+struct DeviceInfo {
+    bool init = false;
+    bool supported = false;
+    int sms = 0;
+    int major = 0, minor = 0;
+};
+
+constexpr int kMaxDevices = 128;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+// Status word written by kernels when a bounded wait gives up: pinned,
+// host-mapped memory, so the host reads it after a stream sync with no copy.
+// Shared by every call of the process: a timeout is reported by the first
+// check (blocking call or bsk_stream_check) that runs after it.
+volatile int* g_status_host = nullptr;
+int* g_status_dev = nullptr;
+
+int prepare_device(int* sms_out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(BSK_ERR_UNSUPPORTED_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.init) {
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail_cuda(e, "cudaDeviceGetAttribute");
+        d.supported = (d.major == 10 && d.minor == 3);
+        d.init = true;
+    }
+    if (!d.supported)
+        return fail(BSK_ERR_UNSUPPORTED_DEVICE, "device %d has compute capability %d.%d; this library is built for 10.3 (sm_103a)",
+                    dev, d.major, d.minor);
+    if (g_status_host == nullptr) {
+        void* h = nullptr;
+        e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaHostAlloc(status word)");
+        std::memset(h, 0, 64);
+        void* dptr = nullptr;
+        e = cudaHostGetDevicePointer(&dptr, h, 0);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaHostGetDevicePointer(status word)");
+        g_status_dev = static_cast<int*>(dptr);
+        g_status_host = static_cast<volatile int*>(h);
+    }
+    long long cap = opt_or(BSK_OPT_NUM_SMS, d.sms);
+    *sms_out = static_cast<int>(cap < d.sms ? cap : d.sms);
+    return BSK_OK;
+}
+
+int check_status_word()
+{
+    if (g_status_host == nullptr) return BSK_OK;
+    const int code = *g_status_host;
+    if (code != 0) {
+        *g_status_host = 0;
+        return fail(BSK_ERR_TIMEOUT, "a device-side wait gave up (site %d); the output is undefined",
+                    code - bsk::kDevErrTimeoutBase);
+    }
+    return BSK_OK;
+}
+
+int sync_and_check(cudaStream_t s)
+{
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    return check_status_word();
+}
+
+// ----------------------------------------------------------------------------
+// helpers
+// ----------------------------------------------------------------------------
+bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes)
+{
+    if (abytes == 0 || bbytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+long long round_up8(long long v) { return (v + 7) / 8 * 8; }
+
+// Stream-ordered workspace for packed operands, freed in stream order after use.
+struct Workspace {
+    void* ptr = nullptr;
+    cudaStream_t s = nullptr;
+    ~Workspace()
+    {
+        if (ptr != nullptr) cudaFreeAsync(ptr, s);
+    }
+};
+
+int alloc_workspace(Workspace& ws, size_t bytes, cudaStream_t s)
+{
+    ws.s = s;
+    cudaError_t e = cudaMallocAsync(&ws.ptr, bytes, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        ws.ptr = nullptr;
+        return fail(BSK_ERR_NO_MEMORY, "cudaMallocAsync(%zu bytes) for the pack workspace failed: %s", bytes,
+                    cudaGetErrorString(e));
+    }
+    return BSK_OK;
+}
+
+// Runs the tcgen05 GEMM on operands in any layout TMA may not take directly.
+// A: M x K (MN-major if a_mn_major, else K-major), B: K-major K x N, C: column-major M x N.
+int run_gemm(const uint16_t* A, bool a_mn_major, const uint16_t* B, uint16_t* C, int M, int N, int K, bool bf16,
+             int sms, cudaStream_t s)
+{
+    const bool force_pack = opt_or(BSK_OPT_FORCE_PACK, 0) != 0;
+    // A's leading dimension: M when MN-major, K when K-major.
+    const long long lda = a_mn_major ? M : K;
+    const long long a_outer = a_mn_major ? K : M;
+    const bool a_ok = !force_pack && aligned16(A) && (lda % 8 == 0);
+    const bool b_ok = !force_pack && aligned16(B) && (K % 8 == 0);
+    const long long lda_p = a_ok ? lda : round_up8(lda);
+    const long long ldb_p = b_ok ? K : round_up8(K);
+    size_t a_bytes = a_ok ? 0 : static_cast<size_t>(lda_p) * a_outer * 2;
+    size_t b_bytes = b_ok ? 0 : static_cast<size_t>(ldb_p) * N * 2;
+    a_bytes = (a_bytes + 255) / 256 * 256;
+
+    Workspace ws;
+    const uint16_t* Ause = A;
+    const uint16_t* Buse = B;
+    char msg[512] = "";
+    if (a_bytes + b_bytes > 0) {
+        int st = alloc_workspace(ws, a_bytes + b_bytes, s);
+        if (st != BSK_OK) return st;
+        uint8_t* base = static_cast<uint8_t*>(ws.ptr);
+        if (!a_ok) {
+            uint16_t* Ap = reinterpret_cast<uint16_t*>(base);
+            if (bsk::launch_pack(A, lda, Ap, lda_p, static_cast<int>(lda), static_cast<int>(a_outer), s, msg,
+                                 sizeof(msg)))
+                return fail(BSK_ERR_CUDA, "%s", msg);
+            Ause = Ap;
+        }
+        if (!b_ok) {
+            uint16_t* Bp = reinterpret_cast<uint16_t*>(base + a_bytes);
+            if (bsk::launch_pack(B, K, Bp, ldb_p, K, N, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
+            Buse = Bp;
+        }
+    }
+
+    bsk::GemmLaunch g;
+    g.A = Ause;
+    g.lda = a_ok ? lda : lda_p;
+    g.a_mn_major = a_mn_major;
+    g.B = Buse;
+    g.ldb = b_ok ? K : ldb_p;
+    g.C = C;
+    g.ldc = M;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.bf16 = bf16;
+    g.block_n = static_cast<int>(opt_or(BSK_OPT_BLOCK_N, 256));
+    g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, 8));
+    g.tma_store = aligned16(C) && (M % 8 == 0) && opt_or(BSK_OPT_FORCE_DIRECT_STORE, 0) == 0;
+    g.num_sms = sms;
+    g.status = g_status_dev;
+    g.wait_limit_ns = static_cast<unsigned long long>(opt_or(BSK_OPT_WAIT_LIMIT_US, kDefaultWaitLimitUs)) * 1000ull;
+    if (bsk::launch_gemm(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
+    return BSK_OK;
+}
+
+int enqueue_gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream)
+{
+    if (M < 0 || N < 0 || K < 0) return fail(BSK_ERR_INVALID_ARG, "negative size (M=%d N=%d K=%d)", M, N, K);
+    if (M == 0 || N == 0) return BSK_OK;
+    const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(K) * N * 2;
+    const size_t c_bytes = static_cast<size_t>(M) * N * 2;
+    if (C == nullptr) return fail(BSK_ERR_INVALID_ARG, "C is NULL");
+    if (K > 0 && (A == nullptr || B == nullptr)) return fail(BSK_ERR_INVALID_ARG, "A or B is NULL");
+    if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes))
+        return fail(BSK_ERR_INVALID_ARG, "C overlaps an input");
+    const long long tiles = ((M + 127LL) / 128) * ((N + 127LL) / 128);
+    if (tiles > INT_MAX) return fail(BSK_ERR_INVALID_ARG, "problem too large (%lld tiles)", tiles);
+    int sms = 0;
+    int st = prepare_device(&sms);
+    if (st != BSK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(C, 0, c_bytes, s);
+        return e == cudaSuccess ? BSK_OK : fail_cuda(e, "cudaMemsetAsync");
+    }
+    return run_gemm(A, true, B, C, M, N, K, false, sms, s);
+}
+
+int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream)
+{
+    if (M < 0 || K < 0 || n < 0) return fail(BSK_ERR_INVALID_ARG, "negative size (M=%d K=%d n=%d)", M, K, n);
+    if (M == 0 || n == 0) return BSK_OK;
+    const size_t w_bytes = static_cast<size_t>(M) * K * 2, x_bytes = static_cast<size_t>(n) * K * 2;
+    const size_t y_bytes = static_cast<size_t>(n) * M * 2;
+    if (y == nullptr) return fail(BSK_ERR_INVALID_ARG, "y is NULL");
+    if (K > 0 && (W == nullptr || x == nullptr)) return fail(BSK_ERR_INVALID_ARG, "W or x is NULL");
+    if (overlaps(y, y_bytes, W, w_bytes) || overlaps(y, y_bytes, x, x_bytes))
+        return fail(BSK_ERR_INVALID_ARG, "y overlaps an input");
+    const long long tiles = ((M + 127LL) / 128) * ((n + 127LL) / 128);
+    if (tiles > INT_MAX) return fail(BSK_ERR_INVALID_ARG, "problem too large (%lld tiles)", tiles);
+    int sms = 0;
+    int st = prepare_device(&sms);
+    if (st != BSK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, y_bytes, s);
+        return e == cudaSuccess ? BSK_OK : fail_cuda(e, "cudaMemsetAsync");
+    }
+    if (n <= 8) {
+        bsk::GemvLaunch g;
+        g.W = W;
+        g.x = x;
+        g.y = y;
+        g.M = M;
+        g.K = K;
+        g.n = n;
+        g.rows_per_warp = static_cast<int>(opt_or(BSK_OPT_GEMV_ROWS, 0));
+        g.warps_per_block = static_cast<int>(opt_or(BSK_OPT_GEMV_WARPS, 0));
+        g.num_sms = sms;
+        char msg[512] = "";
+        if (bsk::launch_gemv(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
+        return BSK_OK;
+    }
+    // Prefill: Y^T (M x n, column-major == y row-major) = W (K-major) * x^T (K-major).
+    return run_gemm(W, false, x, y, M, n, K, true, sms, s);
+}
+
+}  // namespace
+
+namespace bsk {
+
+TmapEncodeFn tmap_encoder()
+{
+    static TmapEncodeFn fn = []() -> TmapEncodeFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<TmapEncodeFn>(p);
+    }();
+    return fn;
+}
+
+}  // namespace bsk
+
+extern "C" {
+
+int gemm_f16_colmajor(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream)
+{
+    int st = enqueue_gemm_f16(A, B, C, M, N, K, stream);
+    if (st != BSK_OK) return st;
+    if (M == 0 || N == 0) return BSK_OK;
+    return sync_and_check(static_cast<cudaStream_t>(stream));
+}
+
+int gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream)
+{
+    int st = enqueue_gemv_bf16(W, x, y, M, K, n, stream);
+    if (st != BSK_OK) return st;
+    if (M == 0 || n == 0) return BSK_OK;
+    return sync_and_check(static_cast<cudaStream_t>(stream));
+}
+
+int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
+                                  void* stream)
+{
+    return enqueue_gemm_f16(A, B, C, M, N, K, stream);
+}
+
+int bsk_gemv_bf16_enqueue(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream)
+{
+    return enqueue_gemv_bf16(W, x, y, M, K, n, stream);
+}
+
+int bsk_stream_check(void* stream)
+{
+    return sync_and_check(static_cast<cudaStream_t>(stream));
+}
+
+const char* bsk_last_error(void) { return t_err; }
+
+const char* bsk_status_string(int status)
+{
+    switch (status) {
+    case BSK_OK: return "BSK_OK";
+    case BSK_ERR_INVALID_ARG: return "BSK_ERR_INVALID_ARG";
+    case BSK_ERR_UNSUPPORTED_DEVICE: return "BSK_ERR_UNSUPPORTED_DEVICE";
+    case BSK_ERR_CUDA: return "BSK_ERR_CUDA";
+    case BSK_ERR_TIMEOUT: return "BSK_ERR_TIMEOUT";
+    case BSK_ERR_NO_MEMORY: return "BSK_ERR_NO_MEMORY";
+    default: return "BSK_ERR_UNKNOWN";
+    }
+}
+
+int bsk_version(void) { return kVersion; }
+
+void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* pid_n)
+{
+    int pm = -1, pn = -1;
+    if (num_m > 0 && num_n > 0 && group_m > 0 && t >= 0 && static_cast<long long>(num_m) * num_n > t)
+        bsk::tile_coord(t, num_m, num_n, group_m, &pm, &pn);
+    if (pid_m) *pid_m = pm;
+    if (pid_n) *pid_n = pn;
+}
+
+int bsk_set_option(int key, long long value)
+{
+    if (key < 1 || key >= kNumOpts) return fail(BSK_ERR_INVALID_ARG, "unknown option key %d", key);
+    bool ok = true;
+    switch (key) {
+    case BSK_OPT_GROUP_M: ok = value >= 0 && value <= 65536; break;
+    case BSK_OPT_BLOCK_N: ok = value == 0 || value == 128 || value == 256; break;
+    case BSK_OPT_FORCE_PACK:
+    case BSK_OPT_FORCE_DIRECT_STORE: ok = value == 0 || value == 1; break;
+    case BSK_OPT_GEMV_ROWS: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8; break;
+    case BSK_OPT_GEMV_WARPS: ok = value >= 0 && value <= 8; break;
+    case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
+    case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
+    default: ok = false;
+    }
+    if (!ok) return fail(BSK_ERR_INVALID_ARG, "value %lld out of range for option %d", value, key);
+    g_opt[key].store(value, std::memory_order_relaxed);
+    return BSK_OK;
+}
+
+long long bsk_get_option(int key)
+{
+    if (key < 1 || key >= kNumOpts) return -1;
+    return g_opt[key].load(std::memory_order_relaxed);
+}
+
+int bsk_test_wait_timeout(unsigned int limit_us, void* stream)
+{
+    if (limit_us < 1 || limit_us > 10000000u) return fail(BSK_ERR_INVALID_ARG, "limit_us out of range");
+    int sms = 0;
+    int st = prepare_device(&sms);
+    if (st != BSK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = sync_and_check(s);   // start from a clean status word
+    if (st != BSK_OK) return st;
+    char msg[512] = "";
+    if (bsk::launch_wait_timeout_probe(g_status_dev, static_cast<unsigned long long>(limit_us) * 1000ull, s, msg,
+                                       sizeof(msg)))
+        return fail(BSK_ERR_CUDA, "%s", msg);
+    return sync_and_check(s);
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// aux_kernels.cu -- the operand pack kernel and the bounded-wait test probe.
+#include <cstdio>
+
+#include "bsk_internal.h"
+#include "ptx.cuh"
+
+namespace bsk {
+namespace {
+
+// dst[i + j*ld_dst] = src[i + j*ld_src] for i < inner, j < outer.  The TMA
+// needs 16-byte aligned bases and leading dimensions; the pack gives unaligned
+// operands that shape in a workspace without touching the caller's buffers
+// ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 1: inputs may not be modified).
+__global__ void __launch_bounds__(256)
+    pack_16bit_kernel(const uint16_t* __restrict__ src, long long ld_src, uint16_t* __restrict__ dst,
+                      long long ld_dst, int inner, int outer)
+{
+    const long long total = static_cast<long long>(inner) * outer;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+        const long long j = e / inner;
+        const long long i = e - j * inner;
+        dst[i + j * ld_dst] = src[i + j * ld_src];
+    }
+}
+
+// One CTA waits on an mbarrier that nobody arrives on.  The wait is the
+// GEMM's bounded wait; it must give up after limit_ns and record a timeout.
+__global__ void wait_timeout_probe_kernel(int* status, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const WaitCtl wc{&abort_flag, status, limit_ns};
+        mbar_wait(smem_u32(&bar), 0u, wc, 0x7F);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long ld_dst, int inner, int outer,
+                cudaStream_t stream, char* msg, size_t msg_len)
+{
+    const long long total = static_cast<long long>(inner) * outer;
+    if (total <= 0) return 0;
+    long long grid = (total + 255) / 256;
+    if (grid > 4096) grid = 4096;
+    pack_16bit_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(src, ld_src, dst, ld_dst, inner, outer);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
+        return 1;
+    }
+    return 0;
+}
+
+int launch_wait_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t stream, char* msg,
+                              size_t msg_len)
+{
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "probe launch failed: %s", cudaGetErrorString(e));
+        return 1;
+    }
+    return 0;
+}
+
+}  // namespace bsk

@@ -1,0 +1,92 @@
+// bsk_internal.h -- declarations shared by the library's translation units
+// (not installed, not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bsk {
+
+// Code a kernel writes into the device status word when a bounded wait gives
+// up: kDevErrTimeoutBase + the number of the wait site (0 = no error).
+constexpr int kDevErrTimeoutBase = 0x100;
+
+// Grouped ordering of output tiles ("Hygon 优化", section 分组调度：提高 L2 数据复用):
+// the 2-D grid of num_m x num_n tiles is flattened so that consecutive tile
+// indices walk down a group of `group_m` tile rows before moving to the next
+// tile column; tiles that share a column of B (and a row of A within the
+// group) run close together in time and hit in L2.  The last group holds the
+// remaining num_m mod group_m rows.
+__host__ __device__ inline void tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* pid_n)
+{
+    const int per_group = group_m * num_n;
+    const int group = t / per_group;
+    const int first_m = group * group_m;
+    const int rows_left = num_m - first_m;
+    const int group_rows = rows_left < group_m ? rows_left : group_m;
+    const int r = t - group * per_group;
+    *pid_m = first_m + r % group_rows;
+    *pid_n = r / group_rows;
+}
+
+using TmapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver (resolved once through the runtime).
+TmapEncodeFn tmap_encoder();
+
+// Launch of the tcgen05 GEMM: C (M x N, column-major, m contiguous, leading
+// dimension ldc) = A (M x K) * B (K x N), FP32 accumulation, FP16 or BF16 in/out.
+// A is either MN-major (A(m,k) at A[m + k*lda]) or K-major (A(m,k) at
+// A[k + m*lda]); B is K-major (B(k,n) at B[k + n*ldb]).  A and B must be
+// 16-byte aligned with 16-byte-multiple leading dimensions (the caller packs
+// them otherwise).
+struct GemmLaunch {
+    const void* A;
+    long long lda;
+    bool a_mn_major;
+    const void* B;
+    long long ldb;
+    void* C;
+    long long ldc;
+    int M, N, K;
+    bool bf16;
+    int block_n;    // 128 or 256
+    int group_m;    // >= 1
+    bool tma_store; // C 16-byte aligned with 16-byte-multiple ldc
+    int num_sms;    // persistent grid size cap
+    int* status;    // device status word
+    unsigned long long wait_limit_ns;
+};
+
+// Returns 0 on success; otherwise an error message is written to `msg`.
+int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
+
+// Decode GEMV / skinny GEMM on the CUDA cores: y[t, j] = sum_k x[t, k] W[j, k]
+// for t < n <= 8, W [M, K] row-major, x [n, K], y [n, M] row-major, BF16.
+struct GemvLaunch {
+    const uint16_t* W;
+    const uint16_t* x;
+    uint16_t* y;
+    int M, K, n;
+    int rows_per_warp;    // 0 = default for n
+    int warps_per_block;  // 0 = default
+    int num_sms;
+};
+int launch_gemv(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
+
+// Copy an `outer` x `inner` matrix of 16-bit elements (inner contiguous) from
+// leading dimension ld_src to ld_dst.  The source is only read.
+int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long ld_dst, int inner, int outer,
+                cudaStream_t stream, char* msg, size_t msg_len);
+
+// Test hook: one CTA waits on an mbarrier that nothing completes, with the same
+// bounded wait the GEMM uses; it must give up after `limit_ns` and record a
+// timeout in the status word.
+int launch_wait_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t stream, char* msg,
+                              size_t msg_len);
+
+}  // namespace bsk

@@ -1,0 +1,424 @@
+// gemm_tcgen05.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// Computes C = A * B with FP32 accumulation in tensor memory and one rounding
+// to FP16 or BF16 in the epilogue ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘",
+// section 1: FP16 in, FP32 accumulate, FP16 out; section 2: the column-major
+// addressing A(m,k) = A[m + k*M], B(k,n) = B[k + n*K], C(m,n) = C[m + n*M]).
+//
+// Structure (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-slices
+//               ("Hygon 优化", section 软件流水线: overlap the k-loop loads with
+//               the MMAs; the per-stage bytes are (BM + BN) * BK * 2).
+//   warp 1      allocates TMEM and issues tcgen05.mma from one thread; each
+//               stage's smem slot is released by tcgen05.commit when its MMAs
+//               have read it.
+//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator, rounding to
+//               16 bits, store to C (TMA store, or masked stores when C's
+//               leading dimension is not a multiple of 16 bytes).  There is no
+//               FP32 intermediate matrix and no separate conversion kernel.
+// The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
+// of tile i overlaps the mainloop of tile i+1.  Tiles are visited in the
+// grouped (GROUP_M) order of "Hygon 优化", section 分组调度.
+//
+// Tails: TMA zero-fills the parts of a box outside the tensor (M, N and K
+// tails contribute zero products) and the TMA store / masked store drop rows
+// and columns outside C ("Hygon 优化", section DUMMA 矩阵指令形状, on tail masks).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdio>
+
+#include "bsk_internal.h"
+#include "ptx.cuh"
+
+namespace bsk {
+namespace {
+
+constexpr int kBM = 128;      // tile rows (TMEM lanes), one MMA of M = 128
+constexpr int kBK = 64;       // k per stage: one 128-byte swizzle row of 16-bit values
+constexpr int kUmmaK = 16;    // k per tcgen05.mma of kind::f16
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBox = 32;   // epilogue chunk: 32 rows x 32 columns per warp
+
+template <int BN>
+struct Cfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kABytes = kBM * kBK * 2;
+    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kEpiBufBytes = kEpiBox * kEpiBox * 2;
+    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
+    static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area too small");
+    static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+};
+
+struct Params {
+    int M, N, K;
+    int num_m, num_n, num_tiles, num_kb;
+    int group_m;
+    void* C;
+    long long ldc;
+    int tma_store;
+    int* status;
+    unsigned long long wait_limit_ns;
+};
+
+// Identifiers of the waits, reported in the status word on a timeout.
+enum WaitSite {
+    kSiteProducerEmpty = 1,
+    kSiteMmaTmemEmpty = 2,
+    kSiteMmaFull = 3,
+    kSiteEpilogueTmemFull = 4,
+    kSiteMmaDrain = 5,
+    kSiteProducerDrain = 6,
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t round_out(uint32_t acc_bits)
+{
+    const float v = __uint_as_float(acc_bits);
+    if constexpr (BF16) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    } else {
+        return __half_as_ushort(__float2half_rn(v));
+    }
+}
+
+template <int BN, bool A_MN, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const Params p)
+{
+    using Cf = Cfg<BN>;
+    constexpr int S = Cf::kStages;
+    constexpr uint32_t kIdesc = idesc_f16(BF16, A_MN, false, kBM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + S * Cf::kABytes;
+    uint8_t* sEpi = sB + S * Cf::kBBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + Cf::kEpiBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cf::kNumBars);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t full0 = smem_u32(bars);            // S barriers: stage loaded
+    const uint32_t empty0 = full0 + 8 * S;            // S barriers: stage consumed
+    const uint32_t tfull0 = empty0 + 8 * S;           // 2 barriers: accumulator ready
+    const uint32_t tempty0 = tfull0 + 16;             // 2 barriers: accumulator drained
+    const uint32_t drain_bar = tempty0 + 16;          // abort path: MMAs finished
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        if (p.tma_store) prefetch_tmap(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cf::kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
+    // Waits on the abort path ignore the abort flag but keep the time limit.
+    uint32_t never = 0u;
+    const WaitCtl wc_drain{&never, p.status, p.wait_limit_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------
+        // TMA producer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                int pm, pn;
+                tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
+                const int m0 = pm * kBM;
+                const int n0 = pn * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_arrive_expect_tx(fb, Cf::kStageBytes);
+                    const uint32_t a_dst = smem_u32(sA + stage * Cf::kABytes);
+                    const uint32_t b_dst = smem_u32(sB + stage * Cf::kBBytes);
+                    const int k0 = kb * kBK;
+                    if constexpr (A_MN) {
+                        // two 64(m) x 64(k) boxes: m is the 128-byte swizzle row
+                        tma_load_2d(a_dst, &tmA, fb, m0, k0);
+                        tma_load_2d(a_dst + Cf::kABytes / 2, &tmA, fb, m0 + 64, k0);
+                    } else {
+                        tma_load_2d(a_dst, &tmA, fb, k0, m0);   // 64(k) x 128(m) box
+                    }
+                    tma_load_2d(b_dst, &tmB, fb, k0, n0);        // 64(k) x BN(n) box
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Abort: let the loads already issued land before the CTA can exit.
+                const long long pending = issued < S ? issued : S;
+                for (long long j = 1; j <= pending; ++j) {
+                    const int s = (stage - static_cast<int>(j) + S) % S;
+                    const uint32_t ph = (stage - static_cast<int>(j) < 0) ? (phase ^ 1u) : phase;
+                    mbar_wait(full0 + 8 * s, ph, wc_drain, kSiteProducerDrain);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------
+        // MMA issuer (one thread)
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            bool issued_any = false;
+            int it = 0;
+            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+                if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_base = smem_u32(sA + stage * Cf::kABytes);
+                    const uint32_t b_base = smem_u32(sB + stage * Cf::kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        // MN-major A: 16 k-rows of 128 bytes per MMA, the two 64-element
+                        // m blocks 8 KB apart; K-major operands: 32 bytes along the row.
+                        const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, Cf::kABytes / 2, 1024)
+                                                 : smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                        mma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(empty0 + 8 * stage);
+                    issued_any = true;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull0 + 8 * acc);
+            }
+            if (!ok && issued_any) {
+                // Abort: every MMA issued so far must finish before TMEM is freed.
+                mma_commit(drain_bar);
+                mbar_wait(drain_bar, 0u, wc_drain, kSiteMmaDrain);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------
+        // Epilogue: TMEM -> registers -> 16-bit -> C
+        // ------------------------------------------------------------------
+        const int quarter = warp & 3;             // TMEM lanes this warp may read
+        const int ew = warp - 2;                  // owner of a staging buffer pair
+        uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
+        uint16_t* Cg = reinterpret_cast<uint16_t*>(p.C);
+        int it = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+            bool ok = mbar_wait(tfull0 + 8 * acc, aph, wc, kSiteEpilogueTmemFull);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            int pm, pn;
+            tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
+            const int m0 = pm * kBM + quarter * 32;
+            const int n0 = pn * BN;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + c * 32, r);
+                tmem_ld_wait();
+                if (c == BN / 32 - 1) {
+                    // all of this accumulator is in registers: hand TMEM back to the MMA warp
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+                }
+                if (p.tma_store) {
+                    uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
+                    if (lane == 0) bulk_wait_group_read<1>();   // the store that used `buf` has read it
+                    __syncwarp();
+                    uint16_t* b16 = reinterpret_cast<uint16_t*>(buf);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) b16[j * 32 + lane] = round_out<BF16>(r[j]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, smem_u32(buf), m0, n0 + c * 32);
+                        bulk_commit_group();
+                    }
+                } else {
+                    const int m = m0 + lane;
+                    if (m < p.M) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int n = n0 + c * 32 + j;
+                            if (n < p.N) Cg[static_cast<long long>(m) + static_cast<long long>(n) * p.ldc] =
+                                round_out<BF16>(r[j]);
+                        }
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cf::kTmemCols);
+    }
+}
+
+bool encode_2d(CUtensorMap* map, bool bf16, const void* base, unsigned long long dim0, unsigned long long dim1,
+               unsigned long long stride1_bytes, unsigned box0, unsigned box1, CUtensorMapSwizzle swz, char* msg,
+               size_t msg_len)
+{
+    TmapEncodeFn enc = tmap_encoder();
+    if (enc == nullptr) {
+        snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride1_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (%d) for dims %llu x %llu, stride %llu B, box %u x %u",
+                 static_cast<int>(r), dim0, dim1, stride1_bytes, box0, box1);
+        return false;
+    }
+    return true;
+}
+
+template <int BN, bool A_MN, bool BF16>
+int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
+{
+    using Cf = Cfg<BN>;
+    CUtensorMap tmA, tmB, tmC;
+    if (A_MN) {
+        if (!encode_2d(&tmA, BF16, g.A, g.M, g.K, g.lda * 2ull, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+            return 1;
+    } else {
+        if (!encode_2d(&tmA, BF16, g.A, g.K, g.M, g.lda * 2ull, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+            return 1;
+    }
+    if (!encode_2d(&tmB, BF16, g.B, g.K, g.N, g.ldb * 2ull, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+        return 1;
+    if (g.tma_store) {
+        if (!encode_2d(&tmC, BF16, g.C, g.M, g.N, g.ldc * 2ull, kEpiBox, kEpiBox, CU_TENSOR_MAP_SWIZZLE_NONE, msg,
+                       msg_len))
+            return 1;
+    } else {
+        tmC = tmA;   // unused by the kernel
+    }
+
+    Params p;
+    p.M = g.M;
+    p.N = g.N;
+    p.K = g.K;
+    p.num_m = (g.M + kBM - 1) / kBM;
+    p.num_n = (g.N + BN - 1) / BN;
+    p.num_tiles = p.num_m * p.num_n;
+    p.num_kb = (g.K + kBK - 1) / kBK;
+    p.group_m = g.group_m < 1 ? 1 : g.group_m;
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.tma_store = g.tma_store ? 1 : 0;
+    p.status = g.status;
+    p.wait_limit_ns = g.wait_limit_ns;
+
+    auto kern = gemm_tcgen05_kernel<BN, A_MN, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return 1;
+    }
+    const int grid = p.num_tiles < g.num_sms ? p.num_tiles : g.num_sms;
+    kern<<<grid, kThreads, Cf::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "GEMM launch failed: %s", cudaGetErrorString(e));
+        return 1;
+    }
+    return 0;
+}
+
+}  // namespace
+
+int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
+{
+    if (g.block_n == 256) {
+        if (g.a_mn_major)
+            return g.bf16 ? launch_instance<256, true, true>(g, stream, msg, msg_len)
+                          : launch_instance<256, true, false>(g, stream, msg, msg_len);
+        return g.bf16 ? launch_instance<256, false, true>(g, stream, msg, msg_len)
+                      : launch_instance<256, false, false>(g, stream, msg, msg_len);
+    }
+    if (g.block_n == 128) {
+        if (g.a_mn_major)
+            return g.bf16 ? launch_instance<128, true, true>(g, stream, msg, msg_len)
+                          : launch_instance<128, true, false>(g, stream, msg, msg_len);
+        return g.bf16 ? launch_instance<128, false, true>(g, stream, msg, msg_len)
+                      : launch_instance<128, false, false>(g, stream, msg, msg_len);
+    }
+    snprintf(msg, msg_len, "unsupported block_n %d (128 or 256)", g.block_n);
+    return 1;
+}
+
+}  // namespace bsk

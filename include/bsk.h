@@ -1,0 +1,149 @@
+/*
+ * bsk.h -- C ABI of libbsk: half-precision GEMM with FP32 accumulation on one
+ * NVIDIA GB300 (sm_103a), in two regimes:
+ *
+ *   gemm_f16_colmajor  large column-major FP16 GEMM on the tcgen05 tensor cores;
+ *   gemv_bf16          BF16 linear layer y = x W^T: the HBM-bound decode GEMV for
+ *                      n <= 8 tokens (CUDA cores), the tensor-core GEMM for
+ *                      larger n (prefill projections).
+ *
+ * Conventions shared by every call:
+ *  - Matrix pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors) to
+ *    16-bit values stored as raw bit patterns (IEEE binary16 or bfloat16).
+ *    The caller owns every buffer; the library never writes an input.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - The blocking calls return only when their work on `stream` is complete
+ *    (they synchronise that stream), so results may be read right away.
+ *    The *_enqueue variants only launch; call bsk_stream_check() later.
+ *  - Return value: a bsk_status code (0 = success).  On failure nothing has
+ *    been written to the output unless the status is BSK_ERR_CUDA or
+ *    BSK_ERR_TIMEOUT, and bsk_last_error() describes the failure.
+ *  - Sizes are `int` (the signature of the original contract); every size
+ *    must be >= 0.  A zero output extent is a no-op; K == 0 writes +0.0
+ *    to every output element (the empty sum).
+ *  - Only devices of compute capability 10.3 are supported; there is no CPU
+ *    fallback and no other backend.
+ */
+#ifndef BSK_H
+#define BSK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bsk_status {
+    BSK_OK = 0,
+    BSK_ERR_INVALID_ARG = 1,        /* bad size, null pointer, or an output overlapping an input */
+    BSK_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
+    BSK_ERR_CUDA = 3,               /* a CUDA runtime/driver call or a launch failed */
+    BSK_ERR_TIMEOUT = 4,            /* a device-side wait gave up (watchdog); output undefined */
+    BSK_ERR_NO_MEMORY = 5           /* the pack workspace could not be allocated */
+} bsk_status;
+
+/*
+ * C = A * B, column-major FP16, FP32 accumulation, FP16 output rounded to
+ * nearest even.  Definition: "MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘",
+ * section 2 (GEMM入门): C(m,n) = sum_k A(m,k) B(k,n), with
+ *     A(m,k) = A[m + k*M]   (M x K, leading dimension M)
+ *     B(k,n) = B[k + n*K]   (K x N, leading dimension K)
+ *     C(m,n) = C[m + n*M]   (M x N, leading dimension M)
+ * and section 1 (规则分析): FP16 in, FP32 accumulate, FP16 out, inputs left
+ * unmodified, computation complete on return, no BLAS library.
+ *
+ * Any M, N, K >= 0 are accepted.  When A or B is not 16-byte aligned or its
+ * leading dimension is not a multiple of 8 elements, the operand is first
+ * copied into a library-owned, stream-ordered workspace with a padded leading
+ * dimension (BSK_ERR_NO_MEMORY if that allocation fails).  C may have any
+ * alignment.  C must not overlap A or B (BSK_ERR_INVALID_ARG).
+ */
+int gemm_f16_colmajor(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream);
+
+/*
+ * y = x W^T in BF16 with FP32 accumulation, output rounded to nearest even.
+ * Definition: DCU decode-GEMV article (forum.sourcefind.cn), section 6.1:
+ *     W : [M, K] row-major   W(j,k) = W[j*K + k]   (weights, output features x input features)
+ *     x : [n, K] row-major   x(t,k) = x[t*K + k]   (n tokens)
+ *     y : [n, M] row-major   y(t,j) = y[t*M + j] = sum_k x(t,k) W(j,k)
+ * Section 2: n = 1 is the decode GEMV, large n the prefill GEMM.
+ *
+ * n <= 8 runs the CUDA-core GEMV (128-bit weight stream, warp-shuffle
+ * reduction); n > 8 runs the tcgen05 GEMM with both operands K-major.
+ * Any M, K, n >= 0 are accepted (unaligned W/x or K % 8 != 0 take slower
+ * variants, or the pack workspace for n > 8).  y must not overlap W or x.
+ */
+int gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);
+
+/*
+ * Same work as gemm_f16_colmajor / gemv_bf16, but asynchronous: validates the
+ * arguments, launches on `stream` and returns without waiting.  A device-side
+ * watchdog timeout raised by this work is reported by the next
+ * bsk_stream_check() (or the next blocking call).  Buffers must stay alive
+ * until the stream has passed this work.
+ */
+int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
+                                  void* stream);
+int bsk_gemv_bf16_enqueue(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);
+
+/* Synchronise `stream`, then report BSK_ERR_CUDA for a pending CUDA error or
+ * BSK_ERR_TIMEOUT if a device-side wait gave up since the last check. */
+int bsk_stream_check(void* stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char* bsk_last_error(void);
+
+/* Short name of a status code. */
+const char* bsk_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int bsk_version(void);
+
+/*
+ * Tile order of the GEMM ("Hygon 优化", section 分组调度：提高 L2 数据复用):
+ * maps the flattened tile index t of a num_m x num_n tile grid to its tile
+ * coordinates, visiting group_m tile rows per tile column, the last group
+ * holding the remaining rows.  Host-side copy of the function the kernel
+ * uses; needs no GPU.  Invalid arguments give (-1, -1).
+ */
+void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* pid_n);
+
+/*
+ * Tuning and test options (process-wide; not thread-safe; 0 restores the
+ * default).  Keys:
+ *   BSK_OPT_GROUP_M          GEMM tile-row group size (default 8)
+ *   BSK_OPT_BLOCK_N          GEMM tile width, 128 or 256 (default 256)
+ *   BSK_OPT_FORCE_PACK       1: pack A and B even when aligned
+ *   BSK_OPT_FORCE_DIRECT_STORE 1: masked register stores instead of the TMA store
+ *   BSK_OPT_GEMV_ROWS        GEMV rows of W per warp: 1, 2, 4 or 8 (default by n)
+ *   BSK_OPT_GEMV_WARPS       GEMV warps per CTA, 1..8 (default 8)
+ *   BSK_OPT_WAIT_LIMIT_US    device-side wait limit in microseconds (default 2 s)
+ *   BSK_OPT_NUM_SMS          cap on the persistent GEMM grid (default: all SMs)
+ * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
+ */
+enum {
+    BSK_OPT_GROUP_M = 1,
+    BSK_OPT_BLOCK_N = 2,
+    BSK_OPT_FORCE_PACK = 3,
+    BSK_OPT_FORCE_DIRECT_STORE = 4,
+    BSK_OPT_GEMV_ROWS = 5,
+    BSK_OPT_GEMV_WARPS = 6,
+    BSK_OPT_WAIT_LIMIT_US = 7,
+    BSK_OPT_NUM_SMS = 8
+};
+int bsk_set_option(int key, long long value);
+long long bsk_get_option(int key);
+
+/*
+ * Test hook for the watchdog: launches one CTA that waits on a barrier that
+ * nothing completes, using the GEMM's bounded wait with a limit of
+ * `limit_us` microseconds (1 .. 10,000,000).  Returns BSK_ERR_TIMEOUT when the
+ * wait gave up as designed, BSK_OK never.  Blocks until the probe finished.
+ */
+int bsk_test_wait_timeout(unsigned int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSK_H */

@@ -1,0 +1,197 @@
+"""GPU parity of gemm_f16_colmajor against the oracle (called through the C ABI).
+
+Random inputs: the tolerance in helpers.check_tolerance.  Integer-valued
+inputs (entries in {-2..2}): bit-identical to the oracle.  Every call also
+checks that the output was fully overwritten (it starts as NaN), that the
+guard words after it are untouched and that the inputs are unchanged.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from bf16_gemm_skinny_gb300 import _native as bsk
+from bf16_gemm_skinny_gb300 import build as bsk_build
+from bf16_gemm_skinny_gb300 import inputs
+from helpers import (CANARY, FP16_NAN, absmax_f16, check_tolerance, from_dev, poisoned, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def operands(M, N, K, dist):
+    key = (M, N, K, dist)
+    if key not in _CACHE:
+        seeds = (11, 12) if dist == "int2" else (1, 2)
+        _CACHE[key] = inputs.gemm_operands(M, N, K, dist, *seeds)
+    return _CACHE[key]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+
+    bsk_build.build()
+    oracle.build()
+    torch.cuda.init()
+    yield bsk.load()
+    for k in bsk.OPTIONS:
+        bsk.set_option(k, 0)
+
+
+def run(A, B, M, N, K, offset=0, enqueue=False):
+    """Runs the GEMM on device copies of A, B; returns C's bits.  offset > 0
+    shifts all three device pointers by that many elements (unaligned bases)."""
+    import torch
+
+    Ad = to_dev(np.concatenate([np.zeros(offset, np.uint16), A]))[offset:]
+    Bd = to_dev(np.concatenate([np.zeros(offset, np.uint16), B]))[offset:]
+    buf, _ = poisoned(M * N + offset, FP16_NAN)
+    C = buf[offset:offset + M * N]
+    if enqueue:
+        bsk.gemm_f16_colmajor_enqueue(Ad, Bd, C, M, N, K)
+        bsk.stream_check()
+    else:
+        bsk.gemm_f16_colmajor(Ad, Bd, C, M, N, K)
+    torch.cuda.synchronize()
+    assert np.all(from_dev(buf[offset + M * N:]) == CANARY), "guard words after C were written"
+    assert np.array_equal(from_dev(Ad), A), "A was modified"
+    assert np.array_equal(from_dev(Bd), B), "B was modified"
+    return from_dev(C)
+
+
+SMALL_SHAPES = [
+    (256, 256, 256),      # the 256^3 workload
+    (1, 1, 1), (1, 300, 17), (17, 33, 19), (8, 8, 8), (64, 64, 64),
+    (128, 256, 64), (129, 257, 65), (127, 1, 63), (300, 517, 200), (1000, 777, 1030), (640, 520, 4096),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_SHAPES)
+def test_integer_inputs_bit_exact(M, N, K):
+    A, B = operands(M, N, K, "int2")
+    got = run(A, B, M, N, K)
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    assert np.array_equal(got, want), f"{int((got != want).sum())} of {got.size} entries differ"
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_SHAPES)
+def test_random_inputs_within_tolerance(M, N, K):
+    dist = "uniform" if (M, N, K) == (256, 256, 256) else "normal0.5"
+    A, B = operands(M, N, K, dist)
+    got = run(A, B, M, N, K)
+    ref, _ = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    check_tolerance(got, ref, "f16", K, absmax_f16(A), absmax_f16(B), f"{M}x{N}x{K}")
+
+
+def sampled_check(got, A, B, M, N, K, cols, rows, integer):
+    refc, outc = oracle.gemm_f16_colmajor(A, B, M, N, K, cols=cols)
+    got_c = np.concatenate([got[n * M:(n + 1) * M] for n in cols])
+    refr, outr = oracle.gemm_f16_colmajor_rows(A, B, M, N, K, rows)
+    got_r = np.concatenate([got[np.arange(N) * M + m] for m in rows])
+    # oracle rows come column-major over the selected rows: entry (i, n) at i + n*len(rows)
+    refr = refr.reshape(N, len(rows)).T.reshape(-1)
+    outr = outr.reshape(N, len(rows)).T.reshape(-1)
+    if integer:
+        assert np.array_equal(got_c, outc)
+        assert np.array_equal(got_r, outr)
+    else:
+        check_tolerance(got_c, refc, "f16", K, absmax_f16(A), absmax_f16(B), "sampled columns")
+        check_tolerance(got_r, refr, "f16", K, absmax_f16(A), absmax_f16(B), "sampled rows")
+
+
+@pytest.mark.parametrize("dist", ["normal0.5", "int2"])
+def test_ragged_4095x4097x4100(dist):
+    """Tails in M, N and K, unaligned leading dimensions (pack + masked stores),
+    and a GROUP_M remainder group (32 tile rows, group 12)."""
+    M, N, K = 4095, 4097, 4100
+    A, B = operands(M, N, K, dist)
+    bsk.set_option("group_m", 12)
+    try:
+        got = run(A, B, M, N, K)
+    finally:
+        bsk.set_option("group_m", 0)
+    cols = [0, 1, 255, 256, 2047, 4095, 4096]
+    rows = [0, 127, 128, 2049, 4094]
+    sampled_check(got, A, B, M, N, K, cols, rows, dist == "int2")
+    if dist == "int2":
+        # every sum is an integer below 2^24: the exact product, full output
+        a = oracle.f16_decode(A).reshape(K, M).T
+        b = oracle.f16_decode(B).reshape(N, K).T
+        want = oracle.f16_encode((a @ b).T.reshape(-1))
+        assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("dist", ["uniform", "int2"])
+def test_8192x8192x16384_sampled(dist):
+    """The headline shape, in the launch configuration the benchmark times."""
+    M, N, K = 8192, 8192, 16384
+    A, B = operands(M, N, K, dist)
+    got = run(A, B, M, N, K)
+    assert np.all(np.isfinite(oracle.f16_decode(got[::997])))
+    cols = [0, 255, 256, 4099, 8191]
+    rows = [0, 127, 128, 5000, 8191]
+    sampled_check(got, A, B, M, N, K, cols, rows, dist == "int2")
+
+
+@pytest.mark.parametrize("block_n,group_m", [(256, 8), (128, 1), (128, 12), (256, 3), (256, 1)])
+def test_result_independent_of_tile_config(block_n, group_m):
+    M, N, K = 1000, 777, 1030
+    A, B = operands(M, N, K, "int2")
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    bsk.set_option("block_n", block_n)
+    bsk.set_option("group_m", group_m)
+    try:
+        got = run(A, B, M, N, K)
+    finally:
+        bsk.set_option("block_n", 0)
+        bsk.set_option("group_m", 0)
+    assert np.array_equal(got, want)
+
+
+def test_deterministic_run_to_run():
+    M, N, K = 1024, 1536, 2048
+    A, B = operands(M, N, K, "normal0.5")
+    first = run(A, B, M, N, K)
+    for _ in range(2):
+        assert np.array_equal(run(A, B, M, N, K), first)
+
+
+@pytest.mark.parametrize("option", ["force_pack", "force_direct_store"])
+def test_pack_and_store_paths_agree(option):
+    M, N, K = 1024, 640, 1040
+    A, B = operands(M, N, K, "normal0.5")
+    base = run(A, B, M, N, K)
+    bsk.set_option(option, 1)
+    try:
+        other = run(A, B, M, N, K)
+    finally:
+        bsk.set_option(option, 0)
+    assert np.array_equal(base, other)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (333, 129, 70)])
+def test_unaligned_pointers(M, N, K):
+    A, B = operands(M, N, K, "normal0.5")
+    got = run(A, B, M, N, K, offset=1)
+    ref, _ = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    check_tolerance(got, ref, "f16", K, absmax_f16(A), absmax_f16(B), "unaligned")
+
+
+def test_k_zero_writes_zeros():
+    got = run(np.zeros(0, np.uint16), np.zeros(0, np.uint16), 37, 19, 0)
+    assert np.all(got == 0)
+
+
+def test_enqueue_variant_matches_blocking():
+    M, N, K = 512, 384, 320
+    A, B = operands(M, N, K, "normal0.5")
+    assert np.array_equal(run(A, B, M, N, K, enqueue=True), run(A, B, M, N, K))
+
+
+def test_watchdog_gives_up_and_library_stays_usable():
+    """A wait that nothing satisfies returns BSK_ERR_TIMEOUT instead of hanging;
+    the context is still healthy afterwards."""
+    assert bsk.test_wait_timeout(2000) == 4
+    assert "gave up" in bsk.last_error()
+    test_integer_inputs_bit_exact(129, 257, 65)

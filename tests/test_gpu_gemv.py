@@ -1,0 +1,152 @@
+"""GPU parity of gemv_bf16 (decode GEMV, n <= 8, and the prefill GEMM, n > 8)
+against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from bf16_gemm_skinny_gb300 import _native as bsk
+from bf16_gemm_skinny_gb300 import build as bsk_build
+from bf16_gemm_skinny_gb300 import inputs
+from helpers import BF16_NAN, CANARY, absmax_bf16, check_tolerance, from_dev, poisoned, to_dev
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def operands(M, K, n, integer):
+    key = (M, K, n, integer)
+    if key not in _CACHE:
+        if integer:
+            _CACHE[key] = inputs.linear_operands(M, K, n, "int2", "int2", seed_x=11, seed_w=12)
+        else:
+            _CACHE[key] = inputs.linear_operands(M, K, n, "normal0.02", "normal1")
+    return _CACHE[key]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+
+    bsk_build.build()
+    oracle.build()
+    torch.cuda.init()
+    yield bsk.load()
+    for k in bsk.OPTIONS:
+        bsk.set_option(k, 0)
+
+
+def run(W, x, M, K, n, offset=0):
+    import torch
+
+    Wd = to_dev(np.concatenate([np.zeros(offset, np.uint16), W]))[offset:]
+    xd = to_dev(np.concatenate([np.zeros(offset, np.uint16), x]))[offset:]
+    buf, _ = poisoned(n * M + offset, BF16_NAN)
+    y = buf[offset:offset + n * M]
+    bsk.gemv_bf16(Wd, xd, y, M, K, n)
+    torch.cuda.synchronize()
+    assert np.all(from_dev(buf[offset + n * M:]) == CANARY), "guard words after y were written"
+    assert np.array_equal(from_dev(Wd), W), "W was modified"
+    assert np.array_equal(from_dev(xd), x), "x was modified"
+    return from_dev(y).reshape(n, M)
+
+
+@pytest.mark.parametrize("n", [1, 4, 8])
+def test_decode_34816x5120_full(n):
+    """The decode shape at full size; every output checked."""
+    M, K = 34816, 5120
+    W, x = operands(M, K, n, False)
+    got = run(W, x, M, K, n)
+    ref, _ = oracle.linear_bf16(W, x, M, K, n)
+    check_tolerance(got, ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"gemv n={n}")
+
+
+@pytest.mark.parametrize("n", [1, 4, 8])
+def test_decode_34816x5120_integer_bit_exact(n):
+    M, K = 34816, 5120
+    W, x = operands(M, K, n, True)
+    _, want = oracle.linear_bf16(W, x, M, K, n)
+    assert np.array_equal(run(W, x, M, K, n), want)
+
+
+@pytest.mark.parametrize("n", range(1, 9))
+@pytest.mark.parametrize("M,K", [(1003, 1032), (1, 8), (33, 5120), (4096, 256)])
+def test_every_token_count(n, M, K):
+    W, x = operands(M, K, n, True)
+    _, want = oracle.linear_bf16(W, x, M, K, n)
+    assert np.array_equal(run(W, x, M, K, n), want)
+    W, x = operands(M, K, n, False)
+    ref, _ = oracle.linear_bf16(W, x, M, K, n)
+    check_tolerance(run(W, x, M, K, n), ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"{M}x{K} n={n}")
+
+
+@pytest.mark.parametrize("rows", [1, 2, 4, 8])
+@pytest.mark.parametrize("warps", [1, 3, 8])
+@pytest.mark.parametrize("n", [1, 3, 8])
+def test_rows_per_warp_and_block_shape(rows, warps, n):
+    M, K = 2051, 2048
+    W, x = operands(M, K, n, True)
+    _, want = oracle.linear_bf16(W, x, M, K, n)
+    bsk.set_option("gemv_rows", rows)
+    bsk.set_option("gemv_warps", warps)
+    try:
+        got = run(W, x, M, K, n)
+    finally:
+        bsk.set_option("gemv_rows", 0)
+        bsk.set_option("gemv_warps", 0)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,K,n,offset", [(517, 1001, 3, 0), (300, 4096, 8, 1), (64, 7, 1, 0)])
+def test_scalar_variant(M, K, n, offset):
+    """K not a multiple of 8, or unaligned pointers: the scalar kernel."""
+    W, x = operands(M, K, n, False)
+    ref, _ = oracle.linear_bf16(W, x, M, K, n)
+    got = run(W, x, M, K, n, offset=offset)
+    check_tolerance(got, ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), "scalar")
+
+
+@pytest.mark.parametrize("n", [1, 8])
+def test_k_slabs(n):
+    """x larger than the shared-memory budget is staged in k-slabs."""
+    M, K = 301, 20000
+    W, x = operands(M, K, n, True)
+    _, want = oracle.linear_bf16(W, x, M, K, n)
+    assert np.array_equal(run(W, x, M, K, n), want)
+
+
+@pytest.mark.parametrize("M,K,n", [(1000, 520, 100), (256, 256, 9), (777, 1032, 300), (1024, 64, 4096)])
+def test_prefill_medium(M, K, n):
+    for integer in (True, False):
+        W, x = operands(M, K, n, integer)
+        ref, want = oracle.linear_bf16(W, x, M, K, n)
+        got = run(W, x, M, K, n)
+        if integer:
+            assert np.array_equal(got, want)
+        else:
+            check_tolerance(got, ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"prefill {M}x{K} n={n}")
+
+
+@pytest.mark.parametrize("integer", [False, True])
+def test_prefill_4096x34816x5120_sampled(integer):
+    """The prefill projection at full size, checked on sampled tokens and features."""
+    M, K, n = 34816, 5120, 4096
+    W, x = operands(M, K, n, integer)
+    got = run(W, x, M, K, n)
+    ts = [0, 1, 255, 256, 4095]
+    reft, outt = oracle.linear_bf16_tokens(W, x, M, K, n, ts)
+    js = [0, 127, 128, 20000, 34815]
+    refj, outj = oracle.linear_bf16(W, x, M, K, n, js=js)
+    if integer:
+        assert np.array_equal(got[ts, :], outt)
+        assert np.array_equal(got[:, js], outj)
+    else:
+        check_tolerance(got[ts, :], reft, "bf16", K, absmax_bf16(x), absmax_bf16(W), "prefill tokens")
+        check_tolerance(got[:, js], refj, "bf16", K, absmax_bf16(x), absmax_bf16(W), "prefill features")
+
+
+def test_k_zero_and_empty():
+    got = run(np.zeros(0, np.uint16), np.zeros(0, np.uint16), 50, 0, 3)
+    assert np.all(got == 0)
+    got = run(np.zeros(0, np.uint16), np.zeros(0, np.uint16), 50, 0, 20)
+    assert np.all(got == 0)

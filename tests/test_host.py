@@ -1,0 +1,139 @@
+"""Host-side checks that need no GPU: the library loads and exports every
+symbol of include/bsk.h, the tile rasteriser is a bijection onto the tile
+grid (remainder group included), argument validation rejects bad calls
+before touching a device, and the option table round-trips."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bf16_gemm_skinny_gb300 import _native as bsk
+from bf16_gemm_skinny_gb300 import build as bsk_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bsk_build.build()
+    return bsk.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "bsk.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int|void|long long|char)\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_bound_symbols():
+    assert header_functions() == sorted(bsk.EXPORTS)
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {bsk.library_path()}").read()
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    missing = set(header_functions()) - exported
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert bsk.version() >= 100
+    for code, name in bsk.STATUS.items():
+        assert lib.bsk_status_string(code).decode() == name
+
+
+def tiles_of(num_m, num_n, group_m):
+    return [bsk.tile_coord(t, num_m, num_n, group_m) for t in range(num_m * num_n)]
+
+
+@pytest.mark.parametrize("num_m,num_n,group_m", [
+    (1, 1, 1), (64, 32, 8), (32, 17, 12), (32, 17, 8), (7, 5, 3), (5, 7, 16), (272, 16, 8), (3, 100, 2),
+])
+def test_tile_coord_is_a_bijection(lib, num_m, num_n, group_m):
+    got = tiles_of(num_m, num_n, group_m)
+    assert sorted(got) == [(m, n) for m in range(num_m) for n in range(num_n)]
+
+
+def test_tile_coord_group_order_and_remainder(lib):
+    """Consecutive tiles walk down a group of group_m rows, then move one column;
+    the last group holds num_m mod group_m rows ("Hygon 优化", 分组调度)."""
+    num_m, num_n, g = 10, 4, 4
+    got = tiles_of(num_m, num_n, g)
+    assert got[:5] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1)]
+    tail = got[2 * g * num_n:]              # remainder group: rows 8, 9
+    assert tail[:4] == [(8, 0), (9, 0), (8, 1), (9, 1)]
+    assert {m for m, _ in tail} == {8, 9}
+
+
+def test_tile_coord_rejects_bad_arguments(lib):
+    assert bsk.tile_coord(5, 2, 2, 1) == (-1, -1)
+    assert bsk.tile_coord(0, 0, 2, 1) == (-1, -1)
+    assert bsk.tile_coord(0, 2, 2, 0) == (-1, -1)
+
+
+FAKE = 1 << 40   # never dereferenced: validation fails before any device access
+
+
+@pytest.mark.parametrize("args", [
+    (FAKE, FAKE + (1 << 30), FAKE + (2 << 30), -1, 4, 4),
+    (FAKE, FAKE + (1 << 30), FAKE + (2 << 30), 4, -1, 4),
+    (FAKE, FAKE + (1 << 30), FAKE + (2 << 30), 4, 4, -3),
+    (FAKE, FAKE + (1 << 30), None, 4, 4, 4),
+    (None, FAKE + (1 << 30), FAKE + (2 << 30), 4, 4, 4),
+    (FAKE, FAKE + 16, FAKE + 8, 4, 4, 4),             # C overlaps A
+    (FAKE, FAKE + 4096, FAKE + 4096 + 8, 4, 4, 4),    # C overlaps B
+])
+def test_gemm_rejects_bad_arguments(lib, args):
+    A, B, C, M, N, K = args
+    assert lib.gemm_f16_colmajor(A, B, C, M, N, K, None) == 1
+    assert lib.bsk_gemm_f16_colmajor_enqueue(A, B, C, M, N, K, None) == 1
+    assert bsk.last_error()
+
+
+@pytest.mark.parametrize("args", [
+    (FAKE, FAKE + (1 << 30), FAKE + (2 << 30), -1, 4, 1),
+    (FAKE, FAKE + (1 << 30), FAKE + (2 << 30), 4, 4, -1),
+    (FAKE, FAKE + (1 << 30), None, 4, 4, 1),
+    (FAKE, None, FAKE + (2 << 30), 4, 4, 1),
+    (FAKE, FAKE + (1 << 30), FAKE + 2, 4, 4, 1),      # y overlaps W
+])
+def test_gemv_rejects_bad_arguments(lib, args):
+    W, x, y, M, K, n = args
+    assert lib.gemv_bf16(W, x, y, M, K, n, None) == 1
+    assert lib.bsk_gemv_bf16_enqueue(W, x, y, M, K, n, None) == 1
+
+
+def test_empty_outputs_are_no_ops_without_a_device(lib):
+    assert lib.gemm_f16_colmajor(None, None, None, 0, 5, 7, None) == 0
+    assert lib.gemm_f16_colmajor(None, None, None, 5, 0, 7, None) == 0
+    assert lib.gemv_bf16(None, None, None, 0, 7, 1, None) == 0
+    assert lib.gemv_bf16(None, None, None, 9, 7, 0, None) == 0
+
+
+def test_options_round_trip_and_range_checks(lib):
+    assert bsk.get_option("group_m") == 0
+    bsk.set_option("group_m", 12)
+    assert bsk.get_option("group_m") == 12
+    bsk.set_option("group_m", 0)
+    with pytest.raises(bsk.BskError):
+        bsk.set_option("block_n", 96)
+    with pytest.raises(bsk.BskError):
+        bsk.set_option("gemv_rows", 3)
+    assert lib.bsk_set_option(99, 1) == 1
+
+
+def test_watchdog_probe_validates_limit(lib):
+    assert lib.bsk_test_wait_timeout(0, None) == 1
+    assert lib.bsk_test_wait_timeout(20_000_000, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """No fallback: a missing library is an error, not a silent CPU path."""
+    monkeypatch.setattr(bsk, "_lib", None)
+    monkeypatch.setattr(bsk_build, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        bsk.load()
