@@ -42,7 +42,7 @@ OPTIONS = {
 EXPORTS = (
     "gemm_f16_colmajor", "gemv_bf16", "bsk_gemm_f16_colmajor_enqueue", "bsk_gemv_bf16_enqueue",
     "bsk_stream_check", "bsk_last_error", "bsk_status_string", "bsk_version", "bsk_tile_coord",
-    "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout",
+    "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout", "gemm_f16_colmajor_noalloc",
 )
 
 
@@ -70,7 +70,7 @@ def load():
         lib = ctypes.CDLL(path)
         p = ctypes.c_void_p
         i = ctypes.c_int
-        for name in ("gemm_f16_colmajor", "bsk_gemm_f16_colmajor_enqueue"):
+        for name in ("gemm_f16_colmajor", "bsk_gemm_f16_colmajor_enqueue", "gemm_f16_colmajor_noalloc"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
             getattr(lib, name).restype = i
         for name in ("gemv_bf16", "bsk_gemv_bf16_enqueue"):
@@ -131,6 +131,12 @@ def gemm_f16_colmajor(A, B, C, M: int, N: int, K: int, stream=None) -> None:
 def gemm_f16_colmajor_enqueue(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     """Asynchronous variant of gemm_f16_colmajor (check with stream_check)."""
     _check(load().bsk_gemm_f16_colmajor_enqueue(_addr(A), _addr(B), _addr(C), M, N, K, _stream(stream)))
+
+
+def gemm_f16_colmajor_noalloc(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """gemm_f16_colmajor without any device allocation: packs unaligned operands
+    into the library's fixed 96 MiB scratch array instead (see include/bsk.h)."""
+    _check(load().gemm_f16_colmajor_noalloc(_addr(A), _addr(B), _addr(C), M, N, K, _stream(stream)))
 
 
 def gemv_bf16(W, x, y, M: int, K: int, n: int, stream=None) -> None:

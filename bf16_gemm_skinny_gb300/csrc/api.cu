@@ -292,6 +292,11 @@ int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, 
 
 namespace bsk {
 
+void record_error(const char* msg)
+{
+    snprintf(t_err, sizeof(t_err), "%s", msg);
+}
+
 TmapEncodeFn tmap_encoder()
 {
     static TmapEncodeFn fn = []() -> TmapEncodeFn {

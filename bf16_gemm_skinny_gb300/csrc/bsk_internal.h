@@ -35,6 +35,9 @@ using TmapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Sets the message bsk_last_error() returns on this host thread.
+void record_error(const char* msg);
+
 // cuTensorMapEncodeTiled from the driver (resolved once through the runtime).
 TmapEncodeFn tmap_encoder();
 

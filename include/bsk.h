@@ -76,6 +76,29 @@ int gemm_f16_colmajor(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, 
 int gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);
 
 /*
+ * gemm_f16_colmajor for callers that cannot allocate device memory during a
+ * call (for example a serving process whose own allocator reserved all free
+ * HBM at start-up, or a program held to a device-memory budget fixed when it
+ * started).  Same arguments, result and blocking behaviour as
+ * gemm_f16_colmajor, and the same kernels.  The pages have no counterpart:
+ * this entry point exists for the way the library is deployed.
+ *
+ * Instead of allocating a workspace when an operand must be packed (base not
+ * 16-byte aligned, or M or K not a multiple of 8), it packs into a fixed
+ * 96 MiB device array that is part of the library (held on every GPU that
+ * loads it, until the process exits), and it calls no cudaMalloc, cudaFree or
+ * other allocating routine.  Calls needing more scratch than 96 MiB return
+ * BSK_ERR_INVALID_ARG; aligned operands need none at any size.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress): make it before any stream capture on that device.
+ * All calls share the array and keep the previous call's contents in it, so
+ * calls that overlap on the GPU (several streams or host threads) race:
+ * serialise them.
+ */
+int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
+                              void* stream);
+
+/*
  * Same work as gemm_f16_colmajor / gemv_bf16, but asynchronous: validates the
  * arguments, launches on `stream` and returns without waiting.  A device-side
  * watchdog timeout raised by this work is reported by the next
