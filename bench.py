@@ -113,22 +113,27 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_digest() -> str:
-    """Hash of the kernel sources; a committed traffic figure is only reported
-    while the kernels are unchanged since it was measured."""
+KERNEL_SOURCES = {
+    "gemm": ("gemm_tcgen05.cu", "ptx.cuh", "bsk_internal.h"),
+    "gemv": ("gemv.cu", "bsk_internal.h"),
+}
+
+
+def source_digest(kernel: str) -> str:
+    """Hash of one kernel's sources; a committed traffic figure is only reported
+    while that kernel is unchanged since it was measured."""
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "bf16_gemm_skinny_gb300", "csrc")
-    for name in sorted(os.listdir(cdir)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(cdir, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(cdir, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(kernel_key: str):
     """DRAM bytes per launch from profiles/traffic.txt (lines: key digest bytes)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    digest = source_digest()
+    digest = source_digest(kernel_key.split("_")[0])
     try:
         with open(path) as f:
             for line in f:
@@ -430,6 +435,52 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """One kernel, one shape, `warmup + steps` launches, nothing else: the
+    command the ncu summaries in profiles/ are taken with.
+    Cases: gemm:MxNxK (FP16 column-major GEMM) or gemv:MxKxn (BF16 linear)."""
+    import torch
+
+    from bf16_gemm_skinny_gb300 import _native as bsk
+    from bf16_gemm_skinny_gb300 import build as bsk_build
+    from bf16_gemm_skinny_gb300 import inputs
+
+    kind, shape = args.case.split(":")
+    a, b, c = (int(v) for v in shape.lower().split("x"))
+    bsk_build.build()
+    for kv in args.opt or []:
+        key, val = kv.split("=")
+        bsk.set_option(key, int(val))
+    dev = torch.device("cuda", 0)
+    to_dev = lambda bits: torch.from_numpy(bits.view("int16")).to(dev)  # noqa: E731
+    if kind == "gemm":
+        A, B = inputs.gemm_operands(a, b, c, "uniform")
+        Ad, Bd = to_dev(A), to_dev(B)
+        C = torch.empty(a * b, dtype=torch.int16, device=dev)
+        call = lambda: bsk.gemm_f16_colmajor_enqueue(Ad, Bd, C, a, b, c)  # noqa: E731
+        work, unit = 2.0 * a * b * c, "TFLOP/s"
+    elif kind == "gemv":
+        W, x = inputs.linear_operands(a, b, c, "normal0.02", "normal1")
+        Wd, xd = to_dev(W), to_dev(x)
+        y = torch.empty(a * c, dtype=torch.int16, device=dev)
+        call = lambda: bsk.gemv_bf16_enqueue(Wd, xd, y, a, b, c)  # noqa: E731
+        work, unit = 2.0 * (a * b + c * b + c * a), "GB/s"
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    for _ in range(args.warmup):
+        call()
+    bsk.stream_check()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    bsk.stream_check()
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"case": args.case, "ms": round(ms, 4), unit: round(rate, 1)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,7 +489,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", help="profile mode: one kernel only, e.g. gemm:8192x8192x8192 or gemv:34816x5120x1")
+    ap.add_argument("--opt", action="append", help="profile mode: library option name=value (repeatable)")
     args = ap.parse_args(argv)
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -36,6 +36,7 @@ OPTIONS = {
     "gemv_warps": 6,
     "wait_limit_us": 7,
     "num_sms": 8,
+    "gemv_kernel": 9,
 }
 
 # Every symbol include/bsk.h declares.

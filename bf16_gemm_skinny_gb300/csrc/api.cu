@@ -43,7 +43,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 9;
+constexpr int kNumOpts = 10;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -279,6 +279,7 @@ int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, 
         g.n = n;
         g.rows_per_warp = static_cast<int>(opt_or(BSK_OPT_GEMV_ROWS, 0));
         g.warps_per_block = static_cast<int>(opt_or(BSK_OPT_GEMV_WARPS, 0));
+        g.kernel = static_cast<int>(opt_or(BSK_OPT_GEMV_KERNEL, 0));
         g.num_sms = sms;
         char msg[512] = "";
         if (bsk::launch_gemv(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
@@ -383,7 +384,8 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_FORCE_PACK:
     case BSK_OPT_FORCE_DIRECT_STORE: ok = value == 0 || value == 1; break;
     case BSK_OPT_GEMV_ROWS: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8; break;
-    case BSK_OPT_GEMV_WARPS: ok = value >= 0 && value <= 8; break;
+    case BSK_OPT_GEMV_WARPS: ok = value >= 0 && value <= 16; break;
+    case BSK_OPT_GEMV_KERNEL: ok = value >= 0 && value <= 3; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

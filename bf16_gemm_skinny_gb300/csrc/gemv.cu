@@ -40,9 +40,14 @@ __device__ __forceinline__ uint4 ld_stream_16B(const uint4* p)
 }
 
 // bf16 pair in one 32-bit word -> the two FP32 values (element 0 = low half).
+// A bfloat16 is the upper half of a binary32, so each value is a byte
+// permutation with zero low bytes (prmt keeps this on the integer pipe).
 __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w)
 {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    uint32_t lo, hi;
+    asm("prmt.b32 %0, %1, 0, 0x1044;" : "=r"(lo) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0x3244;" : "=r"(hi) : "r"(w));
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
 }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
@@ -236,6 +241,190 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined variant (x fits in shared memory next to the W ring).
+//
+// Each warp streams its rows through a private ring of D stages in shared
+// memory with cp.async (16 bytes per lane per row per stage), so the bytes in
+// flight (D-1 stages of R rows x 512 bytes per warp) do not depend on
+// registers or on where the warp is in its arithmetic.  The warp's whole
+// work -- all its row groups, each of ceil(K8/32) steps -- is one linear
+// stream of steps, so the copies for the next row group start while the
+// current one is still being reduced.  Each lane reads back only the
+// 16-byte pieces it copied itself, so cp.async.wait_group is the only
+// synchronisation needed.  Lanes past the end of a row (or rows past M)
+// copy zero bytes, which zero-fills the slot.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// x (n rows of K BF16) into shared memory, whole K.  XF32: FP32, values 0-3 of
+// chunk c of token t at xs4[(2t)*K8 + c], values 4-7 at xs4[(2t+1)*K8 + c];
+// otherwise the raw BF16 chunk at xs4[t*K8 + c].
+template <int NT, bool XF32>
+__device__ __forceinline__ void stage_x_whole(const uint4* __restrict__ x4, int K8, uint4* xs4)
+{
+    for (int i = threadIdx.x; i < NT * K8; i += blockDim.x) {
+        const int t = i / K8;
+        const int c = i - t * K8;
+        const uint4 v = x4[i];
+        if constexpr (XF32) {
+            const float2 f0 = bf16x2_to_f32x2(v.x), f1 = bf16x2_to_f32x2(v.y);
+            const float2 f2 = bf16x2_to_f32x2(v.z), f3 = bf16x2_to_f32x2(v.w);
+            reinterpret_cast<float4*>(xs4)[static_cast<long long>(2 * t) * K8 + c] =
+                make_float4(f0.x, f0.y, f1.x, f1.y);
+            reinterpret_cast<float4*>(xs4)[static_cast<long long>(2 * t + 1) * K8 + c] =
+                make_float4(f2.x, f2.y, f3.x, f3.y);
+        } else {
+            xs4[static_cast<long long>(t) * K8 + c] = v;
+        }
+    }
+}
+
+template <int NT, int R, int D, bool XF32>
+__global__ void __launch_bounds__(512, 1)
+    gemv_bf16_pipe_kernel(const uint4* __restrict__ W4, const uint4* __restrict__ x4, __nv_bfloat16* __restrict__ y,
+                          int M, int K8, int groups_per_warp)
+{
+    extern __shared__ uint4 smem4[];
+    constexpr int V = next_pow2(R * NT);
+    constexpr uint32_t kSlotBytes = R * 512u;       // one stage of one warp: R rows x 32 lanes x 16 B
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int warps = blockDim.x >> 5;
+    const int x_words = NT * K8 * (XF32 ? 2 : 1);
+    uint4* xs4 = smem4;
+    uint4* ring = smem4 + x_words + warp * D * R * 32;
+    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + lane * 16u;
+
+    stage_x_whole<NT, XF32>(x4, K8, xs4);
+    __syncthreads();
+
+    const int num_groups = (M + R - 1) / R;
+    const int g_begin = (blockIdx.x * warps + warp) * groups_per_warp;
+    int g_count = num_groups - g_begin;
+    if (g_count > groups_per_warp) g_count = groups_per_warp;
+    if (g_count <= 0) return;
+    const int steps = (K8 + 31) >> 5;
+    const long long row_stride = K8;                 // uint4 per row
+
+    // Issue cursor: the next (group, step) whose copies go out, and its ring slot.
+    int i_g = 0, i_s = 0, i_slot = 0;
+    const uint4* i_ptr = W4 + static_cast<long long>(g_begin) * R * row_stride + lane;
+    int i_rows = M - g_begin * R;
+    auto issue = [&]() {
+        if (i_g < g_count) {
+            const uint32_t dst = ring_s + static_cast<uint32_t>(i_slot) * kSlotBytes;
+            const bool kok = i_s * 32 + lane < K8;
+            if (kok && i_rows >= R) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) cp_async_16(dst + r * 512u, i_ptr + r * row_stride, 16u);
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const bool ok = kok && r < i_rows;
+                    cp_async_16(dst + r * 512u, ok ? i_ptr + r * row_stride : W4, ok ? 16u : 0u);
+                }
+            }
+            i_ptr += 32;
+            if (++i_s == steps) {
+                i_s = 0;
+                ++i_g;
+                i_ptr += R * row_stride - static_cast<long long>(steps) * 32;
+                i_rows -= R;
+            }
+            if (++i_slot == D) i_slot = 0;
+        }
+        cp_async_commit();
+    };
+
+#pragma unroll
+    for (int q = 0; q < D - 1; ++q) issue();
+
+    int c_slot = 0;
+    for (int gi = 0; gi < g_count; ++gi) {
+        float2 acc[R][NT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[r][t] = make_float2(0.f, 0.f);
+
+        for (int st = 0; st < steps; ++st) {
+            issue();
+            cp_async_wait<D - 1>();
+            const int c = st * 32 + lane;
+            if (c < K8) {
+                const uint4* slot = ring + c_slot * (R * 32) + lane;
+                float2 wf[R][4];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint4 w = slot[r * 32];
+                    wf[r][0] = bf16x2_to_f32x2(w.x);
+                    wf[r][1] = bf16x2_to_f32x2(w.y);
+                    wf[r][2] = bf16x2_to_f32x2(w.z);
+                    wf[r][3] = bf16x2_to_f32x2(w.w);
+                }
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    float2 x0, x1, x2, x3;
+                    if constexpr (XF32) {
+                        const float4* xt = reinterpret_cast<const float4*>(xs4) + 2 * t * K8 + c;
+                        const float4 xa = xt[0];
+                        const float4 xb = xt[K8];
+                        x0 = make_float2(xa.x, xa.y);
+                        x1 = make_float2(xa.z, xa.w);
+                        x2 = make_float2(xb.x, xb.y);
+                        x3 = make_float2(xb.z, xb.w);
+                    } else {
+                        const uint4 xv = xs4[t * K8 + c];
+                        x0 = bf16x2_to_f32x2(xv.x);
+                        x1 = bf16x2_to_f32x2(xv.y);
+                        x2 = bf16x2_to_f32x2(xv.z);
+                        x3 = bf16x2_to_f32x2(xv.w);
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        acc[r][t] = ffma2(wf[r][0], x0, acc[r][t]);
+                        acc[r][t] = ffma2(wf[r][1], x1, acc[r][t]);
+                        acc[r][t] = ffma2(wf[r][2], x2, acc[r][t]);
+                        acc[r][t] = ffma2(wf[r][3], x3, acc[r][t]);
+                    }
+                }
+            }
+            if (++c_slot == D) c_slot = 0;
+        }
+
+        const int row0 = (g_begin + gi) * R;
+        float v[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) v[i] = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) v[r * NT + t] = acc[r][t].x + acc[r][t].y;
+        warp_reduce_scatter<V>(v, lane);
+        if (result_owner<V>(lane)) {
+            constexpr int kHeld = V >= 32 ? V / 32 : 1;
+#pragma unroll
+            for (int i = 0; i < kHeld; ++i) {
+                const int idx = result_index<V>(lane, i);
+                if (idx < R * NT) {
+                    const int r = idx / NT;
+                    const int t = idx - r * NT;
+                    if (row0 + r < M) y[static_cast<long long>(t) * M + row0 + r] = __float2bfloat16_rn(v[i]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
 // Scalar variant: any K, any alignment.  One warp per output row.
 template <int NT>
 __global__ void __launch_bounds__(256)
@@ -273,7 +462,7 @@ int launch_vec(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_l
 {
     auto kern = gemv_bf16_kernel<NT, R, U>;
     const int K8 = g.K / 8;
-    const int threads = 32 * (g.warps_per_block > 0 ? g.warps_per_block : 8);
+    const int threads = 32 * (g.warps_per_block > 0 && g.warps_per_block <= 8 ? g.warps_per_block : 8);
     // x in FP32: NT * slab8 * 32 bytes; keep it within 192 KB (k-slabs beyond that)
     const long long budget = 192 * 1024;
     long long slab8 = budget / (32LL * NT);
@@ -337,7 +526,111 @@ int launch_vec_rows(const GemvLaunch& g, int rows, cudaStream_t stream, char* ms
     }
 }
 
-constexpr int default_rows(int n) { return n <= 2 ? 8 : 4; }
+constexpr int kPipeMaxSmem = 232448;   // 227 KB per CTA
+
+// Shared memory of the pipelined kernel: x (FP32 or BF16) + one ring per warp.
+constexpr long long pipe_smem(int NT, int R, int D, bool xf32, int K8, int warps)
+{
+    return static_cast<long long>(NT) * K8 * (xf32 ? 32 : 16) + static_cast<long long>(warps) * D * R * 512;
+}
+
+// Returns 1 and sets *status if the pipelined kernel ran (or failed to launch), 0 if it does not fit.
+template <int NT, int R, int D, bool XF32>
+int try_launch_pipe(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len, int* status,
+                    int min_warps)
+{
+    const int K8 = g.K / 8;
+    const long long groups = (static_cast<long long>(g.M) + R - 1) / R;
+    // Warps per CTA (one CTA per SM): the requested count, else the count in
+    // [min_warps, 16] that fits in shared memory and leaves the fewest idle warp
+    // slots when every warp takes the same number of row groups.
+    int warps = 0;
+    if (g.warps_per_block > 0) {
+        if (pipe_smem(NT, R, D, XF32, K8, g.warps_per_block) <= kPipeMaxSmem) warps = g.warps_per_block;
+    } else {
+        double best = -1.0;
+        for (int w = 16; w >= min_warps; --w) {
+            if (pipe_smem(NT, R, D, XF32, K8, w) > kPipeMaxSmem) continue;
+            const long long slots = static_cast<long long>(g.num_sms) * w;
+            const long long per = (groups + slots - 1) / slots;
+            const double eff = static_cast<double>(groups) / static_cast<double>(per * slots);
+            if (eff > best + 1e-9) {
+                best = eff;
+                warps = w;
+            }
+        }
+    }
+    if (warps == 0) return 0;
+    const long long smem = pipe_smem(NT, R, D, XF32, K8, warps);
+    auto kern = gemv_bf16_pipe_kernel<NT, R, D, XF32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        *status = 1;
+        return 1;
+    }
+    // Same number of row groups for every warp: size the grid to the work.
+    const long long max_warps = static_cast<long long>(g.num_sms) * warps;
+    const long long per_warp = (groups + max_warps - 1) / max_warps;
+    const long long warps_needed = (groups + per_warp - 1) / per_warp;
+    const long long grid = (warps_needed + warps - 1) / warps;
+    kern<<<static_cast<unsigned>(grid), warps * 32, smem, stream>>>(
+        reinterpret_cast<const uint4*>(g.W), reinterpret_cast<const uint4*>(g.x),
+        reinterpret_cast<__nv_bfloat16*>(g.y), g.M, K8, static_cast<int>(per_warp));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "GEMV launch failed: %s", cudaGetErrorString(e));
+        *status = 1;
+        return 1;
+    }
+    *status = 0;
+    return 1;
+}
+
+// Pipelined kernel with R rows per warp: x in FP32 when that leaves room for at
+// least 8 warps (or the requested count), else x in BF16 (converted per use).
+template <int NT, int R, int D>
+int try_launch_pipe_rows(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len, int* status)
+{
+    const int min_warps = g.warps_per_block > 0 ? g.warps_per_block : 8;
+    if (g.kernel != 3) {
+        if (try_launch_pipe<NT, R, D, true>(g, stream, msg, msg_len, status, min_warps)) return 1;
+    }
+    return try_launch_pipe<NT, R, D, false>(g, stream, msg, msg_len, status, min_warps);
+}
+
+// Kernel choice for the aligned path.  Measured on the 34816 x 5120 decode
+// shape: n <= 2 streams fastest from registers (the arithmetic is light and
+// the loads of U chunks per lane keep HBM busy); for n >= 3 the arithmetic per
+// byte grows and the cp.async ring keeps loads in flight while it runs, with x
+// in FP32 up to n = 4 and in BF16 (more warps fit) beyond.
+template <int NT>
+int launch_vec_any(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
+{
+    const int kernel = g.kernel != 0 ? g.kernel : (NT <= 2 ? 1 : (NT <= 4 ? 2 : 3));
+    const int rows = g.rows_per_warp > 0 ? g.rows_per_warp : 4;
+    if (kernel != 1) {
+        GemvLaunch gk = g;
+        gk.kernel = kernel;
+        int status = 0;
+        int ran = 0;
+        switch (rows) {
+        case 1: ran = try_launch_pipe_rows<NT, 1, 8>(gk, stream, msg, msg_len, &status); break;
+        case 2: ran = try_launch_pipe_rows<NT, 2, 5>(gk, stream, msg, msg_len, &status); break;
+        case 4: ran = try_launch_pipe_rows<NT, 4, 3>(gk, stream, msg, msg_len, &status); break;
+        case 8: ran = try_launch_pipe_rows<NT, 8, 3>(gk, stream, msg, msg_len, &status); break;
+        default:
+            snprintf(msg, msg_len, "unsupported rows_per_warp %d (1, 2, 4 or 8)", rows);
+            return 1;
+        }
+        if (ran) return status;
+        if (g.kernel >= 2) {
+            snprintf(msg, msg_len, "pipelined GEMV does not fit in shared memory for K=%d, n=%d", g.K, NT);
+            return 1;
+        }
+    }
+    return launch_vec_rows<NT>(g, rows, stream, msg, msg_len);
+}
 
 }  // namespace
 
@@ -345,17 +638,16 @@ int launch_gemv(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_
 {
     const bool vec = (g.K % 8 == 0) && (reinterpret_cast<uintptr_t>(g.W) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(g.x) % 16 == 0);
-    const int rows = g.rows_per_warp > 0 ? g.rows_per_warp : default_rows(g.n);
     if (vec) {
         switch (g.n) {
-        case 1: return launch_vec_rows<1>(g, rows, stream, msg, msg_len);
-        case 2: return launch_vec_rows<2>(g, rows, stream, msg, msg_len);
-        case 3: return launch_vec_rows<3>(g, rows, stream, msg, msg_len);
-        case 4: return launch_vec_rows<4>(g, rows, stream, msg, msg_len);
-        case 5: return launch_vec_rows<5>(g, rows, stream, msg, msg_len);
-        case 6: return launch_vec_rows<6>(g, rows, stream, msg, msg_len);
-        case 7: return launch_vec_rows<7>(g, rows, stream, msg, msg_len);
-        case 8: return launch_vec_rows<8>(g, rows, stream, msg, msg_len);
+        case 1: return launch_vec_any<1>(g, stream, msg, msg_len);
+        case 2: return launch_vec_any<2>(g, stream, msg, msg_len);
+        case 3: return launch_vec_any<3>(g, stream, msg, msg_len);
+        case 4: return launch_vec_any<4>(g, stream, msg, msg_len);
+        case 5: return launch_vec_any<5>(g, stream, msg, msg_len);
+        case 6: return launch_vec_any<6>(g, stream, msg, msg_len);
+        case 7: return launch_vec_any<7>(g, stream, msg, msg_len);
+        case 8: return launch_vec_any<8>(g, stream, msg, msg_len);
         default: break;
         }
     } else {

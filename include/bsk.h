@@ -139,9 +139,12 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_FORCE_PACK       1: pack A and B even when aligned
  *   BSK_OPT_FORCE_DIRECT_STORE 1: masked register stores instead of the TMA store
  *   BSK_OPT_GEMV_ROWS        GEMV rows of W per warp: 1, 2, 4 or 8 (default by n)
- *   BSK_OPT_GEMV_WARPS       GEMV warps per CTA, 1..8 (default 8)
+ *   BSK_OPT_GEMV_WARPS       GEMV warps per CTA, 1..16 (default 16 pipelined, 8 streaming)
  *   BSK_OPT_WAIT_LIMIT_US    device-side wait limit in microseconds (default 2 s)
  *   BSK_OPT_NUM_SMS          cap on the persistent GEMM grid (default: all SMs)
+ *   BSK_OPT_GEMV_KERNEL      GEMV kernel: 1 register streaming, 2 cp.async-pipelined,
+ *                            3 pipelined with x kept in BF16 (default: pipelined when x
+ *                            and the ring fit in shared memory)
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
@@ -152,7 +155,8 @@ enum {
     BSK_OPT_GEMV_ROWS = 5,
     BSK_OPT_GEMV_WARPS = 6,
     BSK_OPT_WAIT_LIMIT_US = 7,
-    BSK_OPT_NUM_SMS = 8
+    BSK_OPT_NUM_SMS = 8,
+    BSK_OPT_GEMV_KERNEL = 9
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);

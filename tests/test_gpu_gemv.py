@@ -80,21 +80,40 @@ def test_every_token_count(n, M, K):
     check_tolerance(run(W, x, M, K, n), ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"{M}x{K} n={n}")
 
 
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 @pytest.mark.parametrize("rows", [1, 2, 4, 8])
-@pytest.mark.parametrize("warps", [1, 3, 8])
+@pytest.mark.parametrize("warps", [1, 3, 8, 16])
 @pytest.mark.parametrize("n", [1, 3, 8])
-def test_rows_per_warp_and_block_shape(rows, warps, n):
+def test_kernels_rows_per_warp_and_block_shape(kernel, rows, warps, n):
+    """Both GEMV kernels (register streaming, cp.async pipeline) at every rows-per-warp
+    and block shape give the oracle's bits on integer inputs."""
     M, K = 2051, 2048
     W, x = operands(M, K, n, True)
     _, want = oracle.linear_bf16(W, x, M, K, n)
+    bsk.set_option("gemv_kernel", kernel)
     bsk.set_option("gemv_rows", rows)
     bsk.set_option("gemv_warps", warps)
     try:
         got = run(W, x, M, K, n)
     finally:
+        bsk.set_option("gemv_kernel", 0)
         bsk.set_option("gemv_rows", 0)
         bsk.set_option("gemv_warps", 0)
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("n", [1, 4, 8])
+def test_both_kernels_full_decode_shape(kernel, n):
+    M, K = 34816, 5120
+    W, x = operands(M, K, n, False)
+    ref, _ = oracle.linear_bf16(W, x, M, K, n)
+    bsk.set_option("gemv_kernel", kernel)
+    try:
+        got = run(W, x, M, K, n)
+    finally:
+        bsk.set_option("gemv_kernel", 0)
+    check_tolerance(got, ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"gemv kernel={kernel} n={n}")
 
 
 @pytest.mark.parametrize("M,K,n,offset", [(517, 1001, 3, 0), (300, 4096, 8, 1), (64, 7, 1, 0)])
