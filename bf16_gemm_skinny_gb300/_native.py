@@ -37,6 +37,7 @@ OPTIONS = {
     "wait_limit_us": 7,
     "num_sms": 8,
     "gemv_kernel": 9,
+    "gemm_kernel": 10,
 }
 
 # Every symbol include/bsk.h declares.

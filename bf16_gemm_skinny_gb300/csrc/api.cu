@@ -43,7 +43,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 10;
+constexpr int kNumOpts = 11;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -218,6 +218,7 @@ int run_gemm(const uint16_t* A, bool a_mn_major, const uint16_t* B, uint16_t* C,
     g.bf16 = bf16;
     g.block_n = static_cast<int>(opt_or(BSK_OPT_BLOCK_N, 256));
     g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, 8));
+    g.pair = opt_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
     g.tma_store = aligned16(C) && (M % 8 == 0) && opt_or(BSK_OPT_FORCE_DIRECT_STORE, 0) == 0;
     g.num_sms = sms;
     g.status = g_status_dev;
@@ -386,6 +387,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_GEMV_ROWS: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8; break;
     case BSK_OPT_GEMV_WARPS: ok = value >= 0 && value <= 16; break;
     case BSK_OPT_GEMV_KERNEL: ok = value >= 0 && value <= 3; break;
+    case BSK_OPT_GEMM_KERNEL: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

@@ -58,6 +58,7 @@ struct GemmLaunch {
     int M, N, K;
     bool bf16;
     int block_n;    // 128 or 256
+    bool pair;      // block_n == 256 only: CTA-pair kernel (256 x 256 tiles over two SMs)
     int group_m;    // >= 1
     bool tma_store; // C 16-byte aligned with 16-byte-multiple ldc
     int num_sms;    // persistent grid size cap

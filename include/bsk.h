@@ -142,6 +142,8 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_GEMV_WARPS       GEMV warps per CTA, 1..16 (default 16 pipelined, 8 streaming)
  *   BSK_OPT_WAIT_LIMIT_US    device-side wait limit in microseconds (default 2 s)
  *   BSK_OPT_NUM_SMS          cap on the persistent GEMM grid (default: all SMs)
+ *   BSK_OPT_GEMM_KERNEL      GEMM kernel for 256-wide tiles: 1 one CTA per 128 x 256 tile,
+ *                            2 CTA pairs on 256 x 256 tiles (default 2)
  *   BSK_OPT_GEMV_KERNEL      GEMV kernel: 1 register streaming, 2 cp.async-pipelined,
  *                            3 pipelined with x kept in BF16 (default: pipelined when x
  *                            and the ring fit in shared memory)
@@ -156,7 +158,8 @@ enum {
     BSK_OPT_GEMV_WARPS = 6,
     BSK_OPT_WAIT_LIMIT_US = 7,
     BSK_OPT_NUM_SMS = 8,
-    BSK_OPT_GEMV_KERNEL = 9
+    BSK_OPT_GEMV_KERNEL = 9,
+    BSK_OPT_GEMM_KERNEL = 10
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);

@@ -134,19 +134,37 @@ def test_8192x8192x16384_sampled(dist):
     sampled_check(got, A, B, M, N, K, cols, rows, dist == "int2")
 
 
-@pytest.mark.parametrize("block_n,group_m", [(256, 8), (128, 1), (128, 12), (256, 3), (256, 1)])
-def test_result_independent_of_tile_config(block_n, group_m):
+@pytest.mark.parametrize("kernel,block_n,group_m", [
+    (2, 256, 8), (2, 256, 1), (2, 256, 3), (1, 256, 8), (1, 256, 3), (1, 128, 1), (1, 128, 12)])
+def test_result_independent_of_tile_config(kernel, block_n, group_m):
+    """CTA-pair 256x256 tiles, single-CTA 128x256 and 128x128 tiles, several
+    GROUP_M: bit-identical to the oracle on integer inputs."""
     M, N, K = 1000, 777, 1030
     A, B = operands(M, N, K, "int2")
     _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    bsk.set_option("gemm_kernel", kernel)
     bsk.set_option("block_n", block_n)
     bsk.set_option("group_m", group_m)
     try:
         got = run(A, B, M, N, K)
     finally:
+        bsk.set_option("gemm_kernel", 0)
         bsk.set_option("block_n", 0)
         bsk.set_option("group_m", 0)
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (129, 257, 65), (1000, 777, 1030), (300, 517, 200)])
+def test_single_cta_kernel(M, N, K):
+    """The one-CTA-per-tile kernel stays correct beside the default CTA-pair kernel."""
+    A, B = operands(M, N, K, "normal0.5")
+    bsk.set_option("gemm_kernel", 1)
+    try:
+        got = run(A, B, M, N, K)
+    finally:
+        bsk.set_option("gemm_kernel", 0)
+    ref, _ = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    check_tolerance(got, ref, "f16", K, absmax_f16(A), absmax_f16(B), f"single-CTA {M}x{N}x{K}")
 
 
 def test_deterministic_run_to_run():

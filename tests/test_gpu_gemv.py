@@ -134,8 +134,17 @@ def test_k_slabs(n):
     assert np.array_equal(run(W, x, M, K, n), want)
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("M,K,n", [(1000, 520, 100), (256, 256, 9), (777, 1032, 300), (1024, 64, 4096)])
-def test_prefill_medium(M, K, n):
+def test_prefill_medium(kernel, M, K, n):
+    bsk.set_option("gemm_kernel", kernel)
+    try:
+        _prefill_medium(M, K, n)
+    finally:
+        bsk.set_option("gemm_kernel", 0)
+
+
+def _prefill_medium(M, K, n):
     for integer in (True, False):
         W, x = operands(M, K, n, integer)
         ref, want = oracle.linear_bf16(W, x, M, K, n)
