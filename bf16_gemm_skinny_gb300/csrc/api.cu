@@ -217,8 +217,9 @@ int run_gemm(const uint16_t* A, bool a_mn_major, const uint16_t* B, uint16_t* C,
     g.K = K;
     g.bf16 = bf16;
     g.block_n = static_cast<int>(opt_or(BSK_OPT_BLOCK_N, 256));
-    g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, 8));
     g.pair = opt_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
+    // Tile-row group: measured best on GB300 for 8192^3-class and prefill shapes.
+    g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, g.pair && g.block_n == 256 ? 2 : 16));
     g.tma_store = aligned16(C) && (M % 8 == 0) && opt_or(BSK_OPT_FORCE_DIRECT_STORE, 0) == 0;
     g.num_sms = sms;
     g.status = g_status_dev;

@@ -372,28 +372,26 @@ __global__ void __launch_bounds__(512, 1)
                 }
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    float2 x0, x1, x2, x3;
+                    // rows innermost: consecutive FMAs update different accumulators
                     if constexpr (XF32) {
                         const float4* xt = reinterpret_cast<const float4*>(xs4) + 2 * t * K8 + c;
                         const float4 xa = xt[0];
                         const float4 xb = xt[K8];
-                        x0 = make_float2(xa.x, xa.y);
-                        x1 = make_float2(xa.z, xa.w);
-                        x2 = make_float2(xb.x, xb.y);
-                        x3 = make_float2(xb.z, xb.w);
+                        const float2 xp[4] = {make_float2(xa.x, xa.y), make_float2(xa.z, xa.w),
+                                              make_float2(xb.x, xb.y), make_float2(xb.z, xb.w)};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int r = 0; r < R; ++r) acc[r][t] = ffma2(wf[r][q], xp[q], acc[r][t]);
                     } else {
                         const uint4 xv = xs4[t * K8 + c];
-                        x0 = bf16x2_to_f32x2(xv.x);
-                        x1 = bf16x2_to_f32x2(xv.y);
-                        x2 = bf16x2_to_f32x2(xv.z);
-                        x3 = bf16x2_to_f32x2(xv.w);
-                    }
+                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        acc[r][t] = ffma2(wf[r][0], x0, acc[r][t]);
-                        acc[r][t] = ffma2(wf[r][1], x1, acc[r][t]);
-                        acc[r][t] = ffma2(wf[r][2], x2, acc[r][t]);
-                        acc[r][t] = ffma2(wf[r][3], x3, acc[r][t]);
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 xp = bf16x2_to_f32x2(xw[q]);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) acc[r][t] = ffma2(wf[r][q], xp, acc[r][t]);
+                        }
                     }
                 }
             }

@@ -193,8 +193,9 @@ extern "C" int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, u
     g.K = K;
     g.bf16 = false;
     g.block_n = static_cast<int>(option_or(BSK_OPT_BLOCK_N, 256));
-    g.group_m = static_cast<int>(option_or(BSK_OPT_GROUP_M, 8));
     g.pair = option_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
+    // Tile-row group: measured best on GB300 for 8192^3-class and prefill shapes.
+    g.group_m = static_cast<int>(option_or(BSK_OPT_GROUP_M, g.pair && g.block_n == 256 ? 2 : 16));
     g.tma_store = aligned16(C) && (M % 8 == 0) && bsk_get_option(BSK_OPT_FORCE_DIRECT_STORE) != 1;
     const long long cap = option_or(BSK_OPT_NUM_SMS, d->sms);
     g.num_sms = static_cast<int>(cap < d->sms ? cap : d->sms);

@@ -134,7 +134,7 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
 /*
  * Tuning and test options (process-wide; not thread-safe; 0 restores the
  * default).  Keys:
- *   BSK_OPT_GROUP_M          GEMM tile-row group size (default 8)
+ *   BSK_OPT_GROUP_M          GEMM tile-row group size (default 2 for CTA pairs, 16 otherwise)
  *   BSK_OPT_BLOCK_N          GEMM tile width, 128 or 256 (default 256)
  *   BSK_OPT_FORCE_PACK       1: pack A and B even when aligned
  *   BSK_OPT_FORCE_DIRECT_STORE 1: masked register stores instead of the TMA store
