@@ -381,8 +381,8 @@ def run_ours(args):
         "dtype": "f16/bf16 in, f32 accumulate",
         "data": "synthetic (seeded PCG64: GEMM A,B uniform[-1,1] FP16; W N(0,0.02), x N(0,1) BF16)",
         "config": {"workload": WORKLOAD, "gemm": [GEMM_M, GEMM_N, GEMM_K], "gemv": [GEMV_M, GEMV_K, list(GEMV_NS)],
-                   "parallelism": f"replicas x{world}", "gemm_tile": [128, 256, 64],
-                   "gemm_stage_bytes": tile_stage_bytes(128, 256, 64),
+                   "parallelism": f"replicas x{world}", "gemm_tile": [256, 256, 64],
+                   "gemm_stage_bytes_per_sm": tile_stage_bytes(128, 128, 64),
                    "l2": "inputs larger than L2 (GEMM operands 537 MB; each GEMV reads its own 356 MB weight copy)"},
         "gemv": gemv,
         "e2e": {"value": round(world * gemm_flops() / e2e_gemm_s / 1e12, 2), "unit": "TFLOP/s",
@@ -393,11 +393,11 @@ def run_ours(args):
                      "unit": "TFLOP/s", "frac": round(per_launch_tflops / gemm_peak, 4),
                      "traffic": committed_traffic("gemm_f16_8192x8192x16384"),
                      "peak_source": f"{peak_src} bf16_tflops (FP16 dense rate = BF16 on this part)",
-                     "kernel": "gemm_tcgen05_kernel<256,true,false>"},
+                     "kernel": "gemm_tcgen05_pair_kernel<MN-major A, FP16> (CTA pairs, 256x256 tiles)"},
         "roofline_gemv": {"bound": "hbm", "achieved": round(gemv_n1_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                           "frac": round(gemv_n1_gbs / hbm_peak, 4),
                           "traffic": committed_traffic("gemv_bf16_34816x5120_n1"),
-                          "peak_source": f"{peak_src} hbm_gbs", "kernel": "gemv_bf16_kernel<1,...> (n=1)"},
+                          "peak_source": f"{peak_src} hbm_gbs", "kernel": "gemv_bf16_kernel<1, 4, 4> (n=1, register streaming)"},
         "gpu_launches": args.steps * (1 + len(GEMV_NS)),
         "clocks": clocks,
     }
