@@ -387,7 +387,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_FORCE_DIRECT_STORE: ok = value == 0 || value == 1; break;
     case BSK_OPT_GEMV_ROWS: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8; break;
     case BSK_OPT_GEMV_WARPS: ok = value >= 0 && value <= 16; break;
-    case BSK_OPT_GEMV_KERNEL: ok = value >= 0 && value <= 3; break;
+    case BSK_OPT_GEMV_KERNEL: ok = value >= 0 && value <= 4; break;
     case BSK_OPT_GEMM_KERNEL: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;

@@ -78,7 +78,8 @@ struct GemvLaunch {
     int M, K, n;
     int rows_per_warp;    // 0 = default for n
     int warps_per_block;  // 0 = default
-    int kernel;           // 0 = auto, 1 = register-streaming kernel, 2 = cp.async-pipelined kernel
+    int kernel;           // 0 = auto, 1 = register streaming, 2/3 = cp.async-pipelined (x FP32 / BF16),
+                          // 4 = token-paired accumulators
     int num_sms;
 };
 int launch_gemv(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);

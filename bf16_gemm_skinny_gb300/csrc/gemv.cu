@@ -423,6 +423,173 @@ __global__ void __launch_bounds__(512, 1)
     cp_async_wait<0>();
 }
 
+// ---------------------------------------------------------------------------
+// Token-paired variant for 5..8 tokens (padded to 8).
+//
+// With many tokens the FP32 FMAs, not HBM, set the pace; the accumulators of
+// the pipelined kernel are paired over k (two per row and token), which caps
+// the rows per warp at 4 within the register budget.  Here each fma.rn.f32x2
+// updates the accumulators of two tokens of one row, {w, w} * {x_t, x_t+1},
+// so R = 8 rows take 32 accumulator registers and every widened x pair is
+// reused by 8 rows.  x is staged token-interleaved: for chunk c and element e
+// (0..7), the 8 tokens' BF16 values form one 16-byte slot, placed at slot
+// e ^ (c & 7) so that lanes reading consecutive chunks spread over the banks.
+// ---------------------------------------------------------------------------
+template <int NT>
+__device__ __forceinline__ void stage_x_token_interleaved(const uint16_t* __restrict__ x, int K, int K8, uint4* xs4)
+{
+    for (int i = threadIdx.x; i < K8 * 8; i += blockDim.x) {
+        const int c = i >> 3;
+        const int e = i & 7;
+        const int k = c * 8 + e;
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t lo = (2 * p < NT) ? x[static_cast<long long>(2 * p) * K + k] : 0u;
+            const uint32_t hi = (2 * p + 1 < NT) ? x[static_cast<long long>(2 * p + 1) * K + k] : 0u;
+            w[p] = lo | (hi << 16);
+        }
+        xs4[c * 8 + (e ^ (c & 7))] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// bf16 value in the low (HI = false) or high half of a word -> {v, v}.
+template <bool HI>
+__device__ __forceinline__ float2 bf16_dup(uint32_t w)
+{
+    uint32_t v;
+    if constexpr (HI) {
+        asm("prmt.b32 %0, %1, 0, 0x3244;" : "=r"(v) : "r"(w));
+    } else {
+        asm("prmt.b32 %0, %1, 0, 0x1044;" : "=r"(v) : "r"(w));
+    }
+    return make_float2(__uint_as_float(v), __uint_as_float(v));
+}
+
+template <int NT, int R, int D>
+__global__ void __launch_bounds__(512, 1)
+    gemv_bf16_tokpair_kernel(const uint4* __restrict__ W4, const uint16_t* __restrict__ x,
+                             __nv_bfloat16* __restrict__ y, int M, int K, int groups_per_warp)
+{
+    static_assert(NT >= 1 && NT <= 8, "token-paired kernel takes up to 8 tokens");
+    extern __shared__ uint4 smem4[];
+    constexpr int V = next_pow2(R * 8);
+    constexpr uint32_t kSlotBytes = R * 512u;
+    const int K8 = K >> 3;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int warps = blockDim.x >> 5;
+    uint4* xs4 = smem4;
+    uint4* ring = smem4 + K8 * 8 + warp * D * R * 32;
+    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + lane * 16u;
+
+    stage_x_token_interleaved<NT>(x, K, K8, xs4);
+    __syncthreads();
+
+    const int num_groups = (M + R - 1) / R;
+    const int g_begin = (blockIdx.x * warps + warp) * groups_per_warp;
+    int g_count = num_groups - g_begin;
+    if (g_count > groups_per_warp) g_count = groups_per_warp;
+    if (g_count <= 0) return;
+    const int steps = (K8 + 31) >> 5;
+    const long long row_stride = K8;
+
+    int i_g = 0, i_s = 0, i_slot = 0;
+    const uint4* i_ptr = W4 + static_cast<long long>(g_begin) * R * row_stride + lane;
+    int i_rows = M - g_begin * R;
+    auto issue = [&]() {
+        if (i_g < g_count) {
+            const uint32_t dst = ring_s + static_cast<uint32_t>(i_slot) * kSlotBytes;
+            const bool kok = i_s * 32 + lane < K8;
+            if (kok && i_rows >= R) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) cp_async_16(dst + r * 512u, i_ptr + r * row_stride, 16u);
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const bool ok = kok && r < i_rows;
+                    cp_async_16(dst + r * 512u, ok ? i_ptr + r * row_stride : W4, ok ? 16u : 0u);
+                }
+            }
+            i_ptr += 32;
+            if (++i_s == steps) {
+                i_s = 0;
+                ++i_g;
+                i_ptr += R * row_stride - static_cast<long long>(steps) * 32;
+                i_rows -= R;
+            }
+            if (++i_slot == D) i_slot = 0;
+        }
+        cp_async_commit();
+    };
+
+#pragma unroll
+    for (int q = 0; q < D - 1; ++q) issue();
+
+    int c_slot = 0;
+    for (int gi = 0; gi < g_count; ++gi) {
+        float2 acc[R][4];   // acc[r][p] = {row r . token 2p, row r . token 2p+1}
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[r][p] = make_float2(0.f, 0.f);
+
+        for (int st = 0; st < steps; ++st) {
+            issue();
+            cp_async_wait<D - 1>();
+            const int c = st * 32 + lane;
+            if (c < K8) {
+                const uint4* slot = ring + c_slot * (R * 32) + lane;
+                uint4 w[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) w[r] = slot[r * 32];
+                const uint4* xc = xs4 + c * 8;
+                const int sw = c & 7;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 xv = xc[e ^ sw];
+                    const float2 xp[4] = {bf16x2_to_f32x2(xv.x), bf16x2_to_f32x2(xv.y), bf16x2_to_f32x2(xv.z),
+                                          bf16x2_to_f32x2(xv.w)};
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t word = (e >> 1) == 0 ? w[r].x : (e >> 1) == 1 ? w[r].y
+                                            : (e >> 1) == 2 ? w[r].z : w[r].w;
+                        const float2 wd = (e & 1) ? bf16_dup<true>(word) : bf16_dup<false>(word);
+#pragma unroll
+                        for (int p = 0; p < (NT + 1) / 2; ++p) acc[r][p] = ffma2(wd, xp[p], acc[r][p]);
+                    }
+                }
+            }
+            if (++c_slot == D) c_slot = 0;
+        }
+
+        const int row0 = (g_begin + gi) * R;
+        float v[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) v[i] = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                v[r * 8 + 2 * p] = acc[r][p].x;
+                v[r * 8 + 2 * p + 1] = acc[r][p].y;
+            }
+        warp_reduce_scatter<V>(v, lane);
+        if (result_owner<V>(lane)) {
+            constexpr int kHeld = V >= 32 ? V / 32 : 1;
+#pragma unroll
+            for (int i = 0; i < kHeld; ++i) {
+                const int idx = result_index<V>(lane, i);
+                const int r = idx >> 3;
+                const int t = idx & 7;
+                if (r < R && t < NT && row0 + r < M)
+                    y[static_cast<long long>(t) * M + row0 + r] = __float2bfloat16_rn(v[i]);
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
 // Scalar variant: any K, any alignment.  One warp per output row.
 template <int NT>
 __global__ void __launch_bounds__(256)
@@ -597,19 +764,87 @@ int try_launch_pipe_rows(const GemvLaunch& g, cudaStream_t stream, char* msg, si
     return try_launch_pipe<NT, R, D, false>(g, stream, msg, msg_len, status, min_warps);
 }
 
+// Token-paired kernel: x (K8 x 8 slots of 16 bytes) + one ring per warp.
+template <int NT, int R, int D>
+int try_launch_tokpair(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len, int* status)
+{
+    const int K8 = g.K / 8;
+    const long long x_bytes = static_cast<long long>(K8) * 128;
+    const long long per_warp_ring = static_cast<long long>(D) * R * 512;
+    const long long groups = (static_cast<long long>(g.M) + R - 1) / R;
+    int warps = 0;
+    if (g.warps_per_block > 0) {
+        if (x_bytes + g.warps_per_block * per_warp_ring <= kPipeMaxSmem) warps = g.warps_per_block;
+    } else {
+        double best = -1.0;
+        for (int w = 16; w >= 8; --w) {
+            if (x_bytes + w * per_warp_ring > kPipeMaxSmem) continue;
+            const long long slots = static_cast<long long>(g.num_sms) * w;
+            const long long per = (groups + slots - 1) / slots;
+            const double eff = static_cast<double>(groups) / static_cast<double>(per * slots);
+            if (eff > best + 1e-9) {
+                best = eff;
+                warps = w;
+            }
+        }
+    }
+    if (warps == 0) return 0;
+    const long long smem = x_bytes + warps * per_warp_ring;
+    auto kern = gemv_bf16_tokpair_kernel<NT, R, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        *status = 1;
+        return 1;
+    }
+    const long long max_warps = static_cast<long long>(g.num_sms) * warps;
+    const long long per_warp = (groups + max_warps - 1) / max_warps;
+    const long long warps_needed = (groups + per_warp - 1) / per_warp;
+    const long long grid = (warps_needed + warps - 1) / warps;
+    kern<<<static_cast<unsigned>(grid), warps * 32, smem, stream>>>(
+        reinterpret_cast<const uint4*>(g.W), g.x, reinterpret_cast<__nv_bfloat16*>(g.y), g.M, g.K,
+        static_cast<int>(per_warp));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "GEMV launch failed: %s", cudaGetErrorString(e));
+        *status = 1;
+        return 1;
+    }
+    *status = 0;
+    return 1;
+}
+
 // Kernel choice for the aligned path.  Measured on the 34816 x 5120 decode
 // shape: n <= 2 streams fastest from registers (the arithmetic is light and
-// the loads of U chunks per lane keep HBM busy); for n >= 3 the arithmetic per
-// byte grows and the cp.async ring keeps loads in flight while it runs, with x
-// in FP32 up to n = 4 and in BF16 (more warps fit) beyond.
+// the loads of U chunks per lane keep HBM busy); for n = 3..4 the cp.async
+// ring keeps loads in flight while the arithmetic runs (x in FP32); for
+// n >= 5 the FMAs dominate and the token-paired kernel does the fewest
+// instructions per weight.
 template <int NT>
 int launch_vec_any(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
-    const int kernel = g.kernel != 0 ? g.kernel : (NT <= 2 ? 1 : (NT <= 4 ? 2 : 3));
+    const int kernel = g.kernel != 0 ? g.kernel : (NT <= 2 ? 1 : (NT <= 4 ? 2 : 4));
+    if (kernel == 4) {
+        const int rows = g.rows_per_warp > 0 ? g.rows_per_warp : 8;
+        int status = 0;
+        int ran = 0;
+        switch (rows) {
+        case 4: ran = try_launch_tokpair<NT, 4, 3>(g, stream, msg, msg_len, &status); break;
+        case 8: ran = try_launch_tokpair<NT, 8, 2>(g, stream, msg, msg_len, &status); break;
+        default:
+            snprintf(msg, msg_len, "token-paired GEMV takes rows_per_warp 4 or 8, got %d", rows);
+            return 1;
+        }
+        if (ran) return status;
+        if (g.kernel == 4) {
+            snprintf(msg, msg_len, "token-paired GEMV does not fit in shared memory for K=%d", g.K);
+            return 1;
+        }
+    }
     const int rows = g.rows_per_warp > 0 ? g.rows_per_warp : 4;
-    if (kernel != 1) {
+    if (kernel == 2 || kernel == 3 || (kernel == 4)) {
         GemvLaunch gk = g;
-        gk.kernel = kernel;
+        gk.kernel = kernel == 4 ? 3 : kernel;
         int status = 0;
         int ran = 0;
         switch (rows) {
@@ -622,7 +857,7 @@ int launch_vec_any(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t m
             return 1;
         }
         if (ran) return status;
-        if (g.kernel >= 2) {
+        if (g.kernel == 2 || g.kernel == 3) {
             snprintf(msg, msg_len, "pipelined GEMV does not fit in shared memory for K=%d, n=%d", g.K, NT);
             return 1;
         }

@@ -145,8 +145,9 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_GEMM_KERNEL      GEMM kernel for 256-wide tiles: 1 one CTA per 128 x 256 tile,
  *                            2 CTA pairs on 256 x 256 tiles (default 2)
  *   BSK_OPT_GEMV_KERNEL      GEMV kernel: 1 register streaming, 2 cp.async-pipelined,
- *                            3 pipelined with x kept in BF16 (default: pipelined when x
- *                            and the ring fit in shared memory)
+ *                            3 pipelined with x kept in BF16, 4 token-paired (n >= 5)
+ *                            (default: 1 for n <= 2, 2 for n <= 4, 4 beyond; a kernel
+ *                            whose buffers do not fit in shared memory falls back)
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {

@@ -80,13 +80,16 @@ def test_every_token_count(n, M, K):
     check_tolerance(run(W, x, M, K, n), ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"{M}x{K} n={n}")
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
-@pytest.mark.parametrize("rows", [1, 2, 4, 8])
+GEMV_KERNEL_ROWS = [(k, r) for k in (1, 2, 3) for r in (1, 2, 4, 8)] + [(4, 4), (4, 8)]
+
+
+@pytest.mark.parametrize("kernel,rows", GEMV_KERNEL_ROWS)
 @pytest.mark.parametrize("warps", [1, 3, 8, 16])
-@pytest.mark.parametrize("n", [1, 3, 8])
+@pytest.mark.parametrize("n", [1, 3, 5, 8])
 def test_kernels_rows_per_warp_and_block_shape(kernel, rows, warps, n):
-    """Both GEMV kernels (register streaming, cp.async pipeline) at every rows-per-warp
-    and block shape give the oracle's bits on integer inputs."""
+    """Every GEMV kernel (register streaming, cp.async pipeline with FP32 or BF16 x,
+    token-paired) at its rows-per-warp and block shapes gives the oracle's bits on
+    integer inputs."""
     M, K = 2051, 2048
     W, x = operands(M, K, n, True)
     _, want = oracle.linear_bf16(W, x, M, K, n)
@@ -102,9 +105,9 @@ def test_kernels_rows_per_warp_and_block_shape(kernel, rows, warps, n):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
-@pytest.mark.parametrize("n", [1, 4, 8])
-def test_both_kernels_full_decode_shape(kernel, n):
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
+@pytest.mark.parametrize("n", [1, 4, 5, 8])
+def test_all_kernels_full_decode_shape(kernel, n):
     M, K = 34816, 5120
     W, x = operands(M, K, n, False)
     ref, _ = oracle.linear_bf16(W, x, M, K, n)
