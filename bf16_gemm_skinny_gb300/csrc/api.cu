@@ -216,8 +216,12 @@ int run_gemm(const uint16_t* A, bool a_mn_major, const uint16_t* B, uint16_t* C,
     g.N = N;
     g.K = K;
     g.bf16 = bf16;
-    g.block_n = static_cast<int>(opt_or(BSK_OPT_BLOCK_N, 256));
-    g.pair = opt_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
+    // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
+    // tile, deep ring: the weight stream sets the pace), else 256 on CTA pairs.
+    const long long bn_opt = opt_or(BSK_OPT_BLOCK_N, 0);
+    const int bn_auto = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+    g.block_n = static_cast<int>(bn_opt > 0 ? bn_opt : bn_auto);
+    g.pair = g.block_n == 256 && opt_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
     // Tile-row group: measured best on GB300 for 8192^3-class and prefill shapes.
     g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, g.pair && g.block_n == 256 ? 2 : 16));
     g.tma_store = aligned16(C) && (M % 8 == 0) && opt_or(BSK_OPT_FORCE_DIRECT_STORE, 0) == 0;
@@ -382,7 +386,7 @@ int bsk_set_option(int key, long long value)
     bool ok = true;
     switch (key) {
     case BSK_OPT_GROUP_M: ok = value >= 0 && value <= 65536; break;
-    case BSK_OPT_BLOCK_N: ok = value == 0 || value == 128 || value == 256; break;
+    case BSK_OPT_BLOCK_N: ok = value == 0 || value == 32 || value == 64 || value == 128 || value == 256; break;
     case BSK_OPT_FORCE_PACK:
     case BSK_OPT_FORCE_DIRECT_STORE: ok = value == 0 || value == 1; break;
     case BSK_OPT_GEMV_ROWS: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8; break;

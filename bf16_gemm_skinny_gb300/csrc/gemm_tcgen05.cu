@@ -43,7 +43,8 @@ constexpr int kEpiBox = 32;   // epilogue chunk: 32 rows x 32 columns per warp
 
 template <int BN>
 struct Cfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
+    // ring depth: as many stages as fit next to the epilogue buffers
+    static constexpr int kStages = BN == 256 ? 4 : BN == 128 ? 6 : BN == 64 ? 8 : 10;
     static constexpr int kABytes = kBM * kBK * 2;
     static constexpr int kBBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -659,7 +660,9 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 1;
     }
-    const int grid = p.num_tiles < g.num_sms ? p.num_tiles : g.num_sms;
+    // Every CTA gets the same number of tiles (the last wave is not left partial).
+    const int per_cta = (p.num_tiles + g.num_sms - 1) / g.num_sms;
+    const int grid = (p.num_tiles + per_cta - 1) / per_cta;
     kern<<<grid, kThreads, Cf::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -730,7 +733,8 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     }
     if (clusters > g.num_sms / 2) clusters = g.num_sms / 2;
     if (clusters < 1) clusters = 1;
-    const int pairs = p.num_tiles < clusters ? p.num_tiles : clusters;
+    const int per_pair = (p.num_tiles + clusters - 1) / clusters;
+    const int pairs = (p.num_tiles + per_pair - 1) / per_pair;
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
     if (e == cudaSuccess) e = cudaGetLastError();
@@ -766,7 +770,21 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_
         return g.bf16 ? launch_instance<128, false, true>(g, stream, msg, msg_len)
                       : launch_instance<128, false, false>(g, stream, msg, msg_len);
     }
-    snprintf(msg, msg_len, "unsupported block_n %d (128 or 256)", g.block_n);
+    if (g.block_n == 64) {
+        if (g.a_mn_major)
+            return g.bf16 ? launch_instance<64, true, true>(g, stream, msg, msg_len)
+                          : launch_instance<64, true, false>(g, stream, msg, msg_len);
+        return g.bf16 ? launch_instance<64, false, true>(g, stream, msg, msg_len)
+                      : launch_instance<64, false, false>(g, stream, msg, msg_len);
+    }
+    if (g.block_n == 32) {
+        if (g.a_mn_major)
+            return g.bf16 ? launch_instance<32, true, true>(g, stream, msg, msg_len)
+                          : launch_instance<32, true, false>(g, stream, msg, msg_len);
+        return g.bf16 ? launch_instance<32, false, true>(g, stream, msg, msg_len)
+                      : launch_instance<32, false, false>(g, stream, msg, msg_len);
+    }
+    snprintf(msg, msg_len, "unsupported block_n %d (32, 64, 128 or 256)", g.block_n);
     return 1;
 }
 

@@ -192,8 +192,12 @@ extern "C" int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, u
     g.N = N;
     g.K = K;
     g.bf16 = false;
-    g.block_n = static_cast<int>(option_or(BSK_OPT_BLOCK_N, 256));
-    g.pair = option_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
+    // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
+    // tile, deep ring: the weight stream sets the pace), else 256 on CTA pairs.
+    const long long bn_opt = option_or(BSK_OPT_BLOCK_N, 0);
+    const int bn_auto = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+    g.block_n = static_cast<int>(bn_opt > 0 ? bn_opt : bn_auto);
+    g.pair = g.block_n == 256 && option_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
     // Tile-row group: measured best on GB300 for 8192^3-class and prefill shapes.
     g.group_m = static_cast<int>(option_or(BSK_OPT_GROUP_M, g.pair && g.block_n == 256 ? 2 : 16));
     g.tma_store = aligned16(C) && (M % 8 == 0) && bsk_get_option(BSK_OPT_FORCE_DIRECT_STORE) != 1;

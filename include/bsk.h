@@ -135,7 +135,8 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  * Tuning and test options (process-wide; not thread-safe; 0 restores the
  * default).  Keys:
  *   BSK_OPT_GROUP_M          GEMM tile-row group size (default 2 for CTA pairs, 16 otherwise)
- *   BSK_OPT_BLOCK_N          GEMM tile width, 128 or 256 (default 256)
+ *   BSK_OPT_BLOCK_N          GEMM tile width 32, 64, 128 or 256 (default: the smallest of
+ *                            32/64/128 that covers N, else 256)
  *   BSK_OPT_FORCE_PACK       1: pack A and B even when aligned
  *   BSK_OPT_FORCE_DIRECT_STORE 1: masked register stores instead of the TMA store
  *   BSK_OPT_GEMV_ROWS        GEMV rows of W per warp: 1, 2, 4 or 8 (default by n)
@@ -143,7 +144,8 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_WAIT_LIMIT_US    device-side wait limit in microseconds (default 2 s)
  *   BSK_OPT_NUM_SMS          cap on the persistent GEMM grid (default: all SMs)
  *   BSK_OPT_GEMM_KERNEL      GEMM kernel for 256-wide tiles: 1 one CTA per 128 x 256 tile,
- *                            2 CTA pairs on 256 x 256 tiles (default 2)
+ *                            2 CTA pairs on 256 x 256 tiles (default 2; narrower tiles
+ *                            always run one CTA per 128 x BN tile)
  *   BSK_OPT_GEMV_KERNEL      GEMV kernel: 1 register streaming, 2 cp.async-pipelined,
  *                            3 pipelined with x kept in BF16, 4 token-paired (n >= 5)
  *                            (default: 1 for n <= 2, 2 for n <= 4, 4 beyond; a kernel

@@ -135,10 +135,11 @@ def test_8192x8192x16384_sampled(dist):
 
 
 @pytest.mark.parametrize("kernel,block_n,group_m", [
-    (2, 256, 8), (2, 256, 1), (2, 256, 3), (1, 256, 8), (1, 256, 3), (1, 128, 1), (1, 128, 12)])
+    (2, 256, 8), (2, 256, 1), (2, 256, 3), (1, 256, 8), (1, 256, 3), (1, 128, 1), (1, 128, 12),
+    (1, 64, 5), (1, 32, 2)])
 def test_result_independent_of_tile_config(kernel, block_n, group_m):
-    """CTA-pair 256x256 tiles, single-CTA 128x256 and 128x128 tiles, several
-    GROUP_M: bit-identical to the oracle on integer inputs."""
+    """CTA-pair 256x256 tiles, single-CTA 128x256 / 128x128 / 128x64 / 128x32 tiles,
+    several GROUP_M: bit-identical to the oracle on integer inputs."""
     M, N, K = 1000, 777, 1030
     A, B = operands(M, N, K, "int2")
     _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
@@ -154,7 +155,8 @@ def test_result_independent_of_tile_config(kernel, block_n, group_m):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (129, 257, 65), (1000, 777, 1030), (300, 517, 200)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (129, 257, 65), (1000, 777, 1030), (300, 517, 200),
+                                   (4096, 9, 1024), (1000, 33, 520), (2000, 100, 4096)])
 def test_single_cta_kernel(M, N, K):
     """The one-CTA-per-tile kernel stays correct beside the default CTA-pair kernel."""
     A, B = operands(M, N, K, "normal0.5")

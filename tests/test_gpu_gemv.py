@@ -138,7 +138,8 @@ def test_k_slabs(n):
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("M,K,n", [(1000, 520, 100), (256, 256, 9), (777, 1032, 300), (1024, 64, 4096)])
+@pytest.mark.parametrize("M,K,n", [(1000, 520, 100), (256, 256, 9), (777, 1032, 300), (1024, 64, 4096),
+                                   (3000, 2048, 12), (2048, 1024, 32), (1500, 512, 64), (1024, 5120, 128)])
 def test_prefill_medium(kernel, M, K, n):
     bsk.set_option("gemm_kernel", kernel)
     try:
@@ -174,6 +175,16 @@ def test_prefill_4096x34816x5120_sampled(integer):
     else:
         check_tolerance(got[ts, :], reft, "bf16", K, absmax_bf16(x), absmax_bf16(W), "prefill tokens")
         check_tolerance(got[:, js], refj, "bf16", K, absmax_bf16(x), absmax_bf16(W), "prefill features")
+
+
+@pytest.mark.parametrize("n", [9, 16, 64, 128])
+def test_skinny_34816x5120_full(n):
+    """Skinny tensor-core path (8 < n <= 128: one CTA per 128 x {32,64,128} tile) at the
+    decode shape, every output checked."""
+    M, K = 34816, 5120
+    W, x = operands(M, K, n, False)
+    ref, _ = oracle.linear_bf16(W, x, M, K, n)
+    check_tolerance(run(W, x, M, K, n), ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"skinny n={n}")
 
 
 def test_k_zero_and_empty():
