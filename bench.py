@@ -19,6 +19,8 @@ Reported (one JSON line, rank 0):
   roofline   for the dominant kernel (the GEMM) against the measured bf16
              peak (FP16 and BF16 dense rates are equal on this part), plus
              roofline_gemv against the measured HBM copy bandwidth.
+  other_configs  device time of the remaining workloads (256^3 and 4095x4097x4100
+             FP16 GEMMs, the 4096-token BF16 prefill projection), measured after the step.
   cpu_baseline  the oracle timed on a bounded sample on the host cores.
 
 ``--impl reference`` times the oracle (the plain CPU triple loop) on the same
@@ -248,6 +250,57 @@ def cpu_baseline(A, B, seconds: float):
 # our arm
 # ---------------------------------------------------------------------------
 
+def time_launches(fn, iters: int, warmup: int = 3) -> float:
+    """Mean device time (ms) of `fn`'s launches on the current stream, CUDA events."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for i in range(iters):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.fmean(evs[i].elapsed_time(evs[i + 1]) for i in range(iters))
+
+
+def other_configs(W_prefill, dev, peaks):
+    """Device time of the other workloads (256^3, the ragged 4095x4097x4100 GEMM
+    and the 4096-token prefill projection), each on its own seeded inputs."""
+    import numpy as np
+    import torch
+
+    from bf16_gemm_skinny_gb300 import _native as bsk
+    from bf16_gemm_skinny_gb300 import inputs
+
+    to_dev = lambda bits: torch.from_numpy(bits.view(np.int16)).to(dev)  # noqa: E731
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    out = {}
+    for name, (M, N, K, dist) in (("gemm_256x256x256", (256, 256, 256, "uniform")),
+                                   ("gemm_4095x4097x4100", (4095, 4097, 4100, "normal0.5"))):
+        A, B = inputs.gemm_operands(M, N, K, dist)
+        Ad, Bd = to_dev(A), to_dev(B)
+        C = torch.empty(M * N, dtype=torch.int16, device=dev)
+        ms = time_launches(lambda: bsk.gemm_f16_colmajor_enqueue(Ad, Bd, C, M, N, K), 20)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out[name] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1), "frac_of_peak": round(tf / peak_t, 4),
+                     "note": "includes the pack of unaligned operands" if M % 8 else ""}
+        del Ad, Bd, C
+    S = 4096
+    _, X = inputs.linear_operands(1, GEMV_K, S, "normal0.02", "normal1")
+    Xd = to_dev(X)
+    Y = torch.empty(S * GEMV_M, dtype=torch.int16, device=dev)
+    ms = time_launches(lambda: bsk.gemv_bf16_enqueue(W_prefill, Xd, Y, GEMV_M, GEMV_K, S), 10)
+    tf = 2.0 * S * GEMV_M * GEMV_K / (ms * 1e-3) / 1e12
+    out["prefill_4096x34816x5120"] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1),
+                                      "frac_of_peak": round(tf / peak_t, 4)}
+    bsk.stream_check()
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -391,6 +444,8 @@ def run_ours(args):
                 "note": "blocking C-ABI calls; H2D of A,B (GEMM) and W,x (GEMV) from pinned memory, D2H of C / y"},
         "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2), "peak": gemm_peak,
                      "unit": "TFLOP/s", "frac": round(per_launch_tflops / gemm_peak, 4),
+                     "frac_of_sustained": round(per_launch_tflops / float(
+                         peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])), 4),
                      "traffic": committed_traffic("gemm_f16_8192x8192x16384"),
                      "peak_source": f"{peak_src} bf16_tflops (FP16 dense rate = BF16 on this part)",
                      "kernel": "gemm_tcgen05_pair_kernel<MN-major A, FP16> (CTA pairs, 256x256 tiles)"},
@@ -401,6 +456,8 @@ def run_ours(args):
         "gpu_launches": args.steps * (1 + len(GEMV_NS)),
         "clocks": clocks,
     }
+    if not args.no_other_configs:
+        line["other_configs"] = other_configs(Ws[0], dev, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(A_h, B_h, args.cpu_seconds)
     if dist is not None:
@@ -509,6 +566,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip timing the 256^3, ragged and prefill workloads after the step")
     ap.add_argument("--case", help="profile mode: one kernel only, e.g. gemm:8192x8192x8192 or gemv:34816x5120x1")
     ap.add_argument("--opt", action="append", help="profile mode: library option name=value (repeatable)")
     args = ap.parse_args(argv)
