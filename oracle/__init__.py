@@ -11,6 +11,10 @@ compiles that file with gcc and marshals numpy arrays into it.
 
 Definitions followed:
 
+* DCU decode-GEMV article (forum.sourcefind.cn), sections 6.1 and 7: decode
+  attention over a paged KV cache, out = softmax(scale * q K^T) V per query
+  head, query head h reading KV head h / (num_q_heads / num_kv_heads).
+
 * "MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 2 (GEMM入门):
   C(m,n) = sum_k A(m,k) B(k,n), column-major A[m + k*M], B[k + n*K],
   C[m + n*M]; section 1 (规则分析): FP16 in, FP32 accumulate, FP16 out.
@@ -98,6 +102,10 @@ def _load():
         getattr(lib, name).argtypes = [u16p, u16p, i64, i64, i64, i64p, i64,
                                        f64p, u16p, ctypes.c_int]
         getattr(lib, name).restype = ctypes.c_int
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.orc_decode_attention_bf16.argtypes = [u16p, u16p, u16p, i32p, i32p, i64, i64, i64, i64, i64, i64, i64,
+                                              ctypes.c_double, f64p, u16p, ctypes.c_int]
+    lib.orc_decode_attention_bf16.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -252,3 +260,40 @@ def linear_bf16_tokens(W, X, M: int, K: int, n: int, ts, threads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle linear tokens failed ({rc})")
     return ref.reshape(t.size, M), out.reshape(t.size, M)
+
+
+# --------------------------------------------------------------------------
+# Decode attention over a paged BF16 KV cache
+# --------------------------------------------------------------------------
+
+def decode_attention_bf16(q, k_cache, v_cache, block_tables, seq_lens, num_q_heads: int, num_kv_heads: int,
+                          head_dim: int, block_size: int, scale: float, threads: int = 0):
+    """Oracle for out = softmax(scale * q K^T) V per (sequence, query head) over a paged cache.
+
+    ``q``: uint16 [num_seqs, num_q_heads, head_dim]; ``k_cache``/``v_cache``: uint16
+    [num_blocks, block_size, num_kv_heads, head_dim]; ``block_tables``: int32
+    [num_seqs, max_blocks]; ``seq_lens``: int32 [num_seqs].  Returns ``(ref, out)`` with the
+    float64 result and its BF16 bits, both [num_seqs, num_q_heads, head_dim].
+    """
+    q = _u16(q).reshape(-1)
+    kc = _u16(k_cache).reshape(-1)
+    vc = _u16(v_cache).reshape(-1)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32).reshape(-1)
+    num_seqs = sl.size
+    max_blocks = bt.shape[1] if bt.ndim == 2 else (bt.size // max(num_seqs, 1))
+    per_block = block_size * num_kv_heads * head_dim
+    num_blocks = kc.size // per_block if per_block else 0
+    if q.size != num_seqs * num_q_heads * head_dim or kc.size != vc.size or kc.size != num_blocks * per_block:
+        raise ValueError("oracle: attention operand sizes do not match")
+    ref = np.empty(num_seqs * num_q_heads * head_dim, np.float64)
+    out = np.empty(num_seqs * num_q_heads * head_dim, np.uint16)
+    i32 = ctypes.c_int32
+    rc = _load().orc_decode_attention_bf16(
+        _ptr(q, ctypes.c_uint16), _ptr(kc, ctypes.c_uint16), _ptr(vc, ctypes.c_uint16),
+        _ptr(bt, i32), _ptr(sl, i32), num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+        max_blocks, num_blocks, float(scale), _ptr(ref, ctypes.c_double), _ptr(out, ctypes.c_uint16), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle decode attention failed ({rc})")
+    shape = (num_seqs, num_q_heads, head_dim)
+    return ref.reshape(shape), out.reshape(shape)

@@ -19,6 +19,8 @@
  *    layer Y = X W^T with X:[n,k], W:[m,k], Y:[n,m] (all row-major), i.e.
  *    Y[t,j] = sum_k X[t,k] * W[j,k]; section 6.2: each Y[j] is one
  *    independent dot product over the whole k range.  BF16 in, BF16 out.
+ *  - Same article, sections 6.1 and 7: decode attention over a paged KV
+ *    cache (see orc_decode_attention_bf16 at the end of this file).
  *
  * How the oracle evaluates it:
  *  - Inputs arrive as raw 16-bit patterns and are decoded by this file's own
@@ -342,4 +344,93 @@ int orc_linear_bf16_tokens(const uint16_t* W, const uint16_t* X,
     free(xd);
     free(lut);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention over a paged BF16 KV cache                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * DCU decode-GEMV article (forum.sourcefind.cn), section 6.1: for one query
+ * head, scores[1,L] = Q K^T, prob = softmax(scores), out[1,D] = prob V, with K
+ * and V stored in a paged cache [block, token_in_block, kv_head, head_dim];
+ * section 7: 16 query heads share 4 KV heads (query head h reads KV head
+ * h / (num_q_heads / num_kv_heads)).  The page omits the score scale; it is an
+ * argument here (scores = scale * q.k).
+ *
+ * The oracle computes the definition directly, over the whole sequence, in
+ * double: the maximum score is subtracted before exponentiating (the same
+ * value mathematically), the weighted sum of V rows and the normaliser run over
+ * tokens in increasing order, and each output is rounded once to BF16.  A
+ * sequence of length 0 gives zeros.  Returns 3 if a block-table entry is out
+ * of range.
+ *
+ * q: [num_seqs, num_q_heads, hd]; out/ref: same shape;
+ * block_tables: [num_seqs, max_blocks]; seq_lens: [num_seqs].
+ */
+int orc_decode_attention_bf16(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                              const int32_t* block_tables, const int32_t* seq_lens,
+                              int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_heads, int64_t hd,
+                              int64_t block_size, int64_t max_blocks, int64_t num_blocks, double scale,
+                              double* ref, uint16_t* out, int threads)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || hd <= 0 || block_size <= 0) return 1;
+    if (num_q_heads % num_kv_heads != 0) return 1;
+    const int64_t group = num_q_heads / num_kv_heads;
+    double* lut = (double*)malloc(65536 * sizeof(double));
+    if (!lut) return 2;
+    orc_build_table(lut, 1);
+    orc_set_threads(threads);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        for (int64_t h = 0; h < num_q_heads; ++h) {
+            const int64_t L = seq_lens[s];
+            const int64_t g = h / group;
+            const uint16_t* qh = q + (s * num_q_heads + h) * hd;
+            double* acc = (double*)calloc((size_t)hd, sizeof(double));
+            double* sc = (double*)malloc((size_t)(L > 0 ? L : 1) * sizeof(double));
+            int64_t* rowbase = (int64_t*)malloc((size_t)(L > 0 ? L : 1) * sizeof(int64_t));
+            if (!acc || !sc || !rowbase) {
+#pragma omp atomic write
+                bad = 2;
+            } else {
+                double mx = -INFINITY;
+                for (int64_t t = 0; t < L; ++t) {
+                    const int64_t blk = block_tables[s * max_blocks + t / block_size];
+                    if (blk < 0 || blk >= num_blocks) {
+#pragma omp atomic write
+                        bad = 3;
+                        sc[t] = -INFINITY;
+                        rowbase[t] = -1;
+                        continue;
+                    }
+                    const int64_t base = ((blk * block_size + t % block_size) * num_kv_heads + g) * hd;
+                    rowbase[t] = base;
+                    double d = 0.0;
+                    for (int64_t e = 0; e < hd; ++e) d += lut[qh[e]] * lut[k_cache[base + e]];
+                    sc[t] = scale * d;
+                    if (sc[t] > mx) mx = sc[t];
+                }
+                double l = 0.0;
+                for (int64_t t = 0; t < L; ++t) {
+                    if (rowbase[t] < 0) continue;
+                    const double p = exp(sc[t] - mx);
+                    l += p;
+                    for (int64_t e = 0; e < hd; ++e) acc[e] += p * lut[v_cache[rowbase[t] + e]];
+                }
+                for (int64_t e = 0; e < hd; ++e) {
+                    const double o = (L > 0 && l > 0.0) ? acc[e] / l : 0.0;
+                    const int64_t idx = (s * num_q_heads + h) * hd + e;
+                    if (ref) ref[idx] = o;
+                    if (out) out[idx] = orc_bf16_encode_rn(o);
+                }
+            }
+            free(acc);
+            free(sc);
+            free(rowbase);
+        }
+    }
+    free(lut);
+    return bad;
 }

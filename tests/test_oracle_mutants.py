@@ -10,7 +10,10 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
-# (name, text to replace, replacement, count) -- each must occur in oracle.c
+PINS = "test_oracle_pins.py"
+ATTN_PINS = "test_oracle_attention_pins.py"
+
+# (name, text to replace, replacement, count[, pins file]) -- each must occur in oracle.c
 MUTANTS = [
     ("drop_last_k", "for (int64_t k = 0; k < K; ++k) {\n                    double b",
      "for (int64_t k = 0; k < K - 1; ++k) {\n                    double b", 1),
@@ -24,12 +27,21 @@ MUTANTS = [
      "return orc_round_to_format((double)(float)x, 7, 127, 255);", 1),
     ("linear_reversed_k", "acc += xr[k] * lut[wrow[k]];", "acc += xr[k] * lut[wrow[K - 1 - k]];", 2),
     ("f32_accumulator", "double* acc = (double*)malloc", "float* acc = (float*)malloc", 1),
+    ("attn_drop_last_token", "for (int64_t t = 0; t < L; ++t) {\n                    const int64_t blk",
+     "for (int64_t t = 0; t < L - 1; ++t) {\n                    const int64_t blk", 1, ATTN_PINS),
+    ("attn_wrong_group", "const int64_t g = h / group;", "const int64_t g = h % num_kv_heads;", 1, ATTN_PINS),
+    ("attn_no_max_subtraction", "const double p = exp(sc[t] - mx);", "const double p = exp(sc[t]);", 1, ATTN_PINS),
+    ("attn_wrong_block_offset", "((blk * block_size + t % block_size) * num_kv_heads + g) * hd",
+     "((blk * block_size + t / block_size) * num_kv_heads + g) * hd", 1, ATTN_PINS),
+    ("attn_ignores_scale", "sc[t] = scale * d;", "sc[t] = d;", 1, ATTN_PINS),
 ]
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,old,new,count", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_planted_mistake(tmp_path, name, old, new, count):
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, mutant):
+    name, old, new, count = mutant[:4]
+    pins = mutant[4] if len(mutant) > 4 else PINS
     src = open(SRC).read()
     assert src.count(old) == count, f"mutant {name}: pattern not found as expected"
     mutated = src.replace(old, new)
@@ -43,6 +55,6 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new, count):
     assert r.returncode == 0, r.stderr
     env = dict(os.environ, ORACLE_LIB_OVERRIDE=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", pins)],
                        capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
