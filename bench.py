@@ -21,6 +21,7 @@ Reported (one JSON line, rank 0):
              roofline_gemv against the measured HBM copy bandwidth.
   other_configs  device time of the remaining workloads (256^3 and 4095x4097x4100
              FP16 GEMMs, the 4096-token BF16 prefill projection), measured after the step.
+  decode_attention  split-KV decode attention at 8K/16K/32K tokens (KV-cache GB/s).
   cpu_baseline  the oracle timed on a bounded sample on the host cores.
 
 ``--impl reference`` times the oracle (the plain CPU triple loop) on the same
@@ -301,6 +302,41 @@ def other_configs(W_prefill, dev, peaks):
     return out
 
 
+def attention_configs(dev, hbm_peak):
+    """Split-KV decode attention at the page's head shape (16 query heads over 4 KV
+    heads, head_dim 256, 784-token pages) for 8K / 16K / 32K tokens, with the
+    automatic segment count and with the page's 16 / 32 rule."""
+    import numpy as np
+    import torch
+
+    from bf16_gemm_skinny_gb300 import _native as bsk
+    from bf16_gemm_skinny_gb300 import inputs
+
+    nqh, nkv, hd, bs = 16, 4, 256, 784
+    out = {}
+    for L in (8192, 16384, 32768):
+        nb = -(-L // bs)
+        n = nb * bs * nkv * hd
+        k = torch.from_numpy(inputs.to_bf16_bits(inputs.draw("normal1", n, 31)).view(np.int16)).to(dev)
+        v = torch.from_numpy(inputs.to_bf16_bits(inputs.draw("normal1", n, 32)).view(np.int16)).to(dev)
+        q = torch.from_numpy(inputs.to_bf16_bits(inputs.draw("normal1", nqh * hd, 33)).view(np.int16)).to(dev)
+        bt = torch.from_numpy(np.random.default_rng(34).permutation(nb).astype(np.int32)).to(dev)
+        sl = torch.tensor([L], dtype=torch.int32, device=dev)
+        o = torch.empty(nqh * hd, dtype=torch.int16, device=dev)
+        kv_bytes = L * nkv * hd * 2 * 2
+        row = {}
+        for name, segs in (("auto", 0), ("page_rule", 32 if L >= 12288 else 16)):
+            ms = time_launches(lambda: bsk.decode_attention_bf16_enqueue(
+                q, k, v, bt, sl, o, 1, nqh, nkv, hd, bs, nb, nb, L, 1.0 / 16.0, segs), 20)
+            gbs = kv_bytes / (ms * 1e-3) / 1e9
+            row[name] = {"segments": segs, "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                         "frac_of_hbm": round(gbs / hbm_peak, 4)}
+        out[f"L{L}"] = row
+        del k, v
+    bsk.stream_check()
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -458,6 +494,7 @@ def run_ours(args):
     }
     if not args.no_other_configs:
         line["other_configs"] = other_configs(Ws[0], dev, peaks)
+        line["decode_attention"] = attention_configs(dev, hbm_peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(A_h, B_h, args.cpu_seconds)
     if dist is not None:
@@ -542,6 +579,21 @@ def run_case(args):
         y = torch.empty(a * c, dtype=torch.int16, device=dev)
         call = lambda: bsk.gemv_bf16_enqueue(Wd, xd, y, a, b, c)  # noqa: E731
         work, unit = 2.0 * (a * b + c * b + c * a), "GB/s"
+    elif kind == "attn":
+        # attn:L x segments x 0 -> 16 query / 4 KV heads, head_dim 256, 784-token pages
+        L, segs = a, b
+        nqh, nkv, hd, bs = 16, 4, 256, 784
+        nb = -(-L // bs)
+        n = nb * bs * nkv * hd
+        kd = to_dev(inputs.to_bf16_bits(inputs.draw("normal1", n, 31)))
+        vd = to_dev(inputs.to_bf16_bits(inputs.draw("normal1", n, 32)))
+        qd = to_dev(inputs.to_bf16_bits(inputs.draw("normal1", nqh * hd, 33)))
+        btd = torch.arange(nb, dtype=torch.int32, device=dev)
+        sld = torch.tensor([L], dtype=torch.int32, device=dev)
+        od = torch.empty(nqh * hd, dtype=torch.int16, device=dev)
+        call = lambda: bsk.decode_attention_bf16_enqueue(  # noqa: E731
+            qd, kd, vd, btd, sld, od, 1, nqh, nkv, hd, bs, nb, nb, L, 1.0 / 16.0, segs)
+        work, unit = float(L * nkv * hd * 4), "GB/s"
     else:
         raise SystemExit(f"unknown case {args.case}")
     for _ in range(args.warmup):

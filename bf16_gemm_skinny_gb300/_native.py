@@ -45,6 +45,7 @@ EXPORTS = (
     "gemm_f16_colmajor", "gemv_bf16", "bsk_gemm_f16_colmajor_enqueue", "bsk_gemv_bf16_enqueue",
     "bsk_stream_check", "bsk_last_error", "bsk_status_string", "bsk_version", "bsk_tile_coord",
     "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout", "gemm_f16_colmajor_noalloc",
+    "decode_attention_bf16", "bsk_decode_attention_bf16_enqueue",
 )
 
 
@@ -77,6 +78,9 @@ def load():
             getattr(lib, name).restype = i
         for name in ("gemv_bf16", "bsk_gemv_bf16_enqueue"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
+            getattr(lib, name).restype = i
+        for name in ("decode_attention_bf16", "bsk_decode_attention_bf16_enqueue"):
+            getattr(lib, name).argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, i, ctypes.c_float, i, p]
             getattr(lib, name).restype = i
         lib.bsk_stream_check.argtypes = [p]
         lib.bsk_stream_check.restype = i
@@ -149,6 +153,27 @@ def gemv_bf16(W, x, y, M: int, K: int, n: int, stream=None) -> None:
 def gemv_bf16_enqueue(W, x, y, M: int, K: int, n: int, stream=None) -> None:
     """Asynchronous variant of gemv_bf16 (check with stream_check)."""
     _check(load().bsk_gemv_bf16_enqueue(_addr(W), _addr(x), _addr(y), M, K, n, _stream(stream)))
+
+
+def decode_attention_bf16(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs: int, num_q_heads: int,
+                          num_kv_heads: int, head_dim: int, block_size: int, max_blocks: int, num_blocks: int,
+                          max_seq_len: int, softmax_scale: float, num_segments: int = 0, stream=None) -> None:
+    """Split-KV decode attention over a paged BF16 cache (see include/bsk.h); blocks until done."""
+    _check(load().decode_attention_bf16(_addr(q), _addr(k_cache), _addr(v_cache), _addr(block_tables),
+                                        _addr(seq_lens), _addr(out), num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                        block_size, max_blocks, num_blocks, max_seq_len, softmax_scale,
+                                        num_segments, _stream(stream)))
+
+
+def decode_attention_bf16_enqueue(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs: int,
+                                  num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                                  max_blocks: int, num_blocks: int, max_seq_len: int, softmax_scale: float,
+                                  num_segments: int = 0, stream=None) -> None:
+    """Asynchronous variant of decode_attention_bf16."""
+    _check(load().bsk_decode_attention_bf16_enqueue(
+        _addr(q), _addr(k_cache), _addr(v_cache), _addr(block_tables), _addr(seq_lens), _addr(out), num_seqs,
+        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, max_seq_len, softmax_scale,
+        num_segments, _stream(stream)))
 
 
 def stream_check(stream=None) -> None:

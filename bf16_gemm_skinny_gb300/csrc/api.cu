@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -115,6 +116,8 @@ int check_status_word()
     const int code = *g_status_host;
     if (code != 0) {
         *g_status_host = 0;
+        if (code == bsk::kDevErrBadIndex)
+            return fail(BSK_ERR_INVALID_ARG, "a block-table entry was out of range; its tokens were skipped");
         return fail(BSK_ERR_TIMEOUT, "a device-side wait gave up (site %d); the output is undefined",
                     code - bsk::kDevErrTimeoutBase);
     }
@@ -295,6 +298,89 @@ int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, 
     return run_gemm(W, false, x, y, M, n, K, true, sms, s);
 }
 
+int enqueue_decode_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                             const int32_t* block_tables, const int32_t* seq_lens, uint16_t* out, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                             int num_blocks, int max_seq_len, float softmax_scale, int num_segments, void* stream)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 || max_blocks <= 0 ||
+        num_blocks <= 0 || max_seq_len < 0)
+        return fail(BSK_ERR_INVALID_ARG, "bad attention sizes (seqs=%d q_heads=%d kv_heads=%d block_size=%d "
+                    "max_blocks=%d num_blocks=%d max_seq_len=%d)", num_seqs, num_q_heads, num_kv_heads, block_size,
+                    max_blocks, num_blocks, max_seq_len);
+    if (num_q_heads % num_kv_heads != 0)
+        return fail(BSK_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)", num_q_heads,
+                    num_kv_heads);
+    if (num_seqs > 65535 || num_kv_heads > 65535)
+        return fail(BSK_ERR_INVALID_ARG, "num_seqs and num_kv_heads must be at most 65535");
+    const int group = num_q_heads / num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8)
+        return fail(BSK_ERR_INVALID_ARG, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", group);
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(BSK_ERR_INVALID_ARG, "head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    if (static_cast<long long>(max_seq_len) > static_cast<long long>(max_blocks) * block_size)
+        return fail(BSK_ERR_INVALID_ARG, "max_seq_len %d exceeds max_blocks * block_size", max_seq_len);
+    if (num_segments < 0 || num_segments > 1024)
+        return fail(BSK_ERR_INVALID_ARG, "num_segments %d out of range (0 = automatic, else 1..1024)", num_segments);
+    if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+        return fail(BSK_ERR_INVALID_ARG, "softmax_scale must be finite");
+    if (num_seqs == 0) return BSK_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+        return fail(BSK_ERR_INVALID_ARG, "a pointer argument is NULL");
+    const size_t row_align = static_cast<size_t>(head_dim) * 2 / 32;   // bytes each lane loads
+    const uintptr_t mask = row_align - 1;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+         reinterpret_cast<uintptr_t>(v_cache)) & mask)
+        return fail(BSK_ERR_INVALID_ARG, "q, k_cache and v_cache must be %zu-byte aligned", row_align);
+    const size_t q_bytes = static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 2;
+    const size_t cache_bytes = static_cast<size_t>(num_blocks) * block_size * num_kv_heads * head_dim * 2;
+    if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k_cache, cache_bytes) ||
+        overlaps(out, q_bytes, v_cache, cache_bytes))
+        return fail(BSK_ERR_INVALID_ARG, "out overlaps an input");
+    int sms = 0;
+    int st = prepare_device(&sms);
+    if (st != BSK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Segments: as given (16 / 32 is the page's rule for its 80-CU part), else enough
+    // CTAs for about two per SM on this GPU, each segment at least 64 tokens long.
+    int segs = num_segments;
+    if (segs <= 0) {
+        const long long heads = static_cast<long long>(num_seqs) * num_kv_heads;
+        long long want = (2LL * sms + heads - 1) / heads;
+        const long long cap = (max_seq_len + 63) / 64;
+        if (want > cap) want = cap;
+        if (want < 1) want = 1;
+        if (want > 1024) want = 1024;
+        segs = static_cast<int>(want);
+    }
+    Workspace ws;
+    const size_t ws_bytes = static_cast<size_t>(num_seqs) * num_q_heads * segs * (head_dim + 2) * sizeof(float);
+    st = alloc_workspace(ws, ws_bytes, s);
+    if (st != BSK_OK) return st;
+    bsk::AttnLaunch a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.workspace = static_cast<float*>(ws.ptr);
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.num_segments = segs;
+    a.scale = softmax_scale;
+    a.status = g_status_dev;
+    char msg[512] = "";
+    if (bsk::launch_decode_attention(a, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
+    return BSK_OK;
+}
+
 }  // namespace
 
 namespace bsk {
@@ -347,6 +433,29 @@ int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t
 int bsk_gemv_bf16_enqueue(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream)
 {
     return enqueue_gemv_bf16(W, x, y, M, K, n, stream);
+}
+
+int decode_attention_bf16(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                          const int32_t* block_tables, const int32_t* seq_lens, uint16_t* out, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                          int num_blocks, int max_seq_len, float softmax_scale, int num_segments, void* stream)
+{
+    int st = enqueue_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs, num_q_heads,
+                                      num_kv_heads, head_dim, block_size, max_blocks, num_blocks, max_seq_len,
+                                      softmax_scale, num_segments, stream);
+    if (st != BSK_OK || num_seqs == 0) return st;
+    return sync_and_check(static_cast<cudaStream_t>(stream));
+}
+
+int bsk_decode_attention_bf16_enqueue(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                      const int32_t* block_tables, const int32_t* seq_lens, uint16_t* out,
+                                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                      int max_blocks, int num_blocks, int max_seq_len, float softmax_scale,
+                                      int num_segments, void* stream)
+{
+    return enqueue_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs, num_q_heads,
+                                    num_kv_heads, head_dim, block_size, max_blocks, num_blocks, max_seq_len,
+                                    softmax_scale, num_segments, stream);
 }
 
 int bsk_stream_check(void* stream)

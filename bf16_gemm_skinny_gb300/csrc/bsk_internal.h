@@ -12,6 +12,9 @@ namespace bsk {
 // Code a kernel writes into the device status word when a bounded wait gives
 // up: kDevErrTimeoutBase + the number of the wait site (0 = no error).
 constexpr int kDevErrTimeoutBase = 0x100;
+// Code a kernel writes when an index it reads from the caller (a block-table
+// entry) is out of range; the access is skipped.
+constexpr int kDevErrBadIndex = 0x200;
 
 // Grouped ordering of output tiles ("Hygon 优化", section 分组调度：提高 L2 数据复用):
 // the 2-D grid of num_m x num_n tiles is flattened so that consecutive tile
@@ -83,6 +86,22 @@ struct GemvLaunch {
     int num_sms;
 };
 int launch_gemv(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
+
+// Split-KV decode attention over a paged BF16 cache (see attention.cu).
+struct AttnLaunch {
+    const uint16_t* q;            // [num_seqs, num_q_heads, head_dim]
+    const uint16_t* k_cache;      // [num_blocks, block_size, num_kv_heads, head_dim]
+    const uint16_t* v_cache;
+    const int32_t* block_tables;  // [num_seqs, max_blocks]
+    const int32_t* seq_lens;      // [num_seqs]
+    uint16_t* out;                // [num_seqs, num_q_heads, head_dim]
+    float* workspace;             // num_seqs * num_q_heads * num_segments * (head_dim + 2) floats
+    int num_seqs, num_q_heads, num_kv_heads, head_dim;
+    int block_size, max_blocks, num_blocks, max_seq_len, num_segments;
+    float scale;
+    int* status;
+};
+int launch_decode_attention(const AttnLaunch& a, cudaStream_t stream, char* msg, size_t msg_len);
 
 // Copy an `outer` x `inner` matrix of 16-bit elements (inner contiguous) from
 // leading dimension ld_src to ld_dst.  The source is only read.

@@ -76,6 +76,39 @@ int gemm_f16_colmajor(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, 
 int gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);
 
 /*
+ * Decode attention over a paged BF16 KV cache, split along the sequence and
+ * merged with a numerically stable softmax reduction.  Definition: DCU
+ * decode-GEMV article (forum.sourcefind.cn), section 6.1: per query head,
+ * out = softmax(scale * q K^T) V over the sequence's tokens; section 6.3: the
+ * tokens are cut into contiguous segments whose local (max, sum, prob V) are
+ * merged by rescaling with exp(local max - global max); section 7: query head
+ * h reads KV head h / (num_q_heads / num_kv_heads).  The page omits the score
+ * scale; pass it (1/sqrt(head_dim) is usual; 1.0 gives the literal formula).
+ *
+ *   q            [num_seqs, num_q_heads, head_dim] BF16 (device)
+ *   k_cache      [num_blocks, block_size, num_kv_heads, head_dim] BF16 (device)
+ *   v_cache      same layout as k_cache
+ *   block_tables [num_seqs, max_blocks] int32 (device): physical block of each
+ *                block_size-token chunk of a sequence
+ *   seq_lens     [num_seqs] int32 (device): tokens per sequence (clamped to
+ *                [0, max_seq_len]; a sequence of length 0 gives zeros)
+ *   out          [num_seqs, num_q_heads, head_dim] BF16 (device)
+ *   num_segments segments per sequence, 1..1024 (the page chooses 16, or 32 once
+ *                max_seq_len >= 12288, for its 80-CU part); 0 = automatic: about
+ *                two CTAs per SM of this GPU, each segment >= 64 tokens
+ * head_dim 64, 128 or 256; num_q_heads / num_kv_heads 1, 2, 4 or 8; q, k_cache,
+ * v_cache aligned to head_dim/16 bytes.  FP32 accumulation, output rounded to
+ * nearest even.  A workspace of num_seqs * num_q_heads * segments *
+ * (head_dim + 2) floats is allocated in stream order.  A block-table entry
+ * outside [0, num_blocks) is skipped and reported as BSK_ERR_INVALID_ARG by
+ * the blocking call (or the next bsk_stream_check).
+ */
+int decode_attention_bf16(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                          const int32_t* block_tables, const int32_t* seq_lens, uint16_t* out, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                          int num_blocks, int max_seq_len, float softmax_scale, int num_segments, void* stream);
+
+/*
  * gemm_f16_colmajor for callers that cannot allocate device memory during a
  * call (for example a serving process whose own allocator reserved all free
  * HBM at start-up, or a program held to a device-memory budget fixed when it
@@ -99,7 +132,7 @@ int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, uint16_t* C,
                               void* stream);
 
 /*
- * Same work as gemm_f16_colmajor / gemv_bf16, but asynchronous: validates the
+ * Same work as gemm_f16_colmajor / gemv_bf16 / decode_attention_bf16, but asynchronous: validates the
  * arguments, launches on `stream` and returns without waiting.  A device-side
  * watchdog timeout raised by this work is reported by the next
  * bsk_stream_check() (or the next blocking call).  Buffers must stay alive
@@ -108,6 +141,11 @@ int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, uint16_t* C,
 int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
                                   void* stream);
 int bsk_gemv_bf16_enqueue(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);
+int bsk_decode_attention_bf16_enqueue(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                      const int32_t* block_tables, const int32_t* seq_lens, uint16_t* out,
+                                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                      int max_blocks, int num_blocks, int max_seq_len, float softmax_scale,
+                                      int num_segments, void* stream);
 
 /* Synchronise `stream`, then report BSK_ERR_CUDA for a pending CUDA error or
  * BSK_ERR_TIMEOUT if a device-side wait gave up since the last check. */
