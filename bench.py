@@ -422,14 +422,15 @@ def run_ours(args):
     barrier(dist, dev)
     torch.cuda.synchronize()
     e2e_gemm, e2e_gemv = [], {n: [] for n in GEMV_NS}
-    for _ in range(e2e_steps):
+    for it in range(e2e_steps + 1):            # the first pass warms the copy paths, untimed
         t0 = time.perf_counter()
         A.copy_(A_p, non_blocking=True)
         B.copy_(B_p, non_blocking=True)
         bsk.gemm_f16_colmajor(A, B, C, GEMM_M, GEMM_N, GEMM_K, stream)
         C_p.copy_(C, non_blocking=True)
         torch.cuda.synchronize()
-        e2e_gemm.append(time.perf_counter() - t0)
+        if it:
+            e2e_gemm.append(time.perf_counter() - t0)
         for i, n in enumerate(GEMV_NS):
             t0 = time.perf_counter()
             Ws[i].copy_(W_p, non_blocking=True)
@@ -437,9 +438,10 @@ def run_ours(args):
             bsk.gemv_bf16(Ws[i], xs[n], ys[n], GEMV_M, GEMV_K, n, stream)
             y_p[n].copy_(ys[n], non_blocking=True)
             torch.cuda.synchronize()
-            e2e_gemv[n].append(time.perf_counter() - t0)
-    e2e_gemm_s = max_over_ranks(statistics.fmean(e2e_gemm), dist, dev)
-    e2e_gemv_s = {n: max_over_ranks(statistics.fmean(v), dist, dev) for n, v in e2e_gemv.items()}
+            if it:
+                e2e_gemv[n].append(time.perf_counter() - t0)
+    e2e_gemm_s = max_over_ranks(statistics.median(e2e_gemm), dist, dev)
+    e2e_gemv_s = {n: max_over_ranks(statistics.median(v), dist, dev) for n, v in e2e_gemv.items()}
 
     peaks, peak_src = load_peaks()
     value = whole_job_rate(gemm_flops(), gemm_ms_mean * 1e-3, dist, dev) / 1e12
