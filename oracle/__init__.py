@@ -102,6 +102,10 @@ def _load():
         getattr(lib, name).argtypes = [u16p, u16p, i64, i64, i64, i64p, i64,
                                        f64p, u16p, ctypes.c_int]
         getattr(lib, name).restype = ctypes.c_int
+    ci = ctypes.c_int
+    lib.orc_gemm_f16_general.argtypes = [ci, ci, ci, u16p, i64, u16p, i64, i64, i64, i64, u16p, ci,
+                                         i64p, i64, i64p, i64, f64p, u16p, ci]
+    lib.orc_gemm_f16_general.restype = ctypes.c_int
     i32p = ctypes.POINTER(ctypes.c_int32)
     lib.orc_decode_attention_bf16.argtypes = [u16p, u16p, u16p, i32p, i32p, i64, i64, i64, i64, i64, i64, i64,
                                               ctypes.c_double, f64p, u16p, ctypes.c_int]
@@ -213,6 +217,50 @@ def gemm_f16_colmajor_rows(A, B, M: int, N: int, K: int, rows, threads: int = 0)
         _ptr(ref, ctypes.c_double), _ptr(out, ctypes.c_uint16), threads)
     if rc != 0:
         raise RuntimeError(f"oracle gemm rows failed ({rc})")
+    return ref, out
+
+
+def gemm_f16_general(A, B, M: int, N: int, K: int, lda: int, ldb: int, transa: int = 0, transb: int = 0,
+                     row_major: int = 0, bias=None, bias_mode: int = 0, rows=None, cols=None, threads: int = 0):
+    """Oracle for the FP16 GEMM in any storage form, with an optional bias.
+
+    C(m,n) = fp16_rn(sum_k op(A)(m,k) op(B)(k,n) + bias), op() the BLAS
+    transposition flags, every stored matrix addressed column-major
+    (``row_major=0``: (r,c) at r + c*ld) or row-major (``row_major=1``: (r,c)
+    at c + r*ld).  ``bias_mode`` 1: bias[m], 2: bias[n] (FP16 bits).
+    Returns ``(ref, out)`` for the selected rows (all M when None) x columns
+    (all N when None), flat and column-major over the selection.
+    """
+    A = _u16(A).reshape(-1)
+    B = _u16(B).reshape(-1)
+
+    def span(r, c, ld):  # elements a stored r x c matrix reaches
+        if r == 0 or c == 0:
+            return 0
+        return (r - 1) + (c - 1) * ld + 1 if not row_major else (c - 1) + (r - 1) * ld + 1
+
+    ar, ac = (K, M) if transa else (M, K)
+    br, bc = (N, K) if transb else (K, N)
+    if A.size < span(ar, ac, lda) or B.size < span(br, bc, ldb):
+        raise ValueError("oracle: operands smaller than their shapes and leading dimensions")
+    bz = None
+    if bias_mode:
+        bz = _u16(bias).reshape(-1)
+        if bz.size < (M if bias_mode == 1 else N):
+            raise ValueError("oracle: bias too short")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else r.size
+    nc = N if c is None else c.size
+    ref = np.empty(nr * nc, np.float64)
+    out = np.empty(nr * nc, np.uint16)
+    rc = _load().orc_gemm_f16_general(
+        row_major, transa, transb, _ptr(A, ctypes.c_uint16), lda, _ptr(B, ctypes.c_uint16), ldb, M, N, K,
+        _ptr(bz, ctypes.c_uint16), bias_mode,
+        _ptr(r, ctypes.c_int64), 0 if r is None else r.size, _ptr(c, ctypes.c_int64), 0 if c is None else c.size,
+        _ptr(ref, ctypes.c_double), _ptr(out, ctypes.c_uint16), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle general gemm failed ({rc})")
     return ref, out
 
 

@@ -21,6 +21,10 @@
  *    independent dot product over the whole k range.  BF16 in, BF16 out.
  *  - Same article, sections 6.1 and 7: decode attention over a paged KV
  *    cache (see orc_decode_attention_bf16 at the end of this file).
+ *  - The FP16 GEMM in other storage forms (transposed operands, row-major
+ *    storage, any leading dimension) with an optional bias: the BLAS reading
+ *    of section 2's GEMM, with the bias the DCU article's section 6.1 names
+ *    as a property of the linear call (see orc_gemm_f16_general).
  *
  * How the oracle evaluates it:
  *  - Inputs arrive as raw 16-bit patterns and are decoded by this file's own
@@ -264,6 +268,91 @@ int orc_gemm_f16_colmajor_rows(const uint16_t* A, const uint16_t* B,
     free(arow);
     free(lut);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* General FP16 GEMM: C = op(A) op(B) [+ bias], any storage order and strides */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Element addressing of a stored matrix.  `row_major` == 0: entry (r, c) at
+ * P[r + c*ld] (the column-major storage of the MTT article, section 2);
+ * `row_major` == 1: entry (r, c) at P[c + r*ld].
+ */
+static int64_t orc_at(int row_major, int64_t r, int64_t c, int64_t ld)
+{
+    return row_major ? c + r * ld : r + c * ld;
+}
+
+/*
+ * The BLAS reading of the layouts (one FP16 GEMM, other storage forms):
+ *   op(A)(m,k) = A_stored(m,k) when transa == 0, A_stored(k,m) when transa == 1;
+ *   op(B)(k,n) = B_stored(k,n) when transb == 0, B_stored(n,k) when transb == 1;
+ * every stored matrix addressed through orc_at with the call's storage order
+ * and its leading dimension.  The optional bias (FP16 bits) is bias[m]
+ * (bias_mode 1, one value per row of C) or bias[n] (bias_mode 2, one value
+ * per column); it is added to the exact double sum, so the entry is still
+ * rounded once:
+ *   C(m,n) = fp16_rn( sum_{k ascending} op(A)(m,k) op(B)(k,n) + bias ).
+ *
+ * Computes rows `rows[0..nrows)` (all M when rows is NULL) of columns
+ * `cols[0..ncols)` (all N when cols is NULL); selected entry (i, j) goes to
+ * ref[i + j*nr] / out[i + j*nr], nr the number of selected rows, regardless
+ * of `row_major` (the selection is always returned column-major).
+ */
+int orc_gemm_f16_general(int row_major, int transa, int transb,
+                         const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                         int64_t M, int64_t N, int64_t K,
+                         const uint16_t* bias, int bias_mode,
+                         const int64_t* rows, int64_t nrows, const int64_t* cols, int64_t ncols,
+                         double* ref, uint16_t* out, int threads)
+{
+    if (M < 0 || N < 0 || K < 0) return 1;
+    if (bias_mode < 0 || bias_mode > 2 || (bias_mode != 0 && !bias)) return 1;
+    int64_t nr = rows ? nrows : M;
+    int64_t nc = cols ? ncols : N;
+    double* lut = (double*)malloc(65536 * sizeof(double));
+    if (!lut) return 2;
+    orc_build_table(lut, 0);
+    orc_set_threads(threads);
+    int fail = 0;
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc((size_t)(nr > 0 ? nr : 1) * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            fail = 2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t j = 0; j < nc; ++j) {
+            if (!acc) continue;
+            int64_t n = cols ? cols[j] : j;
+            for (int64_t i = 0; i < nr; ++i) acc[i] = 0.0;
+            if (n >= 0 && n < N) {
+                for (int64_t k = 0; k < K; ++k) {
+                    int64_t bi = transb ? orc_at(row_major, n, k, ldb) : orc_at(row_major, k, n, ldb);
+                    double b = lut[B[bi]];
+                    for (int64_t i = 0; i < nr; ++i) {
+                        int64_t m = rows ? rows[i] : i;
+                        if (m < 0 || m >= M) continue;
+                        int64_t ai = transa ? orc_at(row_major, k, m, lda) : orc_at(row_major, m, k, lda);
+                        acc[i] += lut[A[ai]] * b;
+                    }
+                }
+            }
+            for (int64_t i = 0; i < nr; ++i) {
+                int64_t m = rows ? rows[i] : i;
+                double v = acc[i];
+                if (bias_mode == 1 && m >= 0 && m < M) v += lut[bias[m]];
+                if (bias_mode == 2 && n >= 0 && n < N) v += lut[bias[n]];
+                if (ref) ref[i + j * nr] = v;
+                if (out) out[i + j * nr] = orc_f16_encode_rn(v);
+            }
+        }
+        free(acc);
+    }
+    free(lut);
+    return fail;
 }
 
 /* ------------------------------------------------------------------------ */

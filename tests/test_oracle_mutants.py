@@ -12,6 +12,7 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 PINS = "test_oracle_pins.py"
 ATTN_PINS = "test_oracle_attention_pins.py"
+LAYOUT_PINS = "test_oracle_layout_pins.py"
 
 # (name, text to replace, replacement, count[, pins file]) -- each must occur in oracle.c
 MUTANTS = [
@@ -34,6 +35,16 @@ MUTANTS = [
     ("attn_wrong_block_offset", "((blk * block_size + t % block_size) * num_kv_heads + g) * hd",
      "((blk * block_size + t / block_size) * num_kv_heads + g) * hd", 1, ATTN_PINS),
     ("attn_ignores_scale", "sc[t] = scale * d;", "sc[t] = d;", 1, ATTN_PINS),
+    ("general_transb_ignored", "int64_t bi = transb ? orc_at(row_major, n, k, ldb) : orc_at(row_major, k, n, ldb);",
+     "int64_t bi = orc_at(row_major, k, n, ldb);", 1, LAYOUT_PINS),
+    ("general_row_major_swapped", "return row_major ? c + r * ld : r + c * ld;",
+     "return row_major ? r + c * ld : c + r * ld;", 1, LAYOUT_PINS),
+    ("general_lda_ignored", "orc_at(row_major, k, m, lda) : orc_at(row_major, m, k, lda)",
+     "orc_at(row_major, k, m, K) : orc_at(row_major, m, k, M)", 1, LAYOUT_PINS),
+    ("general_bias_first_only", "v += lut[bias[m]];", "v += lut[bias[0]];", 1, LAYOUT_PINS),
+    ("general_bias_after_rounding", "if (out) out[i + j * nr] = orc_f16_encode_rn(v);",
+     "if (out) out[i + j * nr] = orc_f16_encode_rn(lut[orc_f16_encode_rn(acc[i])] + (v - acc[i]));", 1,
+     LAYOUT_PINS),
 ]
 
 
