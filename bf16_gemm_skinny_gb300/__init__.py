@@ -7,9 +7,18 @@ tcgen05/TMA and SIMT kernels); this package holds its thin ctypes binding
 of a binding function does, and it raises if the library is missing.
 """
 from ._native import (  # noqa: F401
+    BIAS_COLUMN,
+    BIAS_NONE,
+    BIAS_ROW,
+    COL_MAJOR,
+    ROW_MAJOR,
     BskError,
+    decode_attention_bf16,
+    gemm_f16,
     gemm_f16_colmajor,
     gemm_f16_colmajor_enqueue,
+    gemm_f16_colmajor_noalloc,
+    gemm_f16_enqueue,
     gemv_bf16,
     gemv_bf16_enqueue,
     last_error,

@@ -45,8 +45,11 @@ EXPORTS = (
     "gemm_f16_colmajor", "gemv_bf16", "bsk_gemm_f16_colmajor_enqueue", "bsk_gemv_bf16_enqueue",
     "bsk_stream_check", "bsk_last_error", "bsk_status_string", "bsk_version", "bsk_tile_coord",
     "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout", "gemm_f16_colmajor_noalloc",
-    "decode_attention_bf16", "bsk_decode_attention_bf16_enqueue",
+    "decode_attention_bf16", "bsk_decode_attention_bf16_enqueue", "gemm_f16", "bsk_gemm_f16_enqueue",
 )
+
+COL_MAJOR, ROW_MAJOR = 0, 1
+BIAS_NONE, BIAS_ROW, BIAS_COLUMN = 0, 1, 2
 
 
 class BskError(RuntimeError):
@@ -75,6 +78,9 @@ def load():
         i = ctypes.c_int
         for name in ("gemm_f16_colmajor", "bsk_gemm_f16_colmajor_enqueue", "gemm_f16_colmajor_noalloc"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
+            getattr(lib, name).restype = i
+        for name in ("gemm_f16", "bsk_gemm_f16_enqueue"):
+            getattr(lib, name).argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, p, i, p]
             getattr(lib, name).restype = i
         for name in ("gemv_bf16", "bsk_gemv_bf16_enqueue"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
@@ -137,6 +143,21 @@ def gemm_f16_colmajor(A, B, C, M: int, N: int, K: int, stream=None) -> None:
 def gemm_f16_colmajor_enqueue(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     """Asynchronous variant of gemm_f16_colmajor (check with stream_check)."""
     _check(load().bsk_gemm_f16_colmajor_enqueue(_addr(A), _addr(B), _addr(C), M, N, K, _stream(stream)))
+
+
+def gemm_f16(order: int, transa: int, transb: int, A, lda: int, B, ldb: int, C, ldc: int, M: int, N: int,
+             K: int, bias=None, bias_mode: int = BIAS_NONE, stream=None) -> None:
+    """C = op(A) op(B) (+ bias), FP16, any storage order / transposition /
+    leading dimensions (CBLAS conventions); blocks until done."""
+    _check(load().gemm_f16(order, transa, transb, _addr(A), lda, _addr(B), ldb, _addr(C), ldc, M, N, K,
+                           _addr(bias), bias_mode, _stream(stream)))
+
+
+def gemm_f16_enqueue(order: int, transa: int, transb: int, A, lda: int, B, ldb: int, C, ldc: int, M: int, N: int,
+                     K: int, bias=None, bias_mode: int = BIAS_NONE, stream=None) -> None:
+    """Asynchronous variant of gemm_f16 (check with stream_check)."""
+    _check(load().bsk_gemm_f16_enqueue(order, transa, transb, _addr(A), lda, _addr(B), ldb, _addr(C), ldc, M, N,
+                                       K, _addr(bias), bias_mode, _stream(stream)))
 
 
 def gemm_f16_colmajor_noalloc(A, B, C, M: int, N: int, K: int, stream=None) -> None:

@@ -168,26 +168,45 @@ int alloc_workspace(Workspace& ws, size_t bytes, cudaStream_t s)
     return BSK_OK;
 }
 
-// Runs the tcgen05 GEMM on operands in any layout TMA may not take directly.
-// A: M x K (MN-major if a_mn_major, else K-major), B: K-major K x N, C: column-major M x N.
-int run_gemm(const uint16_t* A, bool a_mn_major, const uint16_t* B, uint16_t* C, int M, int N, int K, bool bf16,
-             int sms, cudaStream_t s)
+// One GEMM as the kernels see it: C (column-major, M x N, leading dimension
+// ldc) = A (M x K) * B (K x N) [+ bias].  A is MN-major (A(m,k) at
+// A[m + k*lda]) or K-major (A[k + m*lda]); B is K-major (B[k + n*ldb]) or
+// MN-major (B[n + k*ldb]).
+struct GemmOp {
+    const uint16_t* A = nullptr;
+    long long lda = 0;
+    bool a_mn_major = true;
+    const uint16_t* B = nullptr;
+    long long ldb = 0;
+    bool b_mn_major = false;
+    uint16_t* C = nullptr;
+    long long ldc = 0;
+    int M = 0, N = 0, K = 0;
+    bool bf16 = false;
+    const uint16_t* bias = nullptr;
+    int bias_mode = 0;
+};
+
+// Runs the tcgen05 GEMM on operands in any layout TMA may not take directly:
+// an operand whose base is not 16-byte aligned or whose leading dimension is
+// not a multiple of 8 elements is packed into a stream-ordered workspace.
+int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
 {
     const bool force_pack = opt_or(BSK_OPT_FORCE_PACK, 0) != 0;
-    // A's leading dimension: M when MN-major, K when K-major.
-    const long long lda = a_mn_major ? M : K;
-    const long long a_outer = a_mn_major ? K : M;
-    const bool a_ok = !force_pack && aligned16(A) && (lda % 8 == 0);
-    const bool b_ok = !force_pack && aligned16(B) && (K % 8 == 0);
-    const long long lda_p = a_ok ? lda : round_up8(lda);
-    const long long ldb_p = b_ok ? K : round_up8(K);
+    // stored extents: `inner` contiguous elements in each of `outer` lines
+    const int a_inner = op.a_mn_major ? op.M : op.K, a_outer = op.a_mn_major ? op.K : op.M;
+    const int b_inner = op.b_mn_major ? op.N : op.K, b_outer = op.b_mn_major ? op.K : op.N;
+    const bool a_ok = !force_pack && aligned16(op.A) && (op.lda % 8 == 0);
+    const bool b_ok = !force_pack && aligned16(op.B) && (op.ldb % 8 == 0);
+    const long long lda_p = a_ok ? op.lda : round_up8(a_inner);
+    const long long ldb_p = b_ok ? op.ldb : round_up8(b_inner);
     size_t a_bytes = a_ok ? 0 : static_cast<size_t>(lda_p) * a_outer * 2;
-    size_t b_bytes = b_ok ? 0 : static_cast<size_t>(ldb_p) * N * 2;
+    size_t b_bytes = b_ok ? 0 : static_cast<size_t>(ldb_p) * b_outer * 2;
     a_bytes = (a_bytes + 255) / 256 * 256;
 
     Workspace ws;
-    const uint16_t* Ause = A;
-    const uint16_t* Buse = B;
+    const uint16_t* Ause = op.A;
+    const uint16_t* Buse = op.B;
     char msg[512] = "";
     if (a_bytes + b_bytes > 0) {
         int st = alloc_workspace(ws, a_bytes + b_bytes, s);
@@ -195,39 +214,48 @@ int run_gemm(const uint16_t* A, bool a_mn_major, const uint16_t* B, uint16_t* C,
         uint8_t* base = static_cast<uint8_t*>(ws.ptr);
         if (!a_ok) {
             uint16_t* Ap = reinterpret_cast<uint16_t*>(base);
-            if (bsk::launch_pack(A, lda, Ap, lda_p, static_cast<int>(lda), static_cast<int>(a_outer), s, msg,
-                                 sizeof(msg)))
+            if (bsk::launch_pack(op.A, op.lda, Ap, lda_p, a_inner, a_outer, s, msg, sizeof(msg)))
                 return fail(BSK_ERR_CUDA, "%s", msg);
             Ause = Ap;
         }
         if (!b_ok) {
             uint16_t* Bp = reinterpret_cast<uint16_t*>(base + a_bytes);
-            if (bsk::launch_pack(B, K, Bp, ldb_p, K, N, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
+            if (bsk::launch_pack(op.B, op.ldb, Bp, ldb_p, b_inner, b_outer, s, msg, sizeof(msg)))
+                return fail(BSK_ERR_CUDA, "%s", msg);
             Buse = Bp;
         }
     }
 
     bsk::GemmLaunch g;
     g.A = Ause;
-    g.lda = a_ok ? lda : lda_p;
-    g.a_mn_major = a_mn_major;
+    g.lda = lda_p;
+    g.a_mn_major = op.a_mn_major;
     g.B = Buse;
-    g.ldb = b_ok ? K : ldb_p;
-    g.C = C;
-    g.ldc = M;
-    g.M = M;
-    g.N = N;
-    g.K = K;
-    g.bf16 = bf16;
+    g.ldb = ldb_p;
+    g.b_mn_major = op.b_mn_major;
+    g.C = op.C;
+    g.ldc = op.ldc;
+    g.M = op.M;
+    g.N = op.N;
+    g.K = op.K;
+    g.bf16 = op.bf16;
+    g.bias = op.bias_mode != 0 ? op.bias : nullptr;
+    g.bias_mode = op.bias_mode;
     // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
     // tile, deep ring: the weight stream sets the pace), else 256 on CTA pairs.
+    // An MN-major B is staged in 64-column swizzle atoms: at least 64 wide.
     const long long bn_opt = opt_or(BSK_OPT_BLOCK_N, 0);
-    const int bn_auto = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+    const int bn_auto = op.N <= 32 ? 32 : op.N <= 64 ? 64 : op.N <= 128 ? 128 : 256;
     g.block_n = static_cast<int>(bn_opt > 0 ? bn_opt : bn_auto);
+    if (op.b_mn_major && g.block_n < 64) g.block_n = 64;
     g.pair = g.block_n == 256 && opt_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
     // Tile-row group: measured best on GB300 for 8192^3-class and prefill shapes.
     g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, g.pair && g.block_n == 256 ? 2 : 16));
-    g.tma_store = aligned16(C) && (M % 8 == 0) && opt_or(BSK_OPT_FORCE_DIRECT_STORE, 0) == 0;
+    // TMA store of C: 16-byte aligned base and ldc, and M a multiple of 8.  With
+    // a ragged M the store's clipping was seen to write up to the end of the
+    // last 16-byte unit, i.e. into C's padding rows when ldc > M.
+    g.tma_store = aligned16(op.C) && (op.ldc % 8 == 0) && (op.M % 8 == 0) &&
+                  opt_or(BSK_OPT_FORCE_DIRECT_STORE, 0) == 0;
     g.num_sms = sms;
     g.status = g_status_dev;
     g.wait_limit_ns = static_cast<unsigned long long>(opt_or(BSK_OPT_WAIT_LIMIT_US, kDefaultWaitLimitUs)) * 1000ull;
@@ -235,15 +263,39 @@ int run_gemm(const uint16_t* A, bool a_mn_major, const uint16_t* B, uint16_t* C,
     return BSK_OK;
 }
 
-int enqueue_gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream)
+// Elements a stored matrix with `outer` lines of `inner` elements, `ld` apart, reaches.
+long long span_elems(long long inner, long long outer, long long ld)
+{
+    if (inner == 0 || outer == 0) return 0;
+    return (outer - 1) * ld + inner;
+}
+
+// The general FP16 GEMM on column-major storage (row-major calls are mapped
+// onto it by the caller): C = op(A) op(B) [+ bias].
+int enqueue_gemm_general(int transa, int transb, const uint16_t* A, long long lda, const uint16_t* B,
+                         long long ldb, uint16_t* C, long long ldc, int M, int N, int K, const uint16_t* bias,
+                         int bias_mode, void* stream)
 {
     if (M < 0 || N < 0 || K < 0) return fail(BSK_ERR_INVALID_ARG, "negative size (M=%d N=%d K=%d)", M, N, K);
+    if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1))
+        return fail(BSK_ERR_INVALID_ARG, "transa/transb must be 0 or 1 (got %d, %d)", transa, transb);
+    if (bias_mode < 0 || bias_mode > 2) return fail(BSK_ERR_INVALID_ARG, "bias_mode must be 0, 1 or 2 (got %d)", bias_mode);
+    if (bias_mode != 0 && bias == nullptr) return fail(BSK_ERR_INVALID_ARG, "bias_mode %d needs a bias vector", bias_mode);
+    // stored shapes: A is M x K (transa 0) or K x M (transa 1), B is K x N or N x K
+    const long long a_rows = transa ? K : M, a_cols = transa ? M : K;
+    const long long b_rows = transb ? N : K, b_cols = transb ? K : N;
+    if (lda < (a_rows > 1 ? a_rows : 1) || ldb < (b_rows > 1 ? b_rows : 1) || ldc < (M > 1 ? M : 1))
+        return fail(BSK_ERR_INVALID_ARG, "leading dimension too small (lda=%lld ldb=%lld ldc=%lld for M=%d N=%d K=%d, "
+                    "transa=%d transb=%d)", lda, ldb, ldc, M, N, K, transa, transb);
     if (M == 0 || N == 0) return BSK_OK;
-    const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(K) * N * 2;
-    const size_t c_bytes = static_cast<size_t>(M) * N * 2;
+    const size_t a_bytes = static_cast<size_t>(span_elems(a_rows, a_cols, lda)) * 2;
+    const size_t b_bytes = static_cast<size_t>(span_elems(b_rows, b_cols, ldb)) * 2;
+    const size_t c_bytes = static_cast<size_t>(span_elems(M, N, ldc)) * 2;
+    const size_t bias_bytes = bias_mode == 0 ? 0 : static_cast<size_t>(bias_mode == 1 ? M : N) * 2;
     if (C == nullptr) return fail(BSK_ERR_INVALID_ARG, "C is NULL");
     if (K > 0 && (A == nullptr || B == nullptr)) return fail(BSK_ERR_INVALID_ARG, "A or B is NULL");
-    if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes))
+    if (overlaps(C, c_bytes, A, K > 0 ? a_bytes : 0) || overlaps(C, c_bytes, B, K > 0 ? b_bytes : 0) ||
+        overlaps(C, c_bytes, bias, bias_bytes))
         return fail(BSK_ERR_INVALID_ARG, "C overlaps an input");
     const long long tiles = ((M + 127LL) / 128) * ((N + 127LL) / 128);
     if (tiles > INT_MAX) return fail(BSK_ERR_INVALID_ARG, "problem too large (%lld tiles)", tiles);
@@ -252,10 +304,47 @@ int enqueue_gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, i
     if (st != BSK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) {
-        cudaError_t e = cudaMemsetAsync(C, 0, c_bytes, s);
-        return e == cudaSuccess ? BSK_OK : fail_cuda(e, "cudaMemsetAsync");
+        char msg[512] = "";
+        if (bsk::launch_fill_bias(C, ldc, M, N, bias, bias_mode, s, msg, sizeof(msg)))
+            return fail(BSK_ERR_CUDA, "%s", msg);
+        return BSK_OK;
     }
-    return run_gemm(A, true, B, C, M, N, K, false, sms, s);
+    GemmOp op;
+    op.A = A;
+    op.lda = lda;
+    op.a_mn_major = transa == 0;
+    op.B = B;
+    op.ldb = ldb;
+    op.b_mn_major = transb == 1;
+    op.C = C;
+    op.ldc = ldc;
+    op.M = M;
+    op.N = N;
+    op.K = K;
+    op.bias = bias;
+    op.bias_mode = bias_mode;
+    return run_gemm(op, sms, s);
+}
+
+int enqueue_gemm_f16_cblas(int order, int transa, int transb, const uint16_t* A, int lda, const uint16_t* B,
+                           int ldb, uint16_t* C, int ldc, int M, int N, int K, const uint16_t* bias,
+                           int bias_mode, void* stream)
+{
+    if (order == BSK_COL_MAJOR)
+        return enqueue_gemm_general(transa, transb, A, lda, B, ldb, C, ldc, M, N, K, bias, bias_mode, stream);
+    if (order != BSK_ROW_MAJOR) return fail(BSK_ERR_INVALID_ARG, "order must be BSK_COL_MAJOR or BSK_ROW_MAJOR");
+    // Row-major C (M x N) is column-major C^T (N x M) = op(B)^T op(A)^T, and a
+    // row-major stored matrix is the column-major store of its transpose: swap
+    // the operands and their flags, and the bias's axis.
+    if (bias_mode < 0 || bias_mode > 2) return fail(BSK_ERR_INVALID_ARG, "bias_mode must be 0, 1 or 2 (got %d)", bias_mode);
+    const int swapped_mode = bias_mode == 1 ? 2 : bias_mode == 2 ? 1 : 0;
+    return enqueue_gemm_general(transb, transa, B, ldb, A, lda, C, ldc, N, M, K, bias, swapped_mode, stream);
+}
+
+int enqueue_gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream)
+{
+    return enqueue_gemm_general(0, 0, A, M > 1 ? M : 1, B, K > 1 ? K : 1, C, M > 1 ? M : 1, M, N, K, nullptr, 0,
+                                stream);
 }
 
 int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream)
@@ -295,7 +384,20 @@ int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, 
         return BSK_OK;
     }
     // Prefill: Y^T (M x n, column-major == y row-major) = W (K-major) * x^T (K-major).
-    return run_gemm(W, false, x, y, M, n, K, true, sms, s);
+    GemmOp op;
+    op.A = W;
+    op.lda = K;
+    op.a_mn_major = false;
+    op.B = x;
+    op.ldb = K;
+    op.b_mn_major = false;
+    op.C = y;
+    op.ldc = M;
+    op.M = M;
+    op.N = n;
+    op.K = K;
+    op.bf16 = true;
+    return run_gemm(op, sms, s);
 }
 
 int enqueue_decode_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
@@ -422,6 +524,22 @@ int gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, i
     if (st != BSK_OK) return st;
     if (M == 0 || n == 0) return BSK_OK;
     return sync_and_check(static_cast<cudaStream_t>(stream));
+}
+
+int gemm_f16(int order, int transa, int transb, const uint16_t* A, int lda, const uint16_t* B, int ldb,
+             uint16_t* C, int ldc, int M, int N, int K, const uint16_t* bias, int bias_mode, void* stream)
+{
+    int st = enqueue_gemm_f16_cblas(order, transa, transb, A, lda, B, ldb, C, ldc, M, N, K, bias, bias_mode, stream);
+    if (st != BSK_OK) return st;
+    if (M == 0 || N == 0) return BSK_OK;
+    return sync_and_check(static_cast<cudaStream_t>(stream));
+}
+
+int bsk_gemm_f16_enqueue(int order, int transa, int transb, const uint16_t* A, int lda, const uint16_t* B,
+                         int ldb, uint16_t* C, int ldc, int M, int N, int K, const uint16_t* bias, int bias_mode,
+                         void* stream)
+{
+    return enqueue_gemm_f16_cblas(order, transa, transb, A, lda, B, ldb, C, ldc, M, N, K, bias, bias_mode, stream);
 }
 
 int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,

@@ -24,6 +24,25 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// C(m,n) = bias value (or +0.0) for m < M, n < N, C(m,n) at C[m + n*ldc]: the
+// K == 0 case of the GEMM (an empty sum plus the bias, already in the output
+// format, so no rounding happens).
+__global__ void __launch_bounds__(256)
+    fill_bias_kernel(uint16_t* __restrict__ C, long long ldc, int M, int N, const uint16_t* __restrict__ bias,
+                     int bias_mode)
+{
+    const long long total = static_cast<long long>(M) * N;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+        const long long n = e / M;
+        const long long m = e - n * M;
+        uint16_t v = 0;
+        if (bias_mode == 1) v = bias[m];
+        else if (bias_mode == 2) v = bias[n];
+        C[m + n * ldc] = v;
+    }
+}
+
 // One CTA waits on an mbarrier that nobody arrives on.  The wait is the
 // GEMM's bounded wait; it must give up after limit_ns and record a timeout.
 __global__ void wait_timeout_probe_kernel(int* status, unsigned long long limit_ns)
@@ -56,6 +75,22 @@ int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
+        return 1;
+    }
+    return 0;
+}
+
+int launch_fill_bias(uint16_t* C, long long ldc, int M, int N, const uint16_t* bias, int bias_mode,
+                     cudaStream_t stream, char* msg, size_t msg_len)
+{
+    const long long total = static_cast<long long>(M) * N;
+    if (total <= 0) return 0;
+    long long grid = (total + 255) / 256;
+    if (grid > 4096) grid = 4096;
+    fill_bias_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(C, ldc, M, N, bias, bias_mode);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "fill launch failed: %s", cudaGetErrorString(e));
         return 1;
     }
     return 0;

@@ -45,28 +45,31 @@ void record_error(const char* msg);
 TmapEncodeFn tmap_encoder();
 
 // Launch of the tcgen05 GEMM: C (M x N, column-major, m contiguous, leading
-// dimension ldc) = A (M x K) * B (K x N), FP32 accumulation, FP16 or BF16 in/out.
-// A is either MN-major (A(m,k) at A[m + k*lda]) or K-major (A(m,k) at
-// A[k + m*lda]); B is K-major (B(k,n) at B[k + n*ldb]).  A and B must be
-// 16-byte aligned with 16-byte-multiple leading dimensions (the caller packs
-// them otherwise).
+// dimension ldc) = A (M x K) * B (K x N) [+ bias], FP32 accumulation, FP16 or
+// BF16 in/out.  A is either MN-major (A(m,k) at A[m + k*lda]) or K-major (A(m,k)
+// at A[k + m*lda]); B is K-major (B(k,n) at B[k + n*ldb]) or MN-major (B(k,n)
+// at B[n + k*ldb]).  A and B must be 16-byte aligned with 16-byte-multiple
+// leading dimensions (the caller packs them otherwise).
 struct GemmLaunch {
-    const void* A;
-    long long lda;
-    bool a_mn_major;
-    const void* B;
-    long long ldb;
-    void* C;
-    long long ldc;
-    int M, N, K;
-    bool bf16;
-    int block_n;    // 128 or 256
-    bool pair;      // block_n == 256 only: CTA-pair kernel (256 x 256 tiles over two SMs)
-    int group_m;    // >= 1
-    bool tma_store; // C 16-byte aligned with 16-byte-multiple ldc
-    int num_sms;    // persistent grid size cap
-    int* status;    // device status word
-    unsigned long long wait_limit_ns;
+    const void* A = nullptr;
+    long long lda = 0;
+    bool a_mn_major = true;
+    const void* B = nullptr;
+    long long ldb = 0;
+    bool b_mn_major = false;  // B(k,n) at B[n + k*ldb] (FP16 only, block_n >= 64)
+    void* C = nullptr;
+    long long ldc = 0;
+    int M = 0, N = 0, K = 0;
+    bool bf16 = false;
+    int block_n = 256;       // 32, 64, 128 or 256
+    bool pair = true;        // block_n == 256 only: CTA-pair kernel (256 x 256 tiles over two SMs)
+    int group_m = 2;         // >= 1
+    bool tma_store = false;  // C 16-byte aligned with 16-byte-multiple ldc
+    const uint16_t* bias = nullptr;  // optional, output precision
+    int bias_mode = 0;       // 1: bias[m] per row, 2: bias[n] per column
+    int num_sms = 1;         // persistent grid size cap
+    int* status = nullptr;   // device status word
+    unsigned long long wait_limit_ns = 2000000000ull;
 };
 
 // Returns 0 on success; otherwise an error message is written to `msg`.
@@ -107,6 +110,11 @@ int launch_decode_attention(const AttnLaunch& a, cudaStream_t stream, char* msg,
 // leading dimension ld_src to ld_dst.  The source is only read.
 int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long ld_dst, int inner, int outer,
                 cudaStream_t stream, char* msg, size_t msg_len);
+
+// C(m,n) = bias[m] (mode 1), bias[n] (mode 2) or +0.0 (mode 0) for the M x N
+// column-major C with leading dimension ldc: the GEMM with K == 0.
+int launch_fill_bias(uint16_t* C, long long ldc, int M, int N, const uint16_t* bias, int bias_mode,
+                     cudaStream_t stream, char* msg, size_t msg_len);
 
 // Test hook: one CTA waits on an mbarrier that nothing completes, with the same
 // bounded wait the GEMM uses; it must give up after `limit_ns` and record a

@@ -65,6 +65,8 @@ struct Params {
     void* C;
     long long ldc;
     int tma_store;
+    const uint16_t* bias;   // optional, output precision: bias[m] (mode 1) or bias[n] (mode 2)
+    int bias_mode;
     int* status;
     unsigned long long wait_limit_ns;
 };
@@ -90,14 +92,44 @@ __device__ __forceinline__ uint16_t round_out(uint32_t acc_bits)
     }
 }
 
-template <int BN, bool A_MN, bool BF16>
+template <bool BF16>
+__device__ __forceinline__ float bias_value(const uint16_t* bias, int i)
+{
+    const uint16_t b = bias[i];
+    if constexpr (BF16) {
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    } else {
+        return __half2float(__ushort_as_half(b));
+    }
+}
+
+// Adds the bias to the FP32 accumulators of row m, columns n0..n0+31, before the
+// one rounding to the output type.
+template <bool BF16>
+__device__ __forceinline__ void add_bias(uint32_t (&r)[32], const Params& p, int m, int n0)
+{
+    if (p.bias_mode == 1) {
+        if (m < p.M) {
+            const float b = bias_value<BF16>(p.bias, m);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
+        }
+    } else if (p.bias_mode == 2) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (n0 + j < p.N) r[j] = __float_as_uint(__uint_as_float(r[j]) + bias_value<BF16>(p.bias, n0 + j));
+    }
+}
+
+template <int BN, bool A_MN, bool B_MN, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const Params p)
 {
     using Cf = Cfg<BN>;
     constexpr int S = Cf::kStages;
-    constexpr uint32_t kIdesc = idesc_f16(BF16, A_MN, false, kBM, BN);
+    constexpr uint32_t kIdesc = idesc_f16(BF16, A_MN, B_MN, kBM, BN);
+    static_assert(!B_MN || BN % 64 == 0, "an MN-major B needs whole 64-column swizzle atoms");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -180,7 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         tma_load_2d(a_dst, &tmA, fb, k0, m0);   // 64(k) x 128(m) box
                     }
-                    tma_load_2d(b_dst, &tmB, fb, k0, n0);        // 64(k) x BN(n) box
+                    if constexpr (B_MN) {
+#pragma unroll
+                        for (int i = 0; i < BN / 64; ++i)   // 64(n) x 64(k) boxes, 8 KB apart
+                            tma_load_2d(b_dst + i * 8192, &tmB, fb, n0 + 64 * i, k0);
+                    } else {
+                        tma_load_2d(b_dst, &tmB, fb, k0, n0);    // 64(k) x BN(n) box
+                    }
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -232,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // m blocks 8 KB apart; K-major operands: 32 bytes along the row.
                         const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, Cf::kABytes / 2, 1024)
                                                  : smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
+                                                 : smem_desc_sw128(b_base + kk * 32, 16, 1024);
                         mma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit(empty0 + 8 * stage);
@@ -285,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
                 }
+                if (p.bias_mode != 0) add_bias<BF16>(r, p, m0 + lane, n0 + c * 32);
                 if (p.tma_store) {
                     uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
                     if (lane == 0) bulk_wait_group_read<1>();   // the store that used `buf` has read it
@@ -354,7 +394,7 @@ struct PairCfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
 };
 
-template <bool A_MN, bool BF16>
+template <bool A_MN, bool B_MN, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const Params p)
@@ -362,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Cf = PairCfg;
     constexpr int S = Cf::kStages;
     constexpr int T = Cf::kTile;
-    constexpr uint32_t kIdesc = idesc_f16(BF16, A_MN, false, 2 * kBM, T);
+    constexpr uint32_t kIdesc = idesc_f16(BF16, A_MN, B_MN, 2 * kBM, T);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -451,7 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
                     }
-                    tma_load_2d_pair(b_dst, &tmB, fb, k0, n0);
+                    if constexpr (B_MN) {
+                        tma_load_2d_pair(b_dst, &tmB, fb, n0, k0);            // 64(n) x 64(k)
+                        tma_load_2d_pair(b_dst + 8192, &tmB, fb, n0 + 64, k0);
+                    } else {
+                        tma_load_2d_pair(b_dst, &tmB, fb, k0, n0);
+                    }
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -502,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                         const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, Cf::kABytes / 2, 1024)
                                                  : smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
+                                                 : smem_desc_sw128(b_base + kk * 32, 16, 1024);
                         mma_f16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit_pair_multicast(empty0 + 8 * stage, 0x3);
@@ -553,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_remote(leader_tempty0 + 8 * acc);
                 }
+                if (p.bias_mode != 0) add_bias<BF16>(r, p, m0 + lane, n0 + c * 32);
                 if (p.tma_store) {
                     uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
                     if (lane == 0) bulk_wait_group_read<1>();
@@ -617,7 +664,7 @@ bool encode_2d(CUtensorMap* map, bool bf16, const void* base, unsigned long long
     return true;
 }
 
-template <int BN, bool A_MN, bool BF16>
+template <int BN, bool A_MN, bool B_MN, bool BF16>
 int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
     using Cf = Cfg<BN>;
@@ -629,8 +676,13 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
         if (!encode_2d(&tmA, BF16, g.A, g.K, g.M, g.lda * 2ull, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
             return 1;
     }
-    if (!encode_2d(&tmB, BF16, g.B, g.K, g.N, g.ldb * 2ull, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-        return 1;
+    if (B_MN) {
+        if (!encode_2d(&tmB, BF16, g.B, g.N, g.K, g.ldb * 2ull, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+            return 1;
+    } else {
+        if (!encode_2d(&tmB, BF16, g.B, g.K, g.N, g.ldb * 2ull, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+            return 1;
+    }
     if (g.tma_store) {
         if (!encode_2d(&tmC, BF16, g.C, g.M, g.N, g.ldc * 2ull, kEpiBox, kEpiBox, CU_TENSOR_MAP_SWIZZLE_NONE, msg,
                        msg_len))
@@ -651,10 +703,12 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     p.C = g.C;
     p.ldc = g.ldc;
     p.tma_store = g.tma_store ? 1 : 0;
+    p.bias = g.bias;
+    p.bias_mode = g.bias != nullptr ? g.bias_mode : 0;
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
 
-    auto kern = gemm_tcgen05_kernel<BN, A_MN, BF16>;
+    auto kern = gemm_tcgen05_kernel<BN, A_MN, B_MN, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -672,7 +726,7 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     return 0;
 }
 
-template <bool A_MN, bool BF16>
+template <bool A_MN, bool B_MN, bool BF16>
 int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
     using Cf = PairCfg;
@@ -684,8 +738,13 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
         if (!encode_2d(&tmA, BF16, g.A, g.K, g.M, g.lda * 2ull, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
             return 1;
     }
-    if (!encode_2d(&tmB, BF16, g.B, g.K, g.N, g.ldb * 2ull, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-        return 1;
+    if (B_MN) {
+        if (!encode_2d(&tmB, BF16, g.B, g.N, g.K, g.ldb * 2ull, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+            return 1;
+    } else {
+        if (!encode_2d(&tmB, BF16, g.B, g.K, g.N, g.ldb * 2ull, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+            return 1;
+    }
     if (g.tma_store) {
         if (!encode_2d(&tmC, BF16, g.C, g.M, g.N, g.ldc * 2ull, kEpiBox, kEpiBox, CU_TENSOR_MAP_SWIZZLE_NONE, msg,
                        msg_len))
@@ -705,10 +764,12 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.C = g.C;
     p.ldc = g.ldc;
     p.tma_store = g.tma_store ? 1 : 0;
+    p.bias = g.bias;
+    p.bias_mode = g.bias != nullptr ? g.bias_mode : 0;
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
 
-    auto kern = gemm_tcgen05_pair_kernel<A_MN, BF16>;
+    auto kern = gemm_tcgen05_pair_kernel<A_MN, B_MN, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -747,45 +808,62 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
 
 }  // namespace
 
+namespace {
+
+// B MN-major (a transposed B) is instantiated for FP16 only.
+template <int BN>
+int dispatch_single(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
+{
+    if (g.b_mn_major) {
+        if constexpr (BN >= 64) {
+            if (g.bf16) {
+                snprintf(msg, msg_len, "a transposed B operand is supported for FP16 only");
+                return 1;
+            }
+            return g.a_mn_major ? launch_instance<BN, true, true, false>(g, stream, msg, msg_len)
+                                : launch_instance<BN, false, true, false>(g, stream, msg, msg_len);
+        } else {
+            snprintf(msg, msg_len, "a transposed B operand needs block_n >= 64");
+            return 1;
+        }
+    }
+    if (g.a_mn_major)
+        return g.bf16 ? launch_instance<BN, true, false, true>(g, stream, msg, msg_len)
+                      : launch_instance<BN, true, false, false>(g, stream, msg, msg_len);
+    return g.bf16 ? launch_instance<BN, false, false, true>(g, stream, msg, msg_len)
+                  : launch_instance<BN, false, false, false>(g, stream, msg, msg_len);
+}
+
+int dispatch_pair(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
+{
+    if (g.b_mn_major) {
+        if (g.bf16) {
+            snprintf(msg, msg_len, "a transposed B operand is supported for FP16 only");
+            return 1;
+        }
+        return g.a_mn_major ? launch_pair_instance<true, true, false>(g, stream, msg, msg_len)
+                            : launch_pair_instance<false, true, false>(g, stream, msg, msg_len);
+    }
+    if (g.a_mn_major)
+        return g.bf16 ? launch_pair_instance<true, false, true>(g, stream, msg, msg_len)
+                      : launch_pair_instance<true, false, false>(g, stream, msg, msg_len);
+    return g.bf16 ? launch_pair_instance<false, false, true>(g, stream, msg, msg_len)
+                  : launch_pair_instance<false, false, false>(g, stream, msg, msg_len);
+}
+
+}  // namespace
+
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
-    if (g.block_n == 256 && g.pair) {
-        if (g.a_mn_major)
-            return g.bf16 ? launch_pair_instance<true, true>(g, stream, msg, msg_len)
-                          : launch_pair_instance<true, false>(g, stream, msg, msg_len);
-        return g.bf16 ? launch_pair_instance<false, true>(g, stream, msg, msg_len)
-                      : launch_pair_instance<false, false>(g, stream, msg, msg_len);
+    switch (g.block_n) {
+    case 256: return g.pair ? dispatch_pair(g, stream, msg, msg_len) : dispatch_single<256>(g, stream, msg, msg_len);
+    case 128: return dispatch_single<128>(g, stream, msg, msg_len);
+    case 64: return dispatch_single<64>(g, stream, msg, msg_len);
+    case 32: return dispatch_single<32>(g, stream, msg, msg_len);
+    default:
+        snprintf(msg, msg_len, "unsupported block_n %d (32, 64, 128 or 256)", g.block_n);
+        return 1;
     }
-    if (g.block_n == 256) {
-        if (g.a_mn_major)
-            return g.bf16 ? launch_instance<256, true, true>(g, stream, msg, msg_len)
-                          : launch_instance<256, true, false>(g, stream, msg, msg_len);
-        return g.bf16 ? launch_instance<256, false, true>(g, stream, msg, msg_len)
-                      : launch_instance<256, false, false>(g, stream, msg, msg_len);
-    }
-    if (g.block_n == 128) {
-        if (g.a_mn_major)
-            return g.bf16 ? launch_instance<128, true, true>(g, stream, msg, msg_len)
-                          : launch_instance<128, true, false>(g, stream, msg, msg_len);
-        return g.bf16 ? launch_instance<128, false, true>(g, stream, msg, msg_len)
-                      : launch_instance<128, false, false>(g, stream, msg, msg_len);
-    }
-    if (g.block_n == 64) {
-        if (g.a_mn_major)
-            return g.bf16 ? launch_instance<64, true, true>(g, stream, msg, msg_len)
-                          : launch_instance<64, true, false>(g, stream, msg, msg_len);
-        return g.bf16 ? launch_instance<64, false, true>(g, stream, msg, msg_len)
-                      : launch_instance<64, false, false>(g, stream, msg, msg_len);
-    }
-    if (g.block_n == 32) {
-        if (g.a_mn_major)
-            return g.bf16 ? launch_instance<32, true, true>(g, stream, msg, msg_len)
-                          : launch_instance<32, true, false>(g, stream, msg, msg_len);
-        return g.bf16 ? launch_instance<32, false, true>(g, stream, msg, msg_len)
-                      : launch_instance<32, false, false>(g, stream, msg, msg_len);
-    }
-    snprintf(msg, msg_len, "unsupported block_n %d (32, 64, 128 or 256)", g.block_n);
-    return 1;
 }
 
 }  // namespace bsk

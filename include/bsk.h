@@ -1,11 +1,14 @@
 /*
  * bsk.h -- C ABI of libbsk: half-precision GEMM with FP32 accumulation on one
- * NVIDIA GB300 (sm_103a), in two regimes:
+ * NVIDIA GB300 (sm_103a), in two regimes, plus the decode attention beside them:
  *
  *   gemm_f16_colmajor  large column-major FP16 GEMM on the tcgen05 tensor cores;
+ *   gemm_f16           the same GEMM with transposed operands, row-major storage,
+ *                      any leading dimensions and an optional fused bias;
  *   gemv_bf16          BF16 linear layer y = x W^T: the HBM-bound decode GEMV for
  *                      n <= 8 tokens (CUDA cores), the tensor-core GEMM for
- *                      larger n (prefill projections).
+ *                      larger n (prefill projections);
+ *   decode_attention_bf16  split-KV decode attention over a paged BF16 KV cache.
  *
  * Conventions shared by every call:
  *  - Matrix pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors) to
@@ -59,6 +62,49 @@ typedef enum bsk_status {
  * alignment.  C must not overlap A or B (BSK_ERR_INVALID_ARG).
  */
 int gemm_f16_colmajor(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream);
+
+/* Storage order of every matrix of a gemm_f16 call (the CBLAS convention). */
+typedef enum bsk_order {
+    BSK_COL_MAJOR = 0, /* entry (r, c) of a stored matrix at P[r + c*ld] */
+    BSK_ROW_MAJOR = 1  /* entry (r, c) at P[c + r*ld] */
+} bsk_order;
+
+/* Axis of the optional bias of gemm_f16. */
+typedef enum bsk_bias_mode {
+    BSK_BIAS_NONE = 0,
+    BSK_BIAS_ROW = 1,    /* bias[m]: one value per row of C (length M) */
+    BSK_BIAS_COLUMN = 2  /* bias[n]: one value per column of C (length N) */
+} bsk_bias_mode;
+
+/*
+ * The FP16 GEMM of gemm_f16_colmajor in every storage form, with an optional
+ * fused bias:
+ *     C(m,n) = fp16_rn( sum_k op(A)(m,k) op(B)(k,n) + bias ),  FP32 accumulation,
+ * where op(A) = A (transa 0, A stored M x K) or A^T (transa 1, A stored K x M),
+ * op(B) = B (transb 0, B stored K x N) or B^T (transb 1, B stored N x K), every
+ * stored matrix (and C, M x N) addressed in `order` (bsk_order) with its own
+ * leading dimension.  The product is the one of "MTT S4000 GEMM
+ * 优化中的分块、尾处理与并发实战复盘", section 2 (GEMM入门), whose
+ * column-major NN form gemm_f16_colmajor is; transposition flags and row-major
+ * storage follow the BLAS/CBLAS conventions.  The bias is the optional term
+ * that the DCU decode-GEMV article (forum.sourcefind.cn), section 6.1, names
+ * among the properties of a linear call: an FP16 vector (device pointer) of
+ * length M (BSK_BIAS_ROW) or N (BSK_BIAS_COLUMN), added to the FP32
+ * accumulator before the single rounding; NULL with BSK_BIAS_NONE.  (A
+ * row-major linear layer Y = X W^T + b is order BSK_ROW_MAJOR, transb 1,
+ * BSK_BIAS_COLUMN.)
+ *
+ * Leading dimensions count elements and must be at least the stored row
+ * count (column-major) or column count (row-major), and >= 1.  Operands that
+ * are not 16-byte aligned or whose leading dimension is not a multiple of 8
+ * are packed into a stream-ordered workspace first (BSK_ERR_NO_MEMORY if that
+ * fails); C may have any alignment and stride.  Only the M x N entries of C
+ * are written.  K == 0 writes the bias (or +0.0).  C must not overlap A, B
+ * or the bias (BSK_ERR_INVALID_ARG), nor may a flag or mode be out of range.
+ * Blocking, like gemm_f16_colmajor; bsk_gemm_f16_enqueue only launches.
+ */
+int gemm_f16(int order, int transa, int transb, const uint16_t* A, int lda, const uint16_t* B, int ldb,
+             uint16_t* C, int ldc, int M, int N, int K, const uint16_t* bias, int bias_mode, void* stream);
 
 /*
  * y = x W^T in BF16 with FP32 accumulation, output rounded to nearest even.
@@ -138,6 +184,9 @@ int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, uint16_t* C,
  * bsk_stream_check() (or the next blocking call).  Buffers must stay alive
  * until the stream has passed this work.
  */
+int bsk_gemm_f16_enqueue(int order, int transa, int transb, const uint16_t* A, int lda, const uint16_t* B,
+                         int ldb, uint16_t* C, int ldc, int M, int N, int K, const uint16_t* bias, int bias_mode,
+                         void* stream);
 int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
                                   void* stream);
 int bsk_gemv_bf16_enqueue(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);

@@ -107,7 +107,45 @@ def test_gemv_rejects_bad_arguments(lib, args):
     assert lib.bsk_gemv_bf16_enqueue(W, x, y, M, K, n, None) == 1
 
 
+G_A, G_B, G_C, G_BIAS = FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30)
+
+
+@pytest.mark.parametrize("args", [
+    # order, transa, transb, A, lda, B, ldb, C, ldc, M, N, K, bias, bias_mode
+    (2, 0, 0, G_A, 8, G_B, 8, G_C, 8, 8, 8, 8, None, 0),         # bad order
+    (0, 2, 0, G_A, 8, G_B, 8, G_C, 8, 8, 8, 8, None, 0),         # bad transa
+    (0, 0, -1, G_A, 8, G_B, 8, G_C, 8, 8, 8, 8, None, 0),        # bad transb
+    (0, 0, 0, G_A, 8, G_B, 8, G_C, 8, 8, 8, 8, None, 3),         # bad bias mode
+    (0, 0, 0, G_A, 8, G_B, 8, G_C, 8, 8, 8, 8, None, 1),         # bias mode without a bias
+    (1, 0, 0, G_A, 8, G_B, 8, G_C, 8, 8, 8, 8, None, 2),
+    (0, 0, 0, G_A, 7, G_B, 8, G_C, 8, 8, 8, 8, None, 0),         # lda < M
+    (0, 1, 0, G_A, 8, G_B, 9, G_C, 9, 9, 9, 9, None, 0),         # transa: lda < K
+    (0, 0, 1, G_A, 8, G_B, 8, G_C, 8, 8, 9, 8, None, 0),         # transb: ldb < N
+    (0, 0, 0, G_A, 8, G_B, 8, G_C, 7, 8, 8, 8, None, 0),         # ldc < M
+    (1, 0, 0, G_A, 8, G_B, 8, G_C, 7, 8, 8, 8, None, 0),         # row-major: ldc < N
+    (1, 0, 0, G_A, 7, G_B, 8, G_C, 8, 8, 8, 8, None, 0),         # row-major: lda < K
+    (0, 0, 0, G_A, 8, G_B, 8, G_C, 8, -1, 8, 8, None, 0),        # negative size
+    (0, 0, 0, G_A, 8, G_B, 8, None, 8, 8, 8, 8, None, 0),        # C NULL
+    (0, 0, 0, G_A, 8, G_B, 8, G_A + 126, 8, 8, 8, 8, None, 0),   # C overlaps A's last element
+    (0, 0, 0, G_A, 8, G_B, 8, G_C, 8, 8, 8, 8, G_C + 14, 1),     # C overlaps the bias
+    (0, 0, 0, G_A, 8, G_B, 8, G_C, 0, 0, 8, 8, None, 0),         # ldc 0 even for an empty C
+])
+def test_general_gemm_rejects_bad_arguments(lib, args):
+    assert lib.gemm_f16(*args, None) == 1
+    assert lib.bsk_gemm_f16_enqueue(*args, None) == 1
+    assert bsk.last_error()
+
+
+def test_general_gemm_accepts_exact_leading_dimensions(lib):
+    """Overlap is decided on the spans the strides reach: a C right after A's
+    last element is not an overlap; on a machine without a GPU the call then
+    fails only at the device check."""
+    st = lib.gemm_f16(0, 0, 0, G_A, 8, G_B, 8, G_A + 128, 8, 8, 8, 8, None, 0, None)
+    assert st in (2, 3), bsk.last_error()
+
+
 def test_empty_outputs_are_no_ops_without_a_device(lib):
+    assert lib.gemm_f16(0, 1, 1, None, 7, None, 5, None, 1, 0, 5, 7, None, 0, None) == 0
     assert lib.gemm_f16_colmajor(None, None, None, 0, 5, 7, None) == 0
     assert lib.gemm_f16_colmajor(None, None, None, 5, 0, 7, None) == 0
     assert lib.gemv_bf16(None, None, None, 0, 7, 1, None) == 0
