@@ -20,7 +20,8 @@ Reported (one JSON line, rank 0):
              peak (FP16 and BF16 dense rates are equal on this part), plus
              roofline_gemv against the measured HBM copy bandwidth.
   other_configs  device time of the remaining workloads (256^3 and 4095x4097x4100
-             FP16 GEMMs, the 4096-token BF16 prefill projection), measured after the step.
+             FP16 GEMMs, the 4096-token BF16 prefill projection, and gemm_f16 in
+             other storage forms with a fused bias), measured after the step.
   decode_attention  split-KV decode attention at 8K/16K/32K tokens (KV-cache GB/s).
   cpu_baseline  the oracle timed on a bounded sample on the host cores.
 
@@ -46,6 +47,7 @@ if ROOT not in sys.path:
 
 GEMM_M, GEMM_N, GEMM_K = 8192, 8192, 16384
 GEMV_M, GEMV_K, GEMV_NS = 34816, 5120, (1, 4, 8)
+S_PREFILL = 4096
 METRIC = "FP16 GEMM TFLOP/s @8192x8192x16384; BF16 GEMV HBM GB/s (fraction of peak)"
 WORKLOAD = "gemm_f16_colmajor 8192x8192x16384 + gemv_bf16 34816x5120 n=1,4,8"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -290,7 +292,26 @@ def other_configs(W_prefill, dev, peaks):
         out[name] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1), "frac_of_peak": round(tf / peak_t, 4),
                      "note": "includes the pack of unaligned operands" if M % 8 else ""}
         del Ad, Bd, C
-    S = 4096
+    # The same GEMM in other storage forms with a fused bias (gemm_f16): column-major
+    # NT, and a row-major FP16 linear layer Y = X W^T + b over the prefill shape.
+    for name, (order, ta, tb, M, N, K) in (
+            ("gemm_f16_nt_bias_8192x8192x8192", (0, 0, 1, 8192, 8192, 8192)),
+            ("linear_f16_rowmajor_bias_4096x34816x5120", (1, 0, 1, S_PREFILL, GEMV_M, GEMV_K))):
+        A, B = inputs.gemm_operands(M, N, K, "uniform")
+        Ad, Bd = to_dev(A), to_dev(B)
+        bias = to_dev(inputs.to_f16_bits(inputs.draw("uniform", N, 41)))
+        C = torch.empty(M * N, dtype=torch.int16, device=dev)
+        lda = (K if ta else M) if order == 0 else (M if ta else K)
+        ldb = (N if tb else K) if order == 0 else (K if tb else N)
+        ldc = M if order == 0 else N
+        ms = time_launches(lambda: bsk.gemm_f16_enqueue(order, ta, tb, Ad, lda, Bd, ldb, C, ldc, M, N, K, bias,
+                                                        bsk.BIAS_COLUMN), 20)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out[name] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1), "frac_of_peak": round(tf / peak_t, 4),
+                     "layout": {"order": "row" if order else "column", "transa": ta, "transb": tb,
+                                "bias": "per column"}}
+        del Ad, Bd, C, bias
+    S = S_PREFILL
     _, X = inputs.linear_operands(1, GEMV_K, S, "normal0.02", "normal1")
     Xd = to_dev(X)
     Y = torch.empty(S * GEMV_M, dtype=torch.int16, device=dev)
@@ -573,7 +594,17 @@ def run_case(args):
         A, B = inputs.gemm_operands(a, b, c, "uniform")
         Ad, Bd = to_dev(A), to_dev(B)
         C = torch.empty(a * b, dtype=torch.int16, device=dev)
-        call = lambda: bsk.gemm_f16_colmajor_enqueue(Ad, Bd, C, a, b, c)  # noqa: E731
+        if args.layout:
+            order, ta, tb, mode = (int(v) for v in args.layout.split(","))
+            M, N, K = a, b, c
+            lda = (K if ta else M) if order == 0 else (M if ta else K)
+            ldb = (N if tb else K) if order == 0 else (K if tb else N)
+            ldc = M if order == 0 else N
+            bias = to_dev(inputs.to_f16_bits(inputs.draw("uniform", max(M, N), 41))) if mode else None
+            call = lambda: bsk.gemm_f16_enqueue(order, ta, tb, Ad, lda, Bd, ldb, C, ldc, M, N, K,  # noqa: E731
+                                                bias, mode)
+        else:
+            call = lambda: bsk.gemm_f16_colmajor_enqueue(Ad, Bd, C, a, b, c)  # noqa: E731
         work, unit = 2.0 * a * b * c, "TFLOP/s"
     elif kind == "gemv":
         W, x = inputs.linear_operands(a, b, c, "normal0.02", "normal1")
@@ -624,6 +655,8 @@ def main(argv=None):
                     help="skip timing the 256^3, ragged and prefill workloads after the step")
     ap.add_argument("--case", help="profile mode: one kernel only, e.g. gemm:8192x8192x8192 or gemv:34816x5120x1")
     ap.add_argument("--opt", action="append", help="profile mode: library option name=value (repeatable)")
+    ap.add_argument("--layout", help="profile mode, gemm case: run gemm_f16 with order,transa,transb,bias_mode "
+                                     "(e.g. 0,0,1,2) instead of gemm_f16_colmajor")
     args = ap.parse_args(argv)
     if args.case:
         run_case(args)
