@@ -2,9 +2,9 @@
 
 This module is shared by the tests, the smoke check, the benchmark and the
 oracle's callers.  It holds none of the method's arithmetic: it draws numbers
-with numpy's PCG64 generator and turns them into 16-bit patterns with library
-casts (numpy for FP16, torch for BF16).  The same bit patterns then feed both
-the CUDA path and the oracle.
+with numpy's PCG64 generator and turns them into 16-bit patterns or FP8 codes
+with library casts (numpy for FP16, torch for BF16 and FP8).  The same bit
+patterns then feed both the CUDA path and the oracle.
 
 Recipe (the pages name the shapes but give no seeds or value distributions):
 
@@ -15,7 +15,8 @@ Recipe (the pages name the shapes but give no seeds or value distributions):
   ``rng.standard_normal()``; ``int2``: ``rng.integers(-2, 3)`` (entries in
   {-2,...,2}, every partial sum of a product is an integer);
 * values are drawn in float64, in fixed chunks, then cast to FP16 (numpy) or
-  to float32 and then BF16 (torch).
+  to float32 and then BF16, FP8 E4M3 or FP8 E5M2 (torch's float8_e4m3fn /
+  float8_e5m2 casts).
 """
 from __future__ import annotations
 
@@ -71,6 +72,33 @@ def to_bf16_bits(values: np.ndarray) -> np.ndarray:
         t = torch.from_numpy(flat_in[lo:hi].astype(np.float32)).to(torch.bfloat16)
         flat_out[lo:hi] = t.view(torch.int16).numpy().view(np.uint16)
     return out
+
+
+def to_fp8_bits(values: np.ndarray, fmt: str) -> np.ndarray:
+    """FP8 codes (uint8) of ``values``: cast to float32, then torch's float8 cast
+    (``fmt`` 'e4m3' -> float8_e4m3fn, 'e5m2' -> float8_e5m2)."""
+    import torch
+
+    dtype = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[fmt]
+    out = np.empty(values.shape, np.uint8)
+    flat_in = values.reshape(-1)
+    flat_out = out.reshape(-1)
+    for lo in range(0, flat_in.size, _CHUNK):
+        hi = min(flat_in.size, lo + _CHUNK)
+        t = torch.from_numpy(flat_in[lo:hi].astype(np.float32)).to(dtype)
+        flat_out[lo:hi] = t.view(torch.uint8).numpy()
+    return out
+
+
+def fp8_operands(M: int, N: int, K: int, dist: str, fmt: str, seed_a: int = 1, seed_b: int = 2):
+    """FP8 operands of the K-major FP8 GEMM as flat uint8 arrays.
+
+    Returns ``(A, B)`` with ``A[k + m*K]`` (M*K entries) and ``B[k + n*K]``
+    (K*N entries).
+    """
+    A = to_fp8_bits(draw(dist, M * K, seed_a), fmt)
+    B = to_fp8_bits(draw(dist, K * N, seed_b), fmt)
+    return A, B
 
 
 def gemm_operands(M: int, N: int, K: int, dist: str, seed_a: int = 1, seed_b: int = 2):

@@ -103,6 +103,15 @@ def _load():
                                        f64p, u16p, ctypes.c_int]
         getattr(lib, name).restype = ctypes.c_int
     ci = ctypes.c_int
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    lib.orc_f32_encode_n.argtypes = [f64p, u32p, i64]
+    lib.orc_f32_encode_n.restype = None
+    lib.orc_fp8_decode_n.argtypes = [u8p, f64p, i64, ci]
+    lib.orc_fp8_decode_n.restype = None
+    lib.orc_gemm_fp8.argtypes = [ci, u8p, i64, u8p, i64, i64, i64, i64, ctypes.c_double, ci,
+                                 i64p, i64, i64p, i64, f64p, u32p, u16p, ci]
+    lib.orc_gemm_fp8.restype = ctypes.c_int
     lib.orc_gemm_f16_general.argtypes = [ci, ci, ci, u16p, i64, u16p, i64, i64, i64, i64, u16p, ci,
                                          i64p, i64, i64p, i64, f64p, u16p, ci]
     lib.orc_gemm_f16_general.restype = ctypes.c_int
@@ -262,6 +271,67 @@ def gemm_f16_general(A, B, M: int, N: int, K: int, lda: int, ldb: int, transa: i
     if rc != 0:
         raise RuntimeError(f"oracle general gemm failed ({rc})")
     return ref, out
+
+
+# --------------------------------------------------------------------------
+# FP8 GEMM: C(m,n) = alpha * sum_k A(m,k) B(k,n), FP32 accumulator
+# --------------------------------------------------------------------------
+
+def f32_encode(x) -> np.ndarray:
+    """float64 -> binary32 bits (uint32), one round-to-nearest-even."""
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(v.shape, np.uint32)
+    _load().orc_f32_encode_n(_ptr(v, ctypes.c_double), _ptr(out, ctypes.c_uint32), v.size)
+    return out
+
+
+def fp8_decode(codes, fmt: str) -> np.ndarray:
+    """FP8 codes (uint8) -> float64; fmt 'e4m3' or 'e5m2'."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().orc_fp8_decode_n(_ptr(c, ctypes.c_uint8), _ptr(out, ctypes.c_double), c.size, _fp8_flag(fmt))
+    return out
+
+
+def _fp8_flag(fmt: str) -> int:
+    if fmt not in ("e4m3", "e5m2"):
+        raise ValueError("oracle: FP8 format must be 'e4m3' or 'e5m2'")
+    return 1 if fmt == "e5m2" else 0
+
+
+def gemm_fp8(A, B, M: int, N: int, K: int, lda: int, ldb: int, fmt: str = "e4m3", alpha: float = 1.0,
+             out: str = "f32", rows=None, cols=None, threads: int = 0):
+    """Oracle for the FP8 GEMM: C(m,n) = alpha * sum_k A(m,k) B(k,n) with
+    A(m,k) = A[k + m*lda] and B(k,n) = B[k + n*ldb] (uint8 codes, both K-major).
+
+    Returns ``(ref, out_bits)`` for the selected rows x columns (all when None),
+    flat and column-major over the selection: ``ref`` the float64 value after
+    alpha, ``out_bits`` one RN rounding of it to FP32 (uint32 bits, out='f32')
+    or BF16 (uint16 bits, out='bf16').
+    """
+    A = np.ascontiguousarray(A, dtype=np.uint8).reshape(-1)
+    B = np.ascontiguousarray(B, dtype=np.uint8).reshape(-1)
+    if out not in ("f32", "bf16"):
+        raise ValueError("oracle: FP8 GEMM output must be 'f32' or 'bf16'")
+    if lda < max(1, K) or ldb < max(1, K):
+        raise ValueError("oracle: leading dimension below K")
+    if (M and K and A.size < (M - 1) * lda + K) or (N and K and B.size < (N - 1) * ldb + K):
+        raise ValueError("oracle: operands smaller than their shapes and leading dimensions")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else r.size
+    nc = N if c is None else c.size
+    ref = np.empty(nr * nc, np.float64)
+    o32 = np.empty(nr * nc, np.uint32) if out == "f32" else None
+    o16 = np.empty(nr * nc, np.uint16) if out == "bf16" else None
+    rc = _load().orc_gemm_fp8(
+        _fp8_flag(fmt), _ptr(A, ctypes.c_uint8), lda, _ptr(B, ctypes.c_uint8), ldb, M, N, K, float(alpha),
+        0 if out == "f32" else 1, _ptr(r, ctypes.c_int64), 0 if r is None else r.size,
+        _ptr(c, ctypes.c_int64), 0 if c is None else c.size, _ptr(ref, ctypes.c_double),
+        _ptr(o32, ctypes.c_uint32), _ptr(o16, ctypes.c_uint16), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle FP8 gemm failed ({rc})")
+    return ref, (o32 if out == "f32" else o16)
 
 
 # --------------------------------------------------------------------------

@@ -21,6 +21,9 @@
  *    independent dot product over the whole k range.  BF16 in, BF16 out.
  *  - Same article, sections 6.1 and 7: decode attention over a paged KV
  *    cache (see orc_decode_attention_bf16 at the end of this file).
+ *  - The FP8 GEMM (orc_gemm_fp8): E4M3 or E5M2 inputs, FP32 accumulator,
+ *    the FP8 row of the matrix-instruction table in "Hygon 优化", section
+ *    DUMMA 矩阵指令形状.
  *  - The FP16 GEMM in other storage forms (transposed operands, row-major
  *    storage, any leading dimension) with an optional bias: the BLAS reading
  *    of section 2's GEMM, with the bias the DCU article's section 6.1 names
@@ -89,7 +92,8 @@ double orc_bf16_decode(uint16_t h)
 
 /*
  * Round a double to a binary format with `frac_bits` fraction bits, exponent
- * bias `bias` and all-ones exponent `emax_field`, nearest-even.
+ * bias `bias`, all-ones exponent `emax_field` and the sign at bit `sign_bit`,
+ * nearest-even.
  *
  * |x| is written as n * q where q is the spacing of representable values in
  * x's binade (or the subnormal spacing below the normal range).  x / q is an
@@ -97,13 +101,13 @@ double orc_bf16_decode(uint16_t h)
  * mode rounds it to the nearest integer with ties to even.  n == 2^(frac+1)
  * means the value rounded up into the next binade.
  */
-static uint16_t orc_round_to_format(double x, int frac_bits, int bias, int emax_field)
+static uint32_t orc_round_bits(double x, int frac_bits, int bias, int emax_field, int sign_bit)
 {
-    uint16_t sign = signbit(x) ? (uint16_t)(1u << 15) : 0;
-    uint16_t inf = (uint16_t)(emax_field << frac_bits);
-    if (isnan(x)) return (uint16_t)(sign | inf | (1u << (frac_bits - 1)));
+    uint32_t sign = signbit(x) ? (1u << sign_bit) : 0u;
+    uint32_t inf = (uint32_t)emax_field << frac_bits;
+    if (isnan(x)) return sign | inf | (1u << (frac_bits - 1));
     double a = fabs(x);
-    if (isinf(a)) return (uint16_t)(sign | inf);
+    if (isinf(a)) return sign | inf;
     if (a == 0.0) return sign;
 
     int ex;
@@ -114,7 +118,7 @@ static uint16_t orc_round_to_format(double x, int frac_bits, int bias, int emax_
         /* subnormal range: spacing 2^(emin - frac_bits) */
         double n = rint(ldexp(a, frac_bits - emin));
         /* n == 2^frac_bits is exactly the smallest normal's encoding */
-        return (uint16_t)(sign | (uint16_t)n);
+        return sign | (uint32_t)n;
     }
     double n = rint(ldexp(a, frac_bits - E));   /* in [2^frac, 2^(frac+1)] */
     if (n >= ldexp(1.0, frac_bits + 1)) {
@@ -122,13 +126,49 @@ static uint16_t orc_round_to_format(double x, int frac_bits, int bias, int emax_
         E += 1;
     }
     int field = E + bias;
-    if (field >= emax_field) return (uint16_t)(sign | inf);
+    if (field >= emax_field) return sign | inf;
     uint32_t frac = (uint32_t)n - (1u << frac_bits);
-    return (uint16_t)(sign | (uint16_t)(field << frac_bits) | (uint16_t)frac);
+    return sign | ((uint32_t)field << frac_bits) | frac;
+}
+
+static uint16_t orc_round_to_format(double x, int frac_bits, int bias, int emax_field)
+{
+    return (uint16_t)orc_round_bits(x, frac_bits, bias, emax_field, 15);
 }
 
 uint16_t orc_f16_encode_rn(double x) { return orc_round_to_format(x, 10, 15, 31); }
 uint16_t orc_bf16_encode_rn(double x) { return orc_round_to_format(x, 7, 127, 255); }
+/* binary32: 1 sign bit, 8 exponent bits (bias 127), 23 fraction bits. */
+uint32_t orc_f32_encode_rn(double x) { return orc_round_bits(x, 23, 127, 255, 31); }
+
+/*
+ * The two FP8 formats of the matrix-instruction table ("Hygon 优化", section
+ * DUMMA 矩阵指令形状), in their common (OCP 8-bit floating point) definition:
+ *   E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; exponent
+ *         field 0 is subnormal (f/8 * 2^-6); there is no infinity, and only
+ *         exponent 15 with fraction 7 is NaN, so the largest value is 448.
+ *   E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits, IEEE-style:
+ *         field 0 subnormal (f/4 * 2^-14), field 31 infinity (f = 0) or NaN.
+ */
+double orc_fp8_decode(uint8_t c, int e5m2)
+{
+    int sign = (c >> 7) & 1;
+    double v;
+    if (e5m2) {
+        int e = (c >> 2) & 0x1f;
+        int f = c & 0x3;
+        if (e == 0) v = ldexp((double)f, -16);                 /* f/4 * 2^-14 */
+        else if (e == 31) v = f ? NAN : INFINITY;
+        else v = ldexp((double)(4 + f), e - 17);               /* (1.f) * 2^(e-15) */
+    } else {
+        int e = (c >> 3) & 0xf;
+        int f = c & 0x7;
+        if (e == 0) v = ldexp((double)f, -9);                  /* f/8 * 2^-6 */
+        else if (e == 15 && f == 7) v = NAN;
+        else v = ldexp((double)(8 + f), e - 10);               /* (1.f) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
 
 /* Bulk versions for the Python side. */
 void orc_f16_decode_n(const uint16_t* in, double* out, int64_t n)
@@ -146,6 +186,14 @@ void orc_f16_encode_n(const double* in, uint16_t* out, int64_t n)
 void orc_bf16_encode_n(const double* in, uint16_t* out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_encode_rn(in[i]);
+}
+void orc_f32_encode_n(const double* in, uint32_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_encode_rn(in[i]);
+}
+void orc_fp8_decode_n(const uint8_t* in, double* out, int64_t n, int e5m2)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_fp8_decode(in[i], e5m2);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -353,6 +401,53 @@ int orc_gemm_f16_general(int row_major, int transa, int transb,
     }
     free(lut);
     return fail;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 GEMM: C(m,n) = alpha * sum_k A(m,k) B(k,n), FP32 accumulator          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The FP8 row of the matrix-instruction table ("Hygon 优化", section DUMMA
+ * 矩阵指令形状): FP8 (E4M3 or E5M2) inputs, FP32 accumulator; the product is
+ * the GEMM of "MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 2.
+ * Both operands are stored K-major (the k values of one row of A, or of one
+ * column of B, contiguous): A(m,k) = A[k + m*lda], B(k,n) = B[k + n*ldb].
+ * Every product of two FP8 values is exact in double and the sum runs over k
+ * ascending in double; the result is scaled by alpha and rounded once to the
+ * output format: out_type 0 = FP32 (written to out32), 1 = BF16 (out16).
+ * Rows `rows` (all M when NULL) x columns `cols` (all N when NULL); entry
+ * (i, j) of the selection at index i + j*nr.
+ */
+int orc_gemm_fp8(int e5m2, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+                 int64_t M, int64_t N, int64_t K, double alpha, int out_type,
+                 const int64_t* rows, int64_t nrows, const int64_t* cols, int64_t ncols,
+                 double* ref, uint32_t* out32, uint16_t* out16, int threads)
+{
+    if (M < 0 || N < 0 || K < 0 || out_type < 0 || out_type > 1) return 1;
+    int64_t nr = rows ? nrows : M;
+    int64_t nc = cols ? ncols : N;
+    double lut[256];
+    for (int c = 0; c < 256; ++c) lut[c] = orc_fp8_decode((uint8_t)c, e5m2);
+    orc_set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < nc; ++j) {
+        int64_t n = cols ? cols[j] : j;
+        for (int64_t i = 0; i < nr; ++i) {
+            int64_t m = rows ? rows[i] : i;
+            double acc = 0.0;
+            if (n >= 0 && n < N && m >= 0 && m < M) {
+                const uint8_t* a_row = A + m * lda;
+                const uint8_t* b_col = B + n * ldb;
+                for (int64_t k = 0; k < K; ++k) acc += lut[a_row[k]] * lut[b_col[k]];
+            }
+            double v = alpha * acc;
+            if (ref) ref[i + j * nr] = v;
+            if (out_type == 0 && out32) out32[i + j * nr] = orc_f32_encode_rn(v);
+            if (out_type == 1 && out16) out16[i + j * nr] = orc_bf16_encode_rn(v);
+        }
+    }
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */

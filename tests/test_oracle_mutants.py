@@ -13,6 +13,7 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 PINS = "test_oracle_pins.py"
 ATTN_PINS = "test_oracle_attention_pins.py"
 LAYOUT_PINS = "test_oracle_layout_pins.py"
+FP8_PINS = "test_oracle_fp8_pins.py"
 
 # (name, text to replace, replacement, count[, pins file]) -- each must occur in oracle.c
 MUTANTS = [
@@ -27,7 +28,7 @@ MUTANTS = [
     ("bf16_double_rounding", "return orc_round_to_format(x, 7, 127, 255);",
      "return orc_round_to_format((double)(float)x, 7, 127, 255);", 1),
     ("linear_reversed_k", "acc += xr[k] * lut[wrow[k]];", "acc += xr[k] * lut[wrow[K - 1 - k]];", 2),
-    ("f32_accumulator", "double* acc = (double*)malloc", "float* acc = (float*)malloc", 1),
+    ("f32_accumulator", "double* acc = (double*)malloc", "float* acc = (float*)malloc", 2),
     ("attn_drop_last_token", "for (int64_t t = 0; t < L; ++t) {\n                    const int64_t blk",
      "for (int64_t t = 0; t < L - 1; ++t) {\n                    const int64_t blk", 1, ATTN_PINS),
     ("attn_wrong_group", "const int64_t g = h / group;", "const int64_t g = h % num_kv_heads;", 1, ATTN_PINS),
@@ -45,6 +46,18 @@ MUTANTS = [
     ("general_bias_after_rounding", "if (out) out[i + j * nr] = orc_f16_encode_rn(v);",
      "if (out) out[i + j * nr] = orc_f16_encode_rn(lut[orc_f16_encode_rn(acc[i])] + (v - acc[i]));", 1,
      LAYOUT_PINS),
+    ("fp8_e4m3_wrong_bias", "else v = ldexp((double)(8 + f), e - 10);", "else v = ldexp((double)(8 + f), e - 11);", 1,
+     FP8_PINS),
+    ("fp8_e4m3_ieee_nan_rule", "else if (e == 15 && f == 7) v = NAN;", "else if (e == 15) v = NAN;", 1, FP8_PINS),
+    ("fp8_e5m2_subnormal_scale", "if (e == 0) v = ldexp((double)f, -16);", "if (e == 0) v = ldexp((double)f, -15);", 1,
+     FP8_PINS),
+    ("fp8_alpha_ignored", "double v = alpha * acc;", "double v = acc;", 1, FP8_PINS),
+    ("fp8_reversed_b", "acc += lut[a_row[k]] * lut[b_col[k]];", "acc += lut[a_row[k]] * lut[b_col[K - 1 - k]];", 1,
+     FP8_PINS),
+    ("f32_wrong_sign_bit", "return orc_round_bits(x, 23, 127, 255, 31);", "return orc_round_bits(x, 23, 127, 255, 15);",
+     1, FP8_PINS),
+    ("fp8_bf16_double_rounding", "out16[i + j * nr] = orc_bf16_encode_rn(v);",
+     "out16[i + j * nr] = orc_bf16_encode_rn((double)(float)v);", 1, FP8_PINS),
 ]
 
 
