@@ -11,6 +11,10 @@ from ._native import (  # noqa: F401
     BIAS_NONE,
     BIAS_ROW,
     COL_MAJOR,
+    FP8_E4M3,
+    FP8_E5M2,
+    OUT_BF16,
+    OUT_F32,
     ROW_MAJOR,
     BskError,
     decode_attention_bf16,
@@ -19,6 +23,8 @@ from ._native import (  # noqa: F401
     gemm_f16_colmajor_enqueue,
     gemm_f16_colmajor_noalloc,
     gemm_f16_enqueue,
+    gemm_fp8,
+    gemm_fp8_enqueue,
     gemv_bf16,
     gemv_bf16_enqueue,
     last_error,

@@ -46,10 +46,13 @@ EXPORTS = (
     "bsk_stream_check", "bsk_last_error", "bsk_status_string", "bsk_version", "bsk_tile_coord",
     "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout", "gemm_f16_colmajor_noalloc",
     "decode_attention_bf16", "bsk_decode_attention_bf16_enqueue", "gemm_f16", "bsk_gemm_f16_enqueue",
+    "gemm_fp8", "bsk_gemm_fp8_enqueue",
 )
 
 COL_MAJOR, ROW_MAJOR = 0, 1
 BIAS_NONE, BIAS_ROW, BIAS_COLUMN = 0, 1, 2
+FP8_E4M3, FP8_E5M2 = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
 
 
 class BskError(RuntimeError):
@@ -81,6 +84,9 @@ def load():
             getattr(lib, name).restype = i
         for name in ("gemm_f16", "bsk_gemm_f16_enqueue"):
             getattr(lib, name).argtypes = [i, i, i, p, i, p, i, p, i, i, i, i, p, i, p]
+            getattr(lib, name).restype = i
+        for name in ("gemm_fp8", "bsk_gemm_fp8_enqueue"):
+            getattr(lib, name).argtypes = [i, p, i, p, i, p, i, i, i, i, i, ctypes.c_float, p]
             getattr(lib, name).restype = i
         for name in ("gemv_bf16", "bsk_gemv_bf16_enqueue"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
@@ -158,6 +164,21 @@ def gemm_f16_enqueue(order: int, transa: int, transb: int, A, lda: int, B, ldb: 
     """Asynchronous variant of gemm_f16 (check with stream_check)."""
     _check(load().bsk_gemm_f16_enqueue(order, transa, transb, _addr(A), lda, _addr(B), ldb, _addr(C), ldc, M, N,
                                        K, _addr(bias), bias_mode, _stream(stream)))
+
+
+def gemm_fp8(fmt: int, A, lda: int, B, ldb: int, C, ldc: int, out_type: int, M: int, N: int, K: int,
+             alpha: float = 1.0, stream=None) -> None:
+    """C(m,n) = alpha * sum_k A(m,k) B(k,n): FP8 codes, A[k + m*lda], B[k + n*ldb],
+    C column-major FP32 or BF16; blocks until done."""
+    _check(load().gemm_fp8(fmt, _addr(A), lda, _addr(B), ldb, _addr(C), ldc, out_type, M, N, K, float(alpha),
+                           _stream(stream)))
+
+
+def gemm_fp8_enqueue(fmt: int, A, lda: int, B, ldb: int, C, ldc: int, out_type: int, M: int, N: int, K: int,
+                     alpha: float = 1.0, stream=None) -> None:
+    """Asynchronous variant of gemm_fp8 (check with stream_check)."""
+    _check(load().bsk_gemm_fp8_enqueue(fmt, _addr(A), lda, _addr(B), ldb, _addr(C), ldc, out_type, M, N, K,
+                                       float(alpha), _stream(stream)))
 
 
 def gemm_f16_colmajor_noalloc(A, B, C, M: int, N: int, K: int, stream=None) -> None:

@@ -143,7 +143,6 @@ bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-long long round_up8(long long v) { return (v + 7) / 8 * 8; }
 
 // Stream-ordered workspace for packed operands, freed in stream order after use.
 struct Workspace {
@@ -171,58 +170,72 @@ int alloc_workspace(Workspace& ws, size_t bytes, cudaStream_t s)
 // One GEMM as the kernels see it: C (column-major, M x N, leading dimension
 // ldc) = A (M x K) * B (K x N) [+ bias].  A is MN-major (A(m,k) at
 // A[m + k*lda]) or K-major (A[k + m*lda]); B is K-major (B[k + n*ldb]) or
-// MN-major (B[n + k*ldb]).
+// MN-major (B[n + k*ldb]).  Leading dimensions count elements.
 struct GemmOp {
-    const uint16_t* A = nullptr;
+    const void* A = nullptr;
     long long lda = 0;
     bool a_mn_major = true;
-    const uint16_t* B = nullptr;
+    const void* B = nullptr;
     long long ldb = 0;
     bool b_mn_major = false;
-    uint16_t* C = nullptr;
+    void* C = nullptr;
     long long ldc = 0;
     int M = 0, N = 0, K = 0;
-    bool bf16 = false;
+    int in_type = bsk::kInF16;
+    int out_type = bsk::kOutF16;
+    float alpha = 1.0f;
     const uint16_t* bias = nullptr;
     int bias_mode = 0;
 };
 
+// Copies an operand into the workspace with a 16-byte-multiple leading dimension.
+int pack_operand(const void* src, long long ld_src, void* dst, long long ld_dst, int inner, int outer, int eb,
+                 cudaStream_t s, char* msg, size_t msg_len)
+{
+    if (eb == 1)
+        return bsk::launch_pack_8bit(static_cast<const uint8_t*>(src), ld_src, static_cast<uint8_t*>(dst), ld_dst,
+                                     inner, outer, s, msg, msg_len);
+    return bsk::launch_pack(static_cast<const uint16_t*>(src), ld_src, static_cast<uint16_t*>(dst), ld_dst, inner,
+                            outer, s, msg, msg_len);
+}
+
 // Runs the tcgen05 GEMM on operands in any layout TMA may not take directly:
 // an operand whose base is not 16-byte aligned or whose leading dimension is
-// not a multiple of 8 elements is packed into a stream-ordered workspace.
+// not a multiple of 16 bytes is packed into a stream-ordered workspace.
 int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
 {
     const bool force_pack = opt_or(BSK_OPT_FORCE_PACK, 0) != 0;
+    const bool fp8 = op.in_type == bsk::kInE4M3 || op.in_type == bsk::kInE5M2;
+    const int eb = fp8 ? 1 : 2;              // element bytes of A and B
+    const long long ld_unit = 16 / eb;       // elements per 16 bytes
     // stored extents: `inner` contiguous elements in each of `outer` lines
     const int a_inner = op.a_mn_major ? op.M : op.K, a_outer = op.a_mn_major ? op.K : op.M;
     const int b_inner = op.b_mn_major ? op.N : op.K, b_outer = op.b_mn_major ? op.K : op.N;
-    const bool a_ok = !force_pack && aligned16(op.A) && (op.lda % 8 == 0);
-    const bool b_ok = !force_pack && aligned16(op.B) && (op.ldb % 8 == 0);
-    const long long lda_p = a_ok ? op.lda : round_up8(a_inner);
-    const long long ldb_p = b_ok ? op.ldb : round_up8(b_inner);
-    size_t a_bytes = a_ok ? 0 : static_cast<size_t>(lda_p) * a_outer * 2;
-    size_t b_bytes = b_ok ? 0 : static_cast<size_t>(ldb_p) * b_outer * 2;
+    const bool a_ok = !force_pack && aligned16(op.A) && (op.lda % ld_unit == 0);
+    const bool b_ok = !force_pack && aligned16(op.B) && (op.ldb % ld_unit == 0);
+    const long long lda_p = a_ok ? op.lda : (a_inner + ld_unit - 1) / ld_unit * ld_unit;
+    const long long ldb_p = b_ok ? op.ldb : (b_inner + ld_unit - 1) / ld_unit * ld_unit;
+    size_t a_bytes = a_ok ? 0 : static_cast<size_t>(lda_p) * a_outer * eb;
+    size_t b_bytes = b_ok ? 0 : static_cast<size_t>(ldb_p) * b_outer * eb;
     a_bytes = (a_bytes + 255) / 256 * 256;
 
     Workspace ws;
-    const uint16_t* Ause = op.A;
-    const uint16_t* Buse = op.B;
+    const void* Ause = op.A;
+    const void* Buse = op.B;
     char msg[512] = "";
     if (a_bytes + b_bytes > 0) {
         int st = alloc_workspace(ws, a_bytes + b_bytes, s);
         if (st != BSK_OK) return st;
         uint8_t* base = static_cast<uint8_t*>(ws.ptr);
         if (!a_ok) {
-            uint16_t* Ap = reinterpret_cast<uint16_t*>(base);
-            if (bsk::launch_pack(op.A, op.lda, Ap, lda_p, a_inner, a_outer, s, msg, sizeof(msg)))
+            if (pack_operand(op.A, op.lda, base, lda_p, a_inner, a_outer, eb, s, msg, sizeof(msg)))
                 return fail(BSK_ERR_CUDA, "%s", msg);
-            Ause = Ap;
+            Ause = base;
         }
         if (!b_ok) {
-            uint16_t* Bp = reinterpret_cast<uint16_t*>(base + a_bytes);
-            if (bsk::launch_pack(op.B, op.ldb, Bp, ldb_p, b_inner, b_outer, s, msg, sizeof(msg)))
+            if (pack_operand(op.B, op.ldb, base + a_bytes, ldb_p, b_inner, b_outer, eb, s, msg, sizeof(msg)))
                 return fail(BSK_ERR_CUDA, "%s", msg);
-            Buse = Bp;
+            Buse = base + a_bytes;
         }
     }
 
@@ -238,7 +251,9 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     g.M = op.M;
     g.N = op.N;
     g.K = op.K;
-    g.bf16 = op.bf16;
+    g.in_type = op.in_type;
+    g.out_type = op.out_type;
+    g.alpha = op.alpha;
     g.bias = op.bias_mode != 0 ? op.bias : nullptr;
     g.bias_mode = op.bias_mode;
     // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
@@ -254,7 +269,8 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     // TMA store of C: 16-byte aligned base and ldc, and M a multiple of 8.  With
     // a ragged M the store's clipping was seen to write up to the end of the
     // last 16-byte unit, i.e. into C's padding rows when ldc > M.
-    g.tma_store = aligned16(op.C) && (op.ldc % 8 == 0) && (op.M % 8 == 0) &&
+    // FP32 outputs always take the coalesced direct stores (32 lanes x 4 bytes).
+    g.tma_store = op.out_type != bsk::kOutF32 && aligned16(op.C) && (op.ldc % 8 == 0) && (op.M % 8 == 0) &&
                   opt_or(BSK_OPT_FORCE_DIRECT_STORE, 0) == 0;
     g.num_sms = sms;
     g.status = g_status_dev;
@@ -341,6 +357,55 @@ int enqueue_gemm_f16_cblas(int order, int transa, int transb, const uint16_t* A,
     return enqueue_gemm_general(transb, transa, B, ldb, A, lda, C, ldc, N, M, K, bias, swapped_mode, stream);
 }
 
+int enqueue_gemm_fp8(int format, const uint8_t* A, int lda, const uint8_t* B, int ldb, void* C, int ldc,
+                     int out_type, int M, int N, int K, float alpha, void* stream)
+{
+    if (M < 0 || N < 0 || K < 0) return fail(BSK_ERR_INVALID_ARG, "negative size (M=%d N=%d K=%d)", M, N, K);
+    if (format != BSK_FP8_E4M3 && format != BSK_FP8_E5M2)
+        return fail(BSK_ERR_INVALID_ARG, "format must be BSK_FP8_E4M3 or BSK_FP8_E5M2 (got %d)", format);
+    if (out_type != BSK_OUT_F32 && out_type != BSK_OUT_BF16)
+        return fail(BSK_ERR_INVALID_ARG, "out_type must be BSK_OUT_F32 or BSK_OUT_BF16 (got %d)", out_type);
+    if (!std::isfinite(alpha)) return fail(BSK_ERR_INVALID_ARG, "alpha must be finite");
+    if (lda < (K > 1 ? K : 1) || ldb < (K > 1 ? K : 1) || ldc < (M > 1 ? M : 1))
+        return fail(BSK_ERR_INVALID_ARG, "leading dimension too small (lda=%d ldb=%d ldc=%d for M=%d N=%d K=%d)", lda,
+                    ldb, ldc, M, N, K);
+    if (M == 0 || N == 0) return BSK_OK;
+    const size_t ob = out_type == BSK_OUT_F32 ? 4 : 2;
+    const size_t a_bytes = static_cast<size_t>(span_elems(K, M, lda));
+    const size_t b_bytes = static_cast<size_t>(span_elems(K, N, ldb));
+    const size_t c_bytes = static_cast<size_t>(span_elems(M, N, ldc)) * ob;
+    if (C == nullptr) return fail(BSK_ERR_INVALID_ARG, "C is NULL");
+    if (K > 0 && (A == nullptr || B == nullptr)) return fail(BSK_ERR_INVALID_ARG, "A or B is NULL");
+    if (overlaps(C, c_bytes, A, K > 0 ? a_bytes : 0) || overlaps(C, c_bytes, B, K > 0 ? b_bytes : 0))
+        return fail(BSK_ERR_INVALID_ARG, "C overlaps an input");
+    const long long tiles = ((M + 127LL) / 128) * ((N + 127LL) / 128);
+    if (tiles > INT_MAX) return fail(BSK_ERR_INVALID_ARG, "problem too large (%lld tiles)", tiles);
+    int sms = 0;
+    int st = prepare_device(&sms);
+    if (st != BSK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * ob, 0, static_cast<size_t>(M) * ob, N, s);
+        return e == cudaSuccess ? BSK_OK : fail_cuda(e, "cudaMemset2DAsync");
+    }
+    GemmOp op;
+    op.A = A;
+    op.lda = lda;
+    op.a_mn_major = false;
+    op.B = B;
+    op.ldb = ldb;
+    op.b_mn_major = false;
+    op.C = C;
+    op.ldc = ldc;
+    op.M = M;
+    op.N = N;
+    op.K = K;
+    op.in_type = format == BSK_FP8_E5M2 ? bsk::kInE5M2 : bsk::kInE4M3;
+    op.out_type = out_type == BSK_OUT_F32 ? bsk::kOutF32 : bsk::kOutBF16;
+    op.alpha = alpha;
+    return run_gemm(op, sms, s);
+}
+
 int enqueue_gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream)
 {
     return enqueue_gemm_general(0, 0, A, M > 1 ? M : 1, B, K > 1 ? K : 1, C, M > 1 ? M : 1, M, N, K, nullptr, 0,
@@ -396,7 +461,8 @@ int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, 
     op.M = M;
     op.N = n;
     op.K = K;
-    op.bf16 = true;
+    op.in_type = bsk::kInBF16;
+    op.out_type = bsk::kOutBF16;
     return run_gemm(op, sms, s);
 }
 
@@ -540,6 +606,21 @@ int bsk_gemm_f16_enqueue(int order, int transa, int transb, const uint16_t* A, i
                          void* stream)
 {
     return enqueue_gemm_f16_cblas(order, transa, transb, A, lda, B, ldb, C, ldc, M, N, K, bias, bias_mode, stream);
+}
+
+int gemm_fp8(int format, const uint8_t* A, int lda, const uint8_t* B, int ldb, void* C, int ldc, int out_type,
+             int M, int N, int K, float alpha, void* stream)
+{
+    int st = enqueue_gemm_fp8(format, A, lda, B, ldb, C, ldc, out_type, M, N, K, alpha, stream);
+    if (st != BSK_OK) return st;
+    if (M == 0 || N == 0) return BSK_OK;
+    return sync_and_check(static_cast<cudaStream_t>(stream));
+}
+
+int bsk_gemm_fp8_enqueue(int format, const uint8_t* A, int lda, const uint8_t* B, int ldb, void* C, int ldc,
+                         int out_type, int M, int N, int K, float alpha, void* stream)
+{
+    return enqueue_gemm_fp8(format, A, lda, B, ldb, C, ldc, out_type, M, N, K, alpha, stream);
 }
 
 int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,

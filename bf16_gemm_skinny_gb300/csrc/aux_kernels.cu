@@ -24,6 +24,20 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// The same copy for 8-bit elements (FP8 operands).
+__global__ void __launch_bounds__(256)
+    pack_8bit_kernel(const uint8_t* __restrict__ src, long long ld_src, uint8_t* __restrict__ dst, long long ld_dst,
+                     int inner, int outer)
+{
+    const long long total = static_cast<long long>(inner) * outer;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+        const long long j = e / inner;
+        const long long i = e - j * inner;
+        dst[i + j * ld_dst] = src[i + j * ld_src];
+    }
+}
+
 // C(m,n) = bias value (or +0.0) for m < M, n < N, C(m,n) at C[m + n*ldc]: the
 // K == 0 case of the GEMM (an empty sum plus the bias, already in the output
 // format, so no rounding happens).
@@ -72,6 +86,22 @@ int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long 
     long long grid = (total + 255) / 256;
     if (grid > 4096) grid = 4096;
     pack_16bit_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(src, ld_src, dst, ld_dst, inner, outer);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
+        return 1;
+    }
+    return 0;
+}
+
+int launch_pack_8bit(const uint8_t* src, long long ld_src, uint8_t* dst, long long ld_dst, int inner, int outer,
+                     cudaStream_t stream, char* msg, size_t msg_len)
+{
+    const long long total = static_cast<long long>(inner) * outer;
+    if (total <= 0) return 0;
+    long long grid = (total + 255) / 256;
+    if (grid > 4096) grid = 4096;
+    pack_8bit_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(src, ld_src, dst, ld_dst, inner, outer);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));

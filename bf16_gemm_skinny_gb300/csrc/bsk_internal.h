@@ -50,6 +50,11 @@ TmapEncodeFn tmap_encoder();
 // at A[k + m*lda]); B is K-major (B(k,n) at B[k + n*ldb]) or MN-major (B(k,n)
 // at B[n + k*ldb]).  A and B must be 16-byte aligned with 16-byte-multiple
 // leading dimensions (the caller packs them otherwise).
+// Element types of the GEMM: A and B share one input type; C has its own.
+// The FP8 types run on tcgen05.mma kind::f8f6f4 with K-major A and B only.
+enum GemmInType : int { kInF16 = 0, kInBF16 = 1, kInE4M3 = 2, kInE5M2 = 3 };
+enum GemmOutType : int { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2 };
+
 struct GemmLaunch {
     const void* A = nullptr;
     long long lda = 0;
@@ -60,7 +65,9 @@ struct GemmLaunch {
     void* C = nullptr;
     long long ldc = 0;
     int M = 0, N = 0, K = 0;
-    bool bf16 = false;
+    int in_type = kInF16;    // GemmInType of A and B
+    int out_type = kOutF16;  // GemmOutType of C
+    float alpha = 1.0f;      // FP8 inputs: C = alpha * A * B (the 16-bit kernels ignore it)
     int block_n = 256;       // 32, 64, 128 or 256
     bool pair = true;        // block_n == 256 only: CTA-pair kernel (256 x 256 tiles over two SMs)
     int group_m = 2;         // >= 1
@@ -74,6 +81,8 @@ struct GemmLaunch {
 
 // Returns 0 on success; otherwise an error message is written to `msg`.
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
+// The FP8 part of launch_gemm (gemm_fp8.cu).
+int launch_gemm_fp8(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
 
 // Decode GEMV / skinny GEMM on the CUDA cores: y[t, j] = sum_k x[t, k] W[j, k]
 // for t < n <= 8, W [M, K] row-major, x [n, K], y [n, M] row-major, BF16.
@@ -110,6 +119,10 @@ int launch_decode_attention(const AttnLaunch& a, cudaStream_t stream, char* msg,
 // leading dimension ld_src to ld_dst.  The source is only read.
 int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long ld_dst, int inner, int outer,
                 cudaStream_t stream, char* msg, size_t msg_len);
+
+// The same for 8-bit elements.
+int launch_pack_8bit(const uint8_t* src, long long ld_src, uint8_t* dst, long long ld_dst, int inner, int outer,
+                     cudaStream_t stream, char* msg, size_t msg_len);
 
 // C(m,n) = bias[m] (mode 1), bias[n] (mode 2) or +0.0 (mode 0) for the M x N
 // column-major C with leading dimension ldc: the GEMM with K == 0.

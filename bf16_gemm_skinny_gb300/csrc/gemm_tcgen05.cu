@@ -1,860 +1,67 @@
-// gemm_tcgen05.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
-//
-// Computes C = A * B with FP32 accumulation in tensor memory and one rounding
-// to FP16 or BF16 in the epilogue ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘",
-// section 1: FP16 in, FP32 accumulate, FP16 out; section 2: the column-major
-// addressing A(m,k) = A[m + k*M], B(k,n) = B[k + n*K], C(m,n) = C[m + n*M]).
-//
-// Structure (one CTA per SM, 192 threads):
-//   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-slices
-//               ("Hygon 优化", section 软件流水线: overlap the k-loop loads with
-//               the MMAs; the per-stage bytes are (BM + BN) * BK * 2).
-//   warp 1      allocates TMEM and issues tcgen05.mma from one thread; each
-//               stage's smem slot is released by tcgen05.commit when its MMAs
-//               have read it.
-//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator, rounding to
-//               16 bits, store to C (TMA store, or masked stores when C's
-//               leading dimension is not a multiple of 16 bytes).  There is no
-//               FP32 intermediate matrix and no separate conversion kernel.
-// The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
-// of tile i overlaps the mainloop of tile i+1.  Tiles are visited in the
-// grouped (GROUP_M) order of "Hygon 优化", section 分组调度.
-//
-// Tails: TMA zero-fills the parts of a box outside the tensor (M, N and K
-// tails contribute zero products) and the TMA store / masked store drop rows
-// and columns outside C ("Hygon 优化", section DUMMA 矩阵指令形状, on tail masks).
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include <cstdio>
-
-#include "bsk_internal.h"
-#include "ptx.cuh"
+// gemm_tcgen05.cu -- instances and dispatch of the 16-bit tcgen05 GEMMs
+// (FP16 in/out with any operand majorness, BF16 in/out with an MN- or K-major
+// A); the kernels are in gemm_tcgen05.cuh, the FP8 instances in gemm_fp8.cu.
+#include "gemm_tcgen05.cuh"
 
 namespace bsk {
-namespace {
-
-constexpr int kBM = 128;      // tile rows (TMEM lanes), one MMA of M = 128
-constexpr int kBK = 64;       // k per stage: one 128-byte swizzle row of 16-bit values
-constexpr int kUmmaK = 16;    // k per tcgen05.mma of kind::f16
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
-constexpr int kEpiBox = 32;   // epilogue chunk: 32 rows x 32 columns per warp
-
-template <int BN>
-struct Cfg {
-    // ring depth: as many stages as fit next to the epilogue buffers
-    static constexpr int kStages = BN == 256 ? 4 : BN == 128 ? 6 : BN == 64 ? 8 : 10;
-    static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = BN * kBK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kEpiBufBytes = kEpiBox * kEpiBox * 2;
-    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
-    static constexpr int kTmemCols = 2 * BN;
-    static constexpr int kNumBars = 2 * kStages + 5;
-    static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
-    static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area too small");
-    static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-};
-
-struct Params {
-    int M, N, K;
-    int num_m, num_n, num_tiles, num_kb;
-    int group_m;
-    void* C;
-    long long ldc;
-    int tma_store;
-    const uint16_t* bias;   // optional, output precision: bias[m] (mode 1) or bias[n] (mode 2)
-    int bias_mode;
-    int* status;
-    unsigned long long wait_limit_ns;
-};
-
-// Identifiers of the waits, reported in the status word on a timeout.
-enum WaitSite {
-    kSiteProducerEmpty = 1,
-    kSiteMmaTmemEmpty = 2,
-    kSiteMmaFull = 3,
-    kSiteEpilogueTmemFull = 4,
-    kSiteMmaDrain = 5,
-    kSiteProducerDrain = 6,
-};
-
-template <bool BF16>
-__device__ __forceinline__ uint16_t round_out(uint32_t acc_bits)
-{
-    const float v = __uint_as_float(acc_bits);
-    if constexpr (BF16) {
-        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-    } else {
-        return __half_as_ushort(__float2half_rn(v));
-    }
-}
-
-template <bool BF16>
-__device__ __forceinline__ float bias_value(const uint16_t* bias, int i)
-{
-    const uint16_t b = bias[i];
-    if constexpr (BF16) {
-        return __uint_as_float(static_cast<uint32_t>(b) << 16);
-    } else {
-        return __half2float(__ushort_as_half(b));
-    }
-}
-
-// Adds the bias to the FP32 accumulators of row m, columns n0..n0+31, before the
-// one rounding to the output type.
-template <bool BF16>
-__device__ __forceinline__ void add_bias(uint32_t (&r)[32], const Params& p, int m, int n0)
-{
-    if (p.bias_mode == 1) {
-        if (m < p.M) {
-            const float b = bias_value<BF16>(p.bias, m);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
-        }
-    } else if (p.bias_mode == 2) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (n0 + j < p.N) r[j] = __float_as_uint(__uint_as_float(r[j]) + bias_value<BF16>(p.bias, n0 + j));
-    }
-}
-
-template <int BN, bool A_MN, bool B_MN, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const Params p)
-{
-    using Cf = Cfg<BN>;
-    constexpr int S = Cf::kStages;
-    constexpr uint32_t kIdesc = idesc_f16(BF16, A_MN, B_MN, kBM, BN);
-    static_assert(!B_MN || BN % 64 == 0, "an MN-major B needs whole 64-column swizzle atoms");
-
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t* sA = smem;
-    uint8_t* sB = sA + S * Cf::kABytes;
-    uint8_t* sEpi = sB + S * Cf::kBBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + Cf::kEpiBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cf::kNumBars);
-    volatile uint32_t* abort_flag = tmem_slot + 1;
-
-    const uint32_t full0 = smem_u32(bars);            // S barriers: stage loaded
-    const uint32_t empty0 = full0 + 8 * S;            // S barriers: stage consumed
-    const uint32_t tfull0 = empty0 + 8 * S;           // 2 barriers: accumulator ready
-    const uint32_t tempty0 = tfull0 + 16;             // 2 barriers: accumulator drained
-    const uint32_t drain_bar = tempty0 + 16;          // abort path: MMAs finished
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull0 + 8 * a, 1);
-            mbar_init(tempty0 + 8 * a, kEpiWarps);
-        }
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0u;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-        if (p.tma_store) prefetch_tmap(&tmC);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), Cf::kTmemCols);
-        tmem_relinquish_alloc_permit();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_slot;
-    const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
-    // Waits on the abort path ignore the abort flag but keep the time limit.
-    uint32_t never = 0u;
-    const WaitCtl wc_drain{&never, p.status, p.wait_limit_ns};
-
-    if (warp == 0) {
-        // ------------------------------------------------------------------
-        // TMA producer
-        // ------------------------------------------------------------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            long long issued = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                int pm, pn;
-                tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
-                const int m0 = pm * kBM;
-                const int n0 = pn * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = full0 + 8 * stage;
-                    mbar_arrive_expect_tx(fb, Cf::kStageBytes);
-                    const uint32_t a_dst = smem_u32(sA + stage * Cf::kABytes);
-                    const uint32_t b_dst = smem_u32(sB + stage * Cf::kBBytes);
-                    const int k0 = kb * kBK;
-                    if constexpr (A_MN) {
-                        // two 64(m) x 64(k) boxes: m is the 128-byte swizzle row
-                        tma_load_2d(a_dst, &tmA, fb, m0, k0);
-                        tma_load_2d(a_dst + Cf::kABytes / 2, &tmA, fb, m0 + 64, k0);
-                    } else {
-                        tma_load_2d(a_dst, &tmA, fb, k0, m0);   // 64(k) x 128(m) box
-                    }
-                    if constexpr (B_MN) {
-#pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)   // 64(n) x 64(k) boxes, 8 KB apart
-                            tma_load_2d(b_dst + i * 8192, &tmB, fb, n0 + 64 * i, k0);
-                    } else {
-                        tma_load_2d(b_dst, &tmB, fb, k0, n0);    // 64(k) x BN(n) box
-                    }
-                    ++issued;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                // Abort: let the loads already issued land before the CTA can exit.
-                const long long pending = issued < S ? issued : S;
-                for (long long j = 1; j <= pending; ++j) {
-                    const int s = (stage - static_cast<int>(j) + S) % S;
-                    const uint32_t ph = (stage - static_cast<int>(j) < 0) ? (phase ^ 1u) : phase;
-                    mbar_wait(full0 + 8 * s, ph, wc_drain, kSiteProducerDrain);
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------
-        // MMA issuer (one thread)
-        // ------------------------------------------------------------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            bool issued_any = false;
-            int it = 0;
-            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-                const int acc = it & 1;
-                const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
-                if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t a_base = smem_u32(sA + stage * Cf::kABytes);
-                    const uint32_t b_base = smem_u32(sB + stage * Cf::kBBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        // MN-major A: 16 k-rows of 128 bytes per MMA, the two 64-element
-                        // m blocks 8 KB apart; K-major operands: 32 bytes along the row.
-                        const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, Cf::kABytes / 2, 1024)
-                                                 : smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
-                                                 : smem_desc_sw128(b_base + kk * 32, 16, 1024);
-                        mma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
-                    mma_commit(empty0 + 8 * stage);
-                    issued_any = true;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                mma_commit(tfull0 + 8 * acc);
-            }
-            if (!ok && issued_any) {
-                // Abort: every MMA issued so far must finish before TMEM is freed.
-                mma_commit(drain_bar);
-                mbar_wait(drain_bar, 0u, wc_drain, kSiteMmaDrain);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------------
-        // Epilogue: TMEM -> registers -> 16-bit -> C
-        // ------------------------------------------------------------------
-        const int quarter = warp & 3;             // TMEM lanes this warp may read
-        const int ew = warp - 2;                  // owner of a staging buffer pair
-        uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
-        uint16_t* Cg = reinterpret_cast<uint16_t*>(p.C);
-        int it = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-            const int acc = it & 1;
-            const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
-            bool ok = mbar_wait(tfull0 + 8 * acc, aph, wc, kSiteEpilogueTmemFull);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after_sync();
-            int pm, pn;
-            tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
-            const int m0 = pm * kBM + quarter * 32;
-            const int n0 = pn * BN;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c * 32, r);
-                tmem_ld_wait();
-                if (c == BN / 32 - 1) {
-                    // all of this accumulator is in registers: hand TMEM back to the MMA warp
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-                }
-                if (p.bias_mode != 0) add_bias<BF16>(r, p, m0 + lane, n0 + c * 32);
-                if (p.tma_store) {
-                    uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
-                    if (lane == 0) bulk_wait_group_read<1>();   // the store that used `buf` has read it
-                    __syncwarp();
-                    uint16_t* b16 = reinterpret_cast<uint16_t*>(buf);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) b16[j * 32 + lane] = round_out<BF16>(r[j]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmC, smem_u32(buf), m0, n0 + c * 32);
-                        bulk_commit_group();
-                    }
-                } else {
-                    const int m = m0 + lane;
-                    if (m < p.M) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int n = n0 + c * 32 + j;
-                            if (n < p.N) Cg[static_cast<long long>(m) + static_cast<long long>(n) * p.ldc] =
-                                round_out<BF16>(r[j]);
-                        }
-                    }
-                }
-            }
-        }
-        if (lane == 0) bulk_wait_group<0>();
-        __syncwarp();
-    }
-
-    tc_fence_before_sync();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after_sync();
-        tmem_dealloc(tmem_base, Cf::kTmemCols);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// CTA-pair variant (tcgen05 .cta_group::2).  A cluster of two CTAs on two SMs
-// computes a 256 x 256 tile: CTA r of the pair stages rows [128r, 128r+128) of
-// the tile's A slice and rows [128r, 128r+128) of its B slice (the n range), so
-// each SM loads and stores 32 KB per 64-deep k step instead of 48 KB, and the
-// ring holds 6 stages instead of 4.  One thread of the even CTA issues the
-// 256 x 256 x 16 MMAs, which read both CTAs' halves and leave each CTA's 128
-// accumulator rows in its own TMEM.
-//   * both CTAs' TMA loads signal the even CTA's "full" barrier, which the even
-//     CTA's producer arms with the bytes of both halves;
-//   * the MMA's commits arrive on the "empty" and "accumulator full" barriers of
-//     both CTAs (multicast);
-//   * each CTA's epilogue warps hand the accumulator back by arriving on the even
-//     CTA's "accumulator empty" barrier (8 arrivals).
-// ---------------------------------------------------------------------------
-struct PairCfg {
-    static constexpr int kStages = 6;
-    static constexpr int kABytes = kBM * kBK * 2;          // this CTA's 128 rows of A
-    static constexpr int kBBytes = kBM * kBK * 2;          // this CTA's 128 rows of B
-    static constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB; the pair moves 64 KB per stage
-    static constexpr int kEpiBufBytes = kEpiBox * kEpiBox * 2;
-    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
-    static constexpr int kTile = 256;                      // pair tile is 256 x 256
-    static constexpr int kTmemCols = 2 * kTile;
-    static constexpr int kNumBars = 2 * kStages + 5;
-    static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
-    static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area too small");
-    static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-};
-
-template <bool A_MN, bool B_MN, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmC, const Params p)
-{
-    using Cf = PairCfg;
-    constexpr int S = Cf::kStages;
-    constexpr int T = Cf::kTile;
-    constexpr uint32_t kIdesc = idesc_f16(BF16, A_MN, B_MN, 2 * kBM, T);
-
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t* sA = smem;
-    uint8_t* sB = sA + S * Cf::kABytes;
-    uint8_t* sEpi = sB + S * Cf::kBBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + Cf::kEpiBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cf::kNumBars);
-    volatile uint32_t* abort_flag = tmem_slot + 1;
-
-    const uint32_t full0 = smem_u32(bars);
-    const uint32_t empty0 = full0 + 8 * S;
-    const uint32_t tfull0 = empty0 + 8 * S;
-    const uint32_t tempty0 = tfull0 + 16;
-    const uint32_t drain_bar = tempty0 + 16;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
-    const int pair = blockIdx.x >> 1;
-    const int num_pairs = gridDim.x >> 1;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull0 + 8 * a, 1);
-            mbar_init(tempty0 + 8 * a, 2 * kEpiWarps);
-        }
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0u;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-        if (p.tma_store) prefetch_tmap(&tmC);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(smem_u32(tmem_slot), Cf::kTmemCols);
-        tmem_relinquish_alloc_permit_pair();
-    }
-    // Both CTAs' barriers are initialised and the TMEM columns allocated before
-    // any CTA signals its peer.
-    tc_fence_before_sync();
-    cluster_sync();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_slot;
-    const uint32_t leader_full0 = mapa_shared(full0, 0);
-    const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
-    const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
-    uint32_t never = 0u;
-    const WaitCtl wc_drain{&never, p.status, p.wait_limit_ns};
-
-    if (warp == 0) {
-        // ------------------------------------------------------------------
-        // TMA producer (both CTAs): this CTA's halves of A and B
-        // ------------------------------------------------------------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            long long issued = 0;
-            bool ok = true;
-            for (int tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
-                int pm, pn;
-                tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
-                const int m0 = pm * T + static_cast<int>(rank) * kBM;
-                const int n0 = pn * T + static_cast<int>(rank) * kBM;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * Cf::kStageBytes);
-                    const uint32_t fb = leader_full0 + 8 * stage;
-                    const uint32_t a_dst = smem_u32(sA + stage * Cf::kABytes);
-                    const uint32_t b_dst = smem_u32(sB + stage * Cf::kBBytes);
-                    const int k0 = kb * kBK;
-                    if constexpr (A_MN) {
-                        tma_load_2d_pair(a_dst, &tmA, fb, m0, k0);
-                        tma_load_2d_pair(a_dst + Cf::kABytes / 2, &tmA, fb, m0 + 64, k0);
-                    } else {
-                        tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
-                    }
-                    if constexpr (B_MN) {
-                        tma_load_2d_pair(b_dst, &tmB, fb, n0, k0);            // 64(n) x 64(k)
-                        tma_load_2d_pair(b_dst + 8192, &tmB, fb, n0 + 64, k0);
-                    } else {
-                        tma_load_2d_pair(b_dst, &tmB, fb, k0, n0);
-                    }
-                    ++issued;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok && leader) {
-                // Abort: the even CTA's full barriers count both CTAs' bytes; wait
-                // (bounded) until the loads already armed have landed.
-                const long long pending = issued < S ? issued : S;
-                for (long long j = 1; j <= pending; ++j) {
-                    const int s = (stage - static_cast<int>(j) + S) % S;
-                    const uint32_t ph = (stage - static_cast<int>(j) < 0) ? (phase ^ 1u) : phase;
-                    mbar_wait(full0 + 8 * s, ph, wc_drain, kSiteProducerDrain);
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------
-        // MMA issuer: one thread of the even CTA
-        // ------------------------------------------------------------------
-        if (lane == 0 && leader) {
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            bool issued_any = false;
-            int it = 0;
-            for (int tile = pair; tile < p.num_tiles; tile += num_pairs, ++it) {
-                const int acc = it & 1;
-                const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
-                if (!mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * T);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t a_base = smem_u32(sA + stage * Cf::kABytes);
-                    const uint32_t b_base = smem_u32(sB + stage * Cf::kBBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, Cf::kABytes / 2, 1024)
-                                                 : smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
-                                                 : smem_desc_sw128(b_base + kk * 32, 16, 1024);
-                        mma_f16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
-                    mma_commit_pair_multicast(empty0 + 8 * stage, 0x3);
-                    issued_any = true;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                mma_commit_pair_multicast(tfull0 + 8 * acc, 0x3);
-            }
-            if (!ok && issued_any) {
-                mma_commit_pair_multicast(drain_bar, 0x1);
-                mbar_wait(drain_bar, 0u, wc_drain, kSiteMmaDrain);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------------
-        // Epilogue (both CTAs): this CTA's 128 rows of the 256 x 256 tile
-        // ------------------------------------------------------------------
-        const int quarter = warp & 3;
-        const int ew = warp - 2;
-        uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
-        uint16_t* Cg = reinterpret_cast<uint16_t*>(p.C);
-        int it = 0;
-        for (int tile = pair; tile < p.num_tiles; tile += num_pairs, ++it) {
-            const int acc = it & 1;
-            const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
-            bool ok = mbar_wait(tfull0 + 8 * acc, aph, wc, kSiteEpilogueTmemFull);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after_sync();
-            int pm, pn;
-            tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
-            const int m0 = pm * T + static_cast<int>(rank) * kBM + quarter * 32;
-            const int n0 = pn * T;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(acc * T);
-#pragma unroll 1
-            for (int c = 0; c < T / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c * 32, r);
-                tmem_ld_wait();
-                if (c == T / 32 - 1) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(leader_tempty0 + 8 * acc);
-                }
-                if (p.bias_mode != 0) add_bias<BF16>(r, p, m0 + lane, n0 + c * 32);
-                if (p.tma_store) {
-                    uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
-                    if (lane == 0) bulk_wait_group_read<1>();
-                    __syncwarp();
-                    uint16_t* b16 = reinterpret_cast<uint16_t*>(buf);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) b16[j * 32 + lane] = round_out<BF16>(r[j]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmC, smem_u32(buf), m0, n0 + c * 32);
-                        bulk_commit_group();
-                    }
-                } else {
-                    const int m = m0 + lane;
-                    if (m < p.M) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int n = n0 + c * 32 + j;
-                            if (n < p.N) Cg[static_cast<long long>(m) + static_cast<long long>(n) * p.ldc] =
-                                round_out<BF16>(r[j]);
-                        }
-                    }
-                }
-            }
-        }
-        if (lane == 0) bulk_wait_group<0>();
-        __syncwarp();
-    }
-
-    // Neither CTA may leave while its peer can still read its shared memory or
-    // arrive on its barriers.
-    tc_fence_before_sync();
-    cluster_sync();
-    if (warp == 1) {
-        tc_fence_after_sync();
-        tmem_dealloc_pair(tmem_base, Cf::kTmemCols);
-    }
-}
-
-bool encode_2d(CUtensorMap* map, bool bf16, const void* base, unsigned long long dim0, unsigned long long dim1,
-               unsigned long long stride1_bytes, unsigned box0, unsigned box1, CUtensorMapSwizzle swz, char* msg,
-               size_t msg_len)
-{
-    TmapEncodeFn enc = tmap_encoder();
-    if (enc == nullptr) {
-        snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
-        return false;
-    }
-    const cuuint64_t dims[2] = {dim0, dim1};
-    const cuuint64_t strides[1] = {stride1_bytes};
-    const cuuint32_t box[2] = {box0, box1};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (%d) for dims %llu x %llu, stride %llu B, box %u x %u",
-                 static_cast<int>(r), dim0, dim1, stride1_bytes, box0, box1);
-        return false;
-    }
-    return true;
-}
-
-template <int BN, bool A_MN, bool B_MN, bool BF16>
-int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
-{
-    using Cf = Cfg<BN>;
-    CUtensorMap tmA, tmB, tmC;
-    if (A_MN) {
-        if (!encode_2d(&tmA, BF16, g.A, g.M, g.K, g.lda * 2ull, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-            return 1;
-    } else {
-        if (!encode_2d(&tmA, BF16, g.A, g.K, g.M, g.lda * 2ull, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-            return 1;
-    }
-    if (B_MN) {
-        if (!encode_2d(&tmB, BF16, g.B, g.N, g.K, g.ldb * 2ull, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-            return 1;
-    } else {
-        if (!encode_2d(&tmB, BF16, g.B, g.K, g.N, g.ldb * 2ull, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-            return 1;
-    }
-    if (g.tma_store) {
-        if (!encode_2d(&tmC, BF16, g.C, g.M, g.N, g.ldc * 2ull, kEpiBox, kEpiBox, CU_TENSOR_MAP_SWIZZLE_NONE, msg,
-                       msg_len))
-            return 1;
-    } else {
-        tmC = tmA;   // unused by the kernel
-    }
-
-    Params p;
-    p.M = g.M;
-    p.N = g.N;
-    p.K = g.K;
-    p.num_m = (g.M + kBM - 1) / kBM;
-    p.num_n = (g.N + BN - 1) / BN;
-    p.num_tiles = p.num_m * p.num_n;
-    p.num_kb = (g.K + kBK - 1) / kBK;
-    p.group_m = g.group_m < 1 ? 1 : g.group_m;
-    p.C = g.C;
-    p.ldc = g.ldc;
-    p.tma_store = g.tma_store ? 1 : 0;
-    p.bias = g.bias;
-    p.bias_mode = g.bias != nullptr ? g.bias_mode : 0;
-    p.status = g.status;
-    p.wait_limit_ns = g.wait_limit_ns;
-
-    auto kern = gemm_tcgen05_kernel<BN, A_MN, B_MN, BF16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
-    if (e != cudaSuccess) {
-        snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        return 1;
-    }
-    // Every CTA gets the same number of tiles (the last wave is not left partial).
-    const int per_cta = (p.num_tiles + g.num_sms - 1) / g.num_sms;
-    const int grid = (p.num_tiles + per_cta - 1) / per_cta;
-    kern<<<grid, kThreads, Cf::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        snprintf(msg, msg_len, "GEMM launch failed: %s", cudaGetErrorString(e));
-        return 1;
-    }
-    return 0;
-}
-
-template <bool A_MN, bool B_MN, bool BF16>
-int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
-{
-    using Cf = PairCfg;
-    CUtensorMap tmA, tmB, tmC;
-    if (A_MN) {
-        if (!encode_2d(&tmA, BF16, g.A, g.M, g.K, g.lda * 2ull, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-            return 1;
-    } else {
-        if (!encode_2d(&tmA, BF16, g.A, g.K, g.M, g.lda * 2ull, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-            return 1;
-    }
-    if (B_MN) {
-        if (!encode_2d(&tmB, BF16, g.B, g.N, g.K, g.ldb * 2ull, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-            return 1;
-    } else {
-        if (!encode_2d(&tmB, BF16, g.B, g.K, g.N, g.ldb * 2ull, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
-            return 1;
-    }
-    if (g.tma_store) {
-        if (!encode_2d(&tmC, BF16, g.C, g.M, g.N, g.ldc * 2ull, kEpiBox, kEpiBox, CU_TENSOR_MAP_SWIZZLE_NONE, msg,
-                       msg_len))
-            return 1;
-    } else {
-        tmC = tmA;
-    }
-    Params p;
-    p.M = g.M;
-    p.N = g.N;
-    p.K = g.K;
-    p.num_m = (g.M + Cf::kTile - 1) / Cf::kTile;
-    p.num_n = (g.N + Cf::kTile - 1) / Cf::kTile;
-    p.num_tiles = p.num_m * p.num_n;
-    p.num_kb = (g.K + kBK - 1) / kBK;
-    p.group_m = g.group_m < 1 ? 1 : g.group_m;
-    p.C = g.C;
-    p.ldc = g.ldc;
-    p.tma_store = g.tma_store ? 1 : 0;
-    p.bias = g.bias;
-    p.bias_mode = g.bias != nullptr ? g.bias_mode : 0;
-    p.status = g.status;
-    p.wait_limit_ns = g.wait_limit_ns;
-
-    auto kern = gemm_tcgen05_pair_kernel<A_MN, B_MN, BF16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
-    if (e != cudaSuccess) {
-        snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        return 1;
-    }
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cf::kSmemBytes;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
-        cudaGetLastError();
-        clusters = g.num_sms / 2;
-    }
-    if (clusters > g.num_sms / 2) clusters = g.num_sms / 2;
-    if (clusters < 1) clusters = 1;
-    const int per_pair = (p.num_tiles + clusters - 1) / clusters;
-    const int pairs = (p.num_tiles + per_pair - 1) / per_pair;
-    cfg.gridDim = dim3(2 * pairs, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        snprintf(msg, msg_len, "GEMM (CTA pair) launch failed: %s", cudaGetErrorString(e));
-        return 1;
-    }
-    return 0;
-}
-
-}  // namespace
-
 namespace {
 
 // B MN-major (a transposed B) is instantiated for FP16 only.
 template <int BN>
 int dispatch_single(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
+    const bool bf16 = g.in_type == kInBF16;
     if (g.b_mn_major) {
         if constexpr (BN >= 64) {
-            if (g.bf16) {
+            if (bf16) {
                 snprintf(msg, msg_len, "a transposed B operand is supported for FP16 only");
                 return 1;
             }
-            return g.a_mn_major ? launch_instance<BN, true, true, false>(g, stream, msg, msg_len)
-                                : launch_instance<BN, false, true, false>(g, stream, msg, msg_len);
+            return g.a_mn_major ? launch_instance<BN, true, true, kInF16, kOutF16>(g, stream, msg, msg_len)
+                                : launch_instance<BN, false, true, kInF16, kOutF16>(g, stream, msg, msg_len);
         } else {
             snprintf(msg, msg_len, "a transposed B operand needs block_n >= 64");
             return 1;
         }
     }
     if (g.a_mn_major)
-        return g.bf16 ? launch_instance<BN, true, false, true>(g, stream, msg, msg_len)
-                      : launch_instance<BN, true, false, false>(g, stream, msg, msg_len);
-    return g.bf16 ? launch_instance<BN, false, false, true>(g, stream, msg, msg_len)
-                  : launch_instance<BN, false, false, false>(g, stream, msg, msg_len);
+        return bf16 ? launch_instance<BN, true, false, kInBF16, kOutBF16>(g, stream, msg, msg_len)
+                    : launch_instance<BN, true, false, kInF16, kOutF16>(g, stream, msg, msg_len);
+    return bf16 ? launch_instance<BN, false, false, kInBF16, kOutBF16>(g, stream, msg, msg_len)
+                : launch_instance<BN, false, false, kInF16, kOutF16>(g, stream, msg, msg_len);
 }
 
 int dispatch_pair(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
+    const bool bf16 = g.in_type == kInBF16;
     if (g.b_mn_major) {
-        if (g.bf16) {
+        if (bf16) {
             snprintf(msg, msg_len, "a transposed B operand is supported for FP16 only");
             return 1;
         }
-        return g.a_mn_major ? launch_pair_instance<true, true, false>(g, stream, msg, msg_len)
-                            : launch_pair_instance<false, true, false>(g, stream, msg, msg_len);
+        return g.a_mn_major ? launch_pair_instance<true, true, kInF16, kOutF16>(g, stream, msg, msg_len)
+                            : launch_pair_instance<false, true, kInF16, kOutF16>(g, stream, msg, msg_len);
     }
     if (g.a_mn_major)
-        return g.bf16 ? launch_pair_instance<true, false, true>(g, stream, msg, msg_len)
-                      : launch_pair_instance<true, false, false>(g, stream, msg, msg_len);
-    return g.bf16 ? launch_pair_instance<false, false, true>(g, stream, msg, msg_len)
-                  : launch_pair_instance<false, false, false>(g, stream, msg, msg_len);
+        return bf16 ? launch_pair_instance<true, false, kInBF16, kOutBF16>(g, stream, msg, msg_len)
+                    : launch_pair_instance<true, false, kInF16, kOutF16>(g, stream, msg, msg_len);
+    return bf16 ? launch_pair_instance<false, false, kInBF16, kOutBF16>(g, stream, msg, msg_len)
+                : launch_pair_instance<false, false, kInF16, kOutF16>(g, stream, msg, msg_len);
 }
 
 }  // namespace
 
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
+    if (g.in_type == kInE4M3 || g.in_type == kInE5M2) return launch_gemm_fp8(g, stream, msg, msg_len);
+    if (g.in_type != kInF16 && g.in_type != kInBF16) {
+        snprintf(msg, msg_len, "unknown input type %d", g.in_type);
+        return 1;
+    }
+    if (g.out_type != g.in_type) {
+        snprintf(msg, msg_len, "16-bit GEMMs produce their input type");
+        return 1;
+    }
     switch (g.block_n) {
     case 256: return g.pair ? dispatch_pair(g, stream, msg, msg_len) : dispatch_single<256>(g, stream, msg, msg_len);
     case 128: return dispatch_single<128>(g, stream, msg, msg_len);

@@ -191,7 +191,8 @@ extern "C" int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, u
     g.M = M;
     g.N = N;
     g.K = K;
-    g.bf16 = false;
+    g.in_type = bsk::kInF16;
+    g.out_type = bsk::kOutF16;
     // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
     // tile, deep ring: the weight stream sets the pace), else 256 on CTA pairs.
     const long long bn_opt = option_or(BSK_OPT_BLOCK_N, 0);

@@ -271,6 +271,20 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A * B with FP8 (E4M3 / E5M2) operands and an FP32 accumulator,
+// 128 x N x 32 (kind::f8f6f4).  Same operand descriptors as kind::f16: 32 bytes
+// of every 128-byte K-major row per instruction.
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // One thread: arrive once on mbarrier `bar` when all tcgen05 operations this
 // thread issued so far have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
@@ -331,6 +345,18 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// The CTA-pair form of mma_f8f6f4 (256 x N x 32 over the two CTAs' halves).
+__device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier at shared offset `bar` of every CTA in `cta_mask`
 // when the pair MMAs issued so far by this thread have completed.
 __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t cta_mask)
@@ -372,6 +398,15 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool a_mn_major, boo
 {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
            ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma .kind::f8f6f4 with an FP32 accumulator
+// and K-major operands: the same fields as above, with the A / B type codes of
+// that kind (0 = E4M3, 1 = E5M2).
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t a_code, uint32_t b_code, int m, int n)
+{
+    return (1u << 4) | ((a_code & 7u) << 7) | ((b_code & 7u) << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 

@@ -5,6 +5,7 @@
  *   gemm_f16_colmajor  large column-major FP16 GEMM on the tcgen05 tensor cores;
  *   gemm_f16           the same GEMM with transposed operands, row-major storage,
  *                      any leading dimensions and an optional fused bias;
+ *   gemm_fp8           FP8 (E4M3 / E5M2) GEMM with FP32 accumulation;
  *   gemv_bf16          BF16 linear layer y = x W^T: the HBM-bound decode GEMV for
  *                      n <= 8 tokens (CUDA cores), the tensor-core GEMM for
  *                      larger n (prefill projections);
@@ -106,6 +107,40 @@ typedef enum bsk_bias_mode {
 int gemm_f16(int order, int transa, int transb, const uint16_t* A, int lda, const uint16_t* B, int ldb,
              uint16_t* C, int ldc, int M, int N, int K, const uint16_t* bias, int bias_mode, void* stream);
 
+/* FP8 formats of gemm_fp8 (OCP 8-bit floating point). */
+typedef enum bsk_fp8_format {
+    BSK_FP8_E4M3 = 0, /* 1 sign, 4 exponent (bias 7), 3 fraction bits; max 448; no infinity */
+    BSK_FP8_E5M2 = 1  /* 1 sign, 5 exponent (bias 15), 2 fraction bits; max 57344; IEEE-style inf/NaN */
+} bsk_fp8_format;
+
+/* Output type of gemm_fp8. */
+typedef enum bsk_out_type {
+    BSK_OUT_F32 = 0,  /* IEEE binary32 */
+    BSK_OUT_BF16 = 1  /* bfloat16, rounded to nearest even */
+} bsk_out_type;
+
+/*
+ * FP8 GEMM with FP32 accumulation: C(m,n) = out( alpha * sum_k A(m,k) B(k,n) ).
+ * The FP8 row of the matrix-instruction table in "Hygon 优化" (FlagGems
+ * documentation), section DUMMA 矩阵指令形状: E4M3 or E5M2 inputs, FP32
+ * accumulator; the product is the GEMM of "MTT S4000 GEMM 优化中的分块、尾处理与
+ * 并发实战复盘", section 2.  A and B hold the same `format` (bsk_fp8_format),
+ * both K-major (the layout the FP8 tensor-core instruction reads):
+ *     A(m,k) = A[k + m*lda]   (M x K, each row's K codes contiguous, lda >= K)
+ *     B(k,n) = B[k + n*ldb]   (K x N, each column's K codes contiguous, ldb >= K)
+ *     C(m,n) = C[m + n*ldc]   (M x N column-major, ldc >= M; elements of `out_type`)
+ * (a row-major linear layer Y[T,F] = X[T,K] W[F,K]^T is A = W, B = X, M = F,
+ * N = T, and C = Y row-major with ldc = F).  `alpha` (finite) scales the FP32
+ * accumulator before the output conversion (a product of per-tensor scales;
+ * 1.0 gives the plain product).  BSK_OUT_F32 stores the scaled accumulator;
+ * BSK_OUT_BF16 rounds it once to nearest even.  K == 0 writes +0.0.
+ * Operands that are not 16-byte aligned or whose leading dimension is not a
+ * multiple of 16 are packed into a stream-ordered workspace first.  C must
+ * not overlap A or B.  Blocking; bsk_gemm_fp8_enqueue only launches.
+ */
+int gemm_fp8(int format, const uint8_t* A, int lda, const uint8_t* B, int ldb, void* C, int ldc, int out_type,
+             int M, int N, int K, float alpha, void* stream);
+
 /*
  * y = x W^T in BF16 with FP32 accumulation, output rounded to nearest even.
  * Definition: DCU decode-GEMV article (forum.sourcefind.cn), section 6.1:
@@ -187,6 +222,8 @@ int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, uint16_t* C,
 int bsk_gemm_f16_enqueue(int order, int transa, int transb, const uint16_t* A, int lda, const uint16_t* B,
                          int ldb, uint16_t* C, int ldc, int M, int N, int K, const uint16_t* bias, int bias_mode,
                          void* stream);
+int bsk_gemm_fp8_enqueue(int format, const uint8_t* A, int lda, const uint8_t* B, int ldb, void* C, int ldc,
+                         int out_type, int M, int N, int K, float alpha, void* stream);
 int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
                                   void* stream);
 int bsk_gemv_bf16_enqueue(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);

@@ -136,6 +136,32 @@ def test_general_gemm_rejects_bad_arguments(lib, args):
     assert bsk.last_error()
 
 
+@pytest.mark.parametrize("args", [
+    # format, A, lda, B, ldb, C, ldc, out_type, M, N, K, alpha
+    (2, G_A, 64, G_B, 64, G_C, 64, 0, 64, 64, 64, 1.0),            # bad format
+    (0, G_A, 64, G_B, 64, G_C, 64, 2, 64, 64, 64, 1.0),            # bad output type
+    (1, G_A, 64, G_B, 64, G_C, 64, 1, 64, 64, 64, float("nan")),   # alpha not finite
+    (0, G_A, 64, G_B, 64, G_C, 64, 0, 64, 64, 64, float("inf")),
+    (0, G_A, 63, G_B, 64, G_C, 64, 0, 64, 64, 64, 1.0),            # lda < K
+    (0, G_A, 64, G_B, 63, G_C, 64, 0, 64, 64, 64, 1.0),            # ldb < K
+    (0, G_A, 64, G_B, 64, G_C, 63, 0, 64, 64, 64, 1.0),            # ldc < M
+    (0, G_A, 64, G_B, 64, G_C, 64, 0, -1, 64, 64, 1.0),            # negative size
+    (0, G_A, 64, G_B, 64, None, 64, 0, 64, 64, 64, 1.0),           # C NULL
+    (0, None, 64, G_B, 64, G_C, 64, 0, 64, 64, 64, 1.0),           # A NULL
+    (0, G_A, 64, G_B, 64, G_A + 4000, 64, 0, 64, 64, 64, 1.0),     # C overlaps A (bytes 0..4095)
+    (0, G_A, 64, G_B, 64, G_B - 16 * 1024 + 4, 64, 0, 64, 64, 64, 1.0),  # FP32 C (16 KB) reaches into B
+])
+def test_fp8_gemm_rejects_bad_arguments(lib, args):
+    assert lib.gemm_fp8(*args, None) == 1
+    assert lib.bsk_gemm_fp8_enqueue(*args, None) == 1
+    assert bsk.last_error()
+
+
+def test_fp8_gemm_empty_output_is_a_no_op(lib):
+    assert lib.gemm_fp8(0, None, 8, None, 8, None, 1, 0, 0, 5, 8, 1.0, None) == 0
+    assert lib.gemm_fp8(1, None, 8, None, 8, None, 4, 1, 4, 0, 8, 1.0, None) == 0
+
+
 def test_general_gemm_accepts_exact_leading_dimensions(lib):
     """Overlap is decided on the spans the strides reach: a C right after A's
     last element is not an overlap; on a machine without a GPU the call then
