@@ -20,8 +20,9 @@ Reported (one JSON line, rank 0):
              peak (FP16 and BF16 dense rates are equal on this part), plus
              roofline_gemv against the measured HBM copy bandwidth.
   other_configs  device time of the remaining workloads (256^3 and 4095x4097x4100
-             FP16 GEMMs, the 4096-token BF16 prefill projection, and gemm_f16 in
-             other storage forms with a fused bias), measured after the step.
+             FP16 GEMMs, the 4096-token BF16 prefill projection, gemm_f16 in
+             other storage forms with a fused bias, and the FP8 GEMM), measured
+             after the step.
   decode_attention  split-KV decode attention at 8K/16K/32K tokens (KV-cache GB/s).
   cpu_baseline  the oracle timed on a bounded sample on the host cores.
 
@@ -139,7 +140,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "gemm": ("gemm_tcgen05.cu", "ptx.cuh", "bsk_internal.h"),
+    "gemm": ("gemm_tcgen05.cuh", "gemm_tcgen05.cu", "ptx.cuh", "bsk_internal.h"),
+    "fp8": ("gemm_tcgen05.cuh", "gemm_fp8.cu", "ptx.cuh", "bsk_internal.h"),
     "gemv": ("gemv.cu", "bsk_internal.h"),
 }
 
@@ -311,6 +313,21 @@ def other_configs(W_prefill, dev, peaks):
                      "layout": {"order": "row" if order else "column", "transa": ta, "transb": tb,
                                 "bias": "per column"}}
         del Ad, Bd, C, bias
+    # FP8 (E4M3) GEMMs with FP32 accumulation and BF16 output: the square
+    # shape, and FP8 weights over the prefill projection (A = W, B = X).
+    fp8_peak = 2.0 * peak_t   # FP8 dense rate = 2x the measured BF16 rate (nominal ratio)
+    for name, (M, N, K) in (("gemm_fp8_e4m3_8192x8192x8192", (8192, 8192, 8192)),
+                            ("linear_fp8_e4m3_34816x4096x5120", (GEMV_M, S_PREFILL, GEMV_K))):
+        A, B = inputs.fp8_operands(M, N, K, "normal1", "e4m3")
+        Ad = torch.from_numpy(A).to(dev)
+        Bd = torch.from_numpy(B).to(dev)
+        C = torch.empty(M * N, dtype=torch.int16, device=dev)
+        ms = time_launches(lambda: bsk.gemm_fp8_enqueue(bsk.FP8_E4M3, Ad, K, Bd, K, C, M, bsk.OUT_BF16, M, N, K,
+                                                        1.0), 20)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out[name] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 4),
+                     "fp8_peak": round(fp8_peak, 1), "out": "bf16"}
+        del Ad, Bd, C
     S = S_PREFILL
     _, X = inputs.linear_operands(1, GEMV_K, S, "normal0.02", "normal1")
     Xd = to_dev(X)
@@ -605,6 +622,14 @@ def run_case(args):
                                                 bias, mode)
         else:
             call = lambda: bsk.gemm_f16_colmajor_enqueue(Ad, Bd, C, a, b, c)  # noqa: E731
+        work, unit = 2.0 * a * b * c, "TFLOP/s"
+    elif kind == "fp8":
+        # fp8:MxNxK -> E4M3 A (K-major), B (K-major), BF16 C
+        A, B = inputs.fp8_operands(a, b, c, "normal1", "e4m3")
+        Ad, Bd = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+        C = torch.empty(a * b, dtype=torch.int16, device=dev)
+        call = lambda: bsk.gemm_fp8_enqueue(bsk.FP8_E4M3, Ad, c, Bd, c, C, a, bsk.OUT_BF16,  # noqa: E731
+                                            a, b, c, 1.0)
         work, unit = 2.0 * a * b * c, "TFLOP/s"
     elif kind == "gemv":
         W, x = inputs.linear_operands(a, b, c, "normal0.02", "normal1")
