@@ -362,15 +362,27 @@ def attention_configs(dev, hbm_peak):
         sl = torch.tensor([L], dtype=torch.int32, device=dev)
         o = torch.empty(nqh * hd, dtype=torch.int16, device=dev)
         kv_bytes = L * nkv * hd * 2 * 2
+        # Enough copies of the cache that successive calls never find it in L2
+        # (together at least twice the 129 MB L2).
+        copies = max(2, -(-260_000_000 // kv_bytes))
+        kvs = [(k, v)] + [(k.clone(), v.clone()) for _ in range(copies - 1)]
         row = {}
         for name, segs in (("auto", 0), ("page_rule", 32 if L >= 12288 else 16)):
-            ms = time_launches(lambda: bsk.decode_attention_bf16_enqueue(
-                q, k, v, bt, sl, o, 1, nqh, nkv, hd, bs, nb, nb, L, 1.0 / 16.0, segs), 20)
+            it = [0]
+
+            def call():
+                kc, vc = kvs[it[0] % copies]
+                it[0] += 1
+                bsk.decode_attention_bf16_enqueue(q, kc, vc, bt, sl, o, 1, nqh, nkv, hd, bs, nb, nb, L, 1.0 / 16.0,
+                                                  segs)
+
+            ms = time_launches(call, 20)
             gbs = kv_bytes / (ms * 1e-3) / 1e9
             row[name] = {"segments": segs, "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
                          "frac_of_hbm": round(gbs / hbm_peak, 4)}
+        row["kv_copies"] = copies
         out[f"L{L}"] = row
-        del k, v
+        del k, v, kvs
     bsk.stream_check()
     return out
 

@@ -15,11 +15,13 @@
 // Kernel 1 (one CTA per segment x KV head x sequence): the CTA owns the G query
 // heads that read its KV head.  Each lane holds head_dim/32 consecutive
 // elements of every q, k and v row; warps take tokens in turn, T at a time,
-// compute the G dot products with warp shuffles and keep an online softmax
-// state (running max m, sum l, unnormalised output o) per head in base-2
-// (scores pre-multiplied by scale * log2 e).  The warps' states are combined in
-// shared memory and the segment's (m, l, o) go to a workspace.
-// Kernel 2 (one CTA per query head x sequence) merges the segments:
+// streamed through a per-warp cp.async ring in shared memory, compute the G
+// dot products with warp shuffles and keep an online softmax state (running
+// max m, sum l, unnormalised output o) per head in base-2 (scores
+// pre-multiplied by scale * log2 e).  The warps' states are combined in shared
+// memory and the segment's (m, l, o) go to a workspace.
+// Kernel 2 (one CTA per query head x sequence x 32 output elements) merges the
+// segments:
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  out = sum_s o_s 2^(m_s - M) / L.
 // A block-table entry out of range is recorded in the status word and its
 // tokens are skipped (no out-of-range read).
@@ -34,7 +36,8 @@ namespace bsk {
 namespace {
 
 constexpr int kAttnWarps = 8;
-constexpr int kAttnTokens = 4;   // tokens per warp per iteration (loads in flight)
+constexpr int kAttnTokens = 4;   // tokens per warp per ring stage
+constexpr int kAttnStages = 3;   // cp.async ring depth per warp
 
 template <int EPL>
 struct RowVec;   // EPL bf16 values per lane
@@ -51,33 +54,68 @@ struct RowVec<2> {
     using T = uint32_t;
 };
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-template <int EPL>
-__device__ __forceinline__ void widen(const typename RowVec<EPL>::T& v, float (&f)[EPL])
+// bf16 pair in one 32-bit word -> the two FP32 values (element 0 = low half):
+// a bfloat16 is the upper half of a binary32 (byte permutations, integer pipe).
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w)
 {
-    if constexpr (EPL == 8) {
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-    } else if constexpr (EPL == 4) {
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    } else {
-        f[0] = bf16_lo(v); f[1] = bf16_hi(v);
-    }
+    uint32_t lo, hi;
+    asm("prmt.b32 %0, %1, 0, 0x1044;" : "=r"(lo) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0x3244;" : "=r"(hi) : "r"(w));
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
 }
 
-template <int EPL>
-__device__ __forceinline__ typename RowVec<EPL>::T zero_vec()
+// Packed two-lane FP32 FMA: {a.x*b.x + c.x, a.y*b.y + c.y}, each rounded once.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
 {
-    if constexpr (EPL == 8) {
-        return make_uint4(0u, 0u, 0u, 0u);
-    } else if constexpr (EPL == 4) {
-        return make_uint2(0u, 0u);
+    unsigned long long d;
+    const unsigned long long ua = *reinterpret_cast<unsigned long long*>(&a);
+    const unsigned long long ub = *reinterpret_cast<unsigned long long*>(&b);
+    const unsigned long long uc = *reinterpret_cast<unsigned long long*>(&c);
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(ua), "l"(ub), "l"(uc));
+    return *reinterpret_cast<float2*>(&d);
+}
+
+// 2^x for x <= 0 (a softmax weight): the hardware approximation, one
+// instruction; 2^-inf = +0.
+__device__ __forceinline__ float exp2_weight(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The EPL/2 bf16 pairs of one lane's row slice, widened.
+template <int EPL>
+__device__ __forceinline__ void widen2(const uint8_t* src, float2 (&f)[EPL / 2])
+{
+    const typename RowVec<EPL>::T v = *reinterpret_cast<const typename RowVec<EPL>::T*>(src);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+    for (int i = 0; i < EPL / 2; ++i) f[i] = bf16x2_to_f32x2(w[i]);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Asynchronous global -> shared copy of BYTES (4, 8 or 16); src_bytes = 0
+// copies nothing and zero-fills the destination.
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void* src, uint32_t src_bytes)
+{
+    if constexpr (BYTES == 16) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                     : "memory");
     } else {
-        return 0u;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(BYTES),
+                     "r"(src_bytes)
+                     : "memory");
     }
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 struct AttnParams {
     const uint16_t* q;
@@ -92,11 +130,33 @@ struct AttnParams {
     int* status;
 };
 
+// Shared memory of the split kernel: the warps' cp.async rings, reused after
+// the token loop for the warps' (unnormalised) outputs.
 template <int HD, int G>
-__global__ void __launch_bounds__(kAttnWarps * 32)
+struct SplitSmem {
+    static constexpr int kRow = HD * 2;                          // bytes of one K or V row
+    static constexpr int kStage = 2 * kAttnTokens * kRow;        // T K rows, then T V rows
+    static constexpr int kWarpRing = kAttnStages * kStage;
+    static constexpr int kRing = kAttnWarps * kWarpRing;
+    static constexpr int kOut = kAttnWarps * G * HD * 4;
+    static constexpr int kBytes = kRing > kOut ? kRing : kOut;
+};
+
+// Each warp streams its chunks (T tokens each; the warps take chunks in turn)
+// through a private D-stage ring in shared memory: the copies for chunk i+D-1
+// are issued before chunk i is consumed, so the bytes in flight do not depend
+// on where the warp is in its arithmetic.  Each lane copies, and later reads,
+// only its own slice (head_dim/32 values) of every row, so cp.async.wait_group
+// is the only synchronisation the ring needs.
+template <int HD, int G>
+__global__ void __launch_bounds__(kAttnWarps * 32, G >= 8 ? 1 : 2)
     attn_split_kernel(const AttnParams p)
 {
     constexpr int EPL = HD / 32;
+    constexpr int LB = EPL * 2;   // bytes per lane per row
+    constexpr int T = kAttnTokens;
+    constexpr int D = kAttnStages;
+    using SM = SplitSmem<HD, G>;
     using Vec = typename RowVec<EPL>::T;
     const int seg = blockIdx.x;
     const int kvh = blockIdx.y;
@@ -106,7 +166,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
 
     __shared__ float s_m[kAttnWarps][G];
     __shared__ float s_l[kAttnWarps][G];
-    extern __shared__ float s_o[];   // [kAttnWarps][G][HD]
+    extern __shared__ __align__(16) uint8_t smem[];
 
     int L = p.seq_lens[seq];
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
@@ -114,129 +174,213 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     const int t0 = seg * seg_len;
     const int t1 = (t0 + seg_len < L) ? t0 + seg_len : L;
 
-    // this lane's slice of the G query rows, pre-scaled into the base-2 domain
-    float qf[G][EPL];
+    // this lane's slice of the G query rows, pre-scaled into the base-2 domain,
+    // as FP32 pairs (the dot products and the output run on packed FMAs)
+    constexpr int P = EPL / 2;
+    float2 qf[G][P];
 #pragma unroll
     for (int j = 0; j < G; ++j) {
-        const Vec qv = *reinterpret_cast<const Vec*>(
-            p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + j) * HD + lane * EPL);
-        widen<EPL>(qv, qf[j]);
+        widen2<EPL>(reinterpret_cast<const uint8_t*>(
+                        p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + j) * HD + lane * EPL),
+                    qf[j]);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) qf[j][e] *= p.scale_log2;
+        for (int e = 0; e < P; ++e) {
+            qf[j][e].x *= p.scale_log2;
+            qf[j][e].y *= p.scale_log2;
+        }
     }
 
-    float m[G], l[G], o[G][EPL];
+    float m[G], l[G];
+    float2 o[G][P];
 #pragma unroll
     for (int j = 0; j < G; ++j) {
         m[j] = -INFINITY;
         l[j] = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[j][e] = 0.f;
+        for (int e = 0; e < P; ++e) o[j][e] = make_float2(0.f, 0.f);
     }
 
     const int32_t* bt = p.block_tables + static_cast<long long>(seq) * p.max_blocks;
-    constexpr int T = kAttnTokens;
-    constexpr int V = T * G;   // scores per iteration, index u * G + j
-    // Warps take T-token chunks of the segment in turn; within a chunk the
-    // block and in-block offset advance incrementally (one division per chunk).
-    for (int c0 = t0 + warp * T; c0 < t1; c0 += kAttnWarps * T) {
-        Vec kv[T], vv[T];
-        bool ok[T];
+    const long long tok_stride = static_cast<long long>(p.num_kv_heads) * HD;   // elements between tokens
+    const long long head_off = static_cast<long long>(kvh) * HD + lane * EPL;
+    uint8_t* wring = smem + warp * SM::kWarpRing;                 // this warp's ring
+    const uint32_t ring = smem_addr(wring) + lane * LB;            // this lane's slice of it
+    constexpr int kChunkStep = kAttnWarps * T;
+    const int first = t0 + warp * T;
+    const int nch = first < t1 ? (t1 - first + kChunkStep - 1) / kChunkStep : 0;
+
+    // Copies chunk i of this warp into ring stage `st`; returns the mask of its
+    // tokens that exist (inside the segment, with a valid block).
+    auto issue = [&](int i, int st) -> uint32_t {
+        const int c0 = first + i * kChunkStep;
         int bi = c0 / p.block_size;
         int off = c0 - bi * p.block_size;
+        const uint32_t dst0 = ring + st * SM::kStage;
+        if (c0 + T <= t1 && off + T <= p.block_size) {
+            // the usual case: the whole chunk inside one page and the segment
+            const int blk = bt[bi];
+            if (blk >= 0 && blk < p.num_blocks) {
+                const long long row = (static_cast<long long>(blk) * p.block_size + off) * tok_stride + head_off;
+                const uint16_t* ks = p.k + row;
+                const uint16_t* vs = p.v + row;
+#pragma unroll
+                for (int u = 0; u < T; ++u) {
+                    cp_async<LB>(dst0 + u * SM::kRow, ks + u * tok_stride, LB);
+                    cp_async<LB>(dst0 + (T + u) * SM::kRow, vs + u * tok_stride, LB);
+                }
+                cp_async_commit();
+                return (1u << T) - 1u;
+            }
+        }
+        uint32_t bits = 0;
 #pragma unroll
         for (int u = 0; u < T; ++u) {
             const int t = c0 + u;
-            ok[u] = t < t1;
-            kv[u] = zero_vec<EPL>();
-            vv[u] = zero_vec<EPL>();
-            if (ok[u]) {
+            bool ok = t < t1;
+            const uint16_t* ks = p.k;
+            const uint16_t* vs = p.v;
+            if (ok) {
                 const int blk = bt[bi];
                 if (blk < 0 || blk >= p.num_blocks) {
                     if (lane == 0) *reinterpret_cast<volatile int*>(p.status) = kDevErrBadIndex;
-                    ok[u] = false;
+                    ok = false;
                 } else {
-                    const long long row =
-                        ((static_cast<long long>(blk) * p.block_size + off) * p.num_kv_heads + kvh) * HD + lane * EPL;
-                    kv[u] = *reinterpret_cast<const Vec*>(p.k + row);
-                    vv[u] = *reinterpret_cast<const Vec*>(p.v + row);
+                    const long long row = (static_cast<long long>(blk) * p.block_size + off) * tok_stride + head_off;
+                    ks = p.k + row;
+                    vs = p.v + row;
                 }
             }
+            const uint32_t dst = dst0 + u * SM::kRow;
+            cp_async<LB>(dst, ks, ok ? LB : 0u);
+            cp_async<LB>(dst + T * SM::kRow, vs, ok ? LB : 0u);
+            bits |= (ok ? 1u : 0u) << u;
             if (++off == p.block_size) {
                 off = 0;
                 ++bi;
             }
         }
-        // partial dot products, then a butterfly that leaves each lane pair one
-        // full score, then a broadcast of all V scores to every lane
+        cp_async_commit();
+        return bits;
+    };
+
+    constexpr uint32_t kMask = (1u << T) - 1u;
+    uint32_t vbits = 0;   // validity of the tokens held by each stage: bits [st*T, st*T+T)
+#pragma unroll
+    for (int i = 0; i < D - 1; ++i) {
+        uint32_t b = 0;
+        if (i < nch) {
+            b = issue(i, i);
+        } else {
+            cp_async_commit();
+        }
+        vbits |= b << (i * T);
+    }
+
+    constexpr int V = T * G;   // scores per chunk, index u * G + j
+    for (int i = 0; i < nch; ++i) {
+        const int st = i % D;
+        const int in = i + D - 1;
+        const int sn = in % D;
+        uint32_t b = 0;
+        if (in < nch) {
+            b = issue(in, sn);
+        } else {
+            cp_async_commit();
+        }
+        vbits = (vbits & ~(kMask << (sn * T))) | (b << (sn * T));
+        cp_async_wait<D - 1>();   // chunk i has landed (this lane's slices)
+        const uint32_t okb = (vbits >> (st * T)) & kMask;
+        const uint8_t* stage = wring + st * SM::kStage + lane * LB;
+
+        // partial dot products, then a butterfly that leaves each lane pair (or
+        // group) one full score
         float sc[V];
 #pragma unroll
         for (int u = 0; u < T; ++u) {
-            float kf[EPL];
-            widen<EPL>(kv[u], kf);
+            float2 kf[P];
+            widen2<EPL>(stage + u * SM::kRow, kf);
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                float d = 0.f;
+                float2 d = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) d = fmaf(qf[j][e], kf[e], d);
-                sc[u * G + j] = d;
+                for (int e = 0; e < P; ++e) d = ffma2(qf[j][e], kf[e], d);
+                sc[u * G + j] = d.x + d.y;
             }
         }
         float red[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) red[i] = sc[i];
+        for (int r = 0; r < V; ++r) red[r] = sc[r];
         constexpr int kSteps = V >= 32 ? 5 : (V >= 16 ? 4 : (V >= 8 ? 3 : (V >= 4 ? 2 : (V >= 2 ? 1 : 0))));
 #pragma unroll
-        for (int st = 0; st < kSteps; ++st) {
-            const int offs = 16 >> st;
-            const int half = V >> (st + 1);
+        for (int k = 0; k < kSteps; ++k) {
+            const int offs = 16 >> k;
+            const int half = V >> (k + 1);
             const bool upper = (lane & offs) != 0;
 #pragma unroll
-            for (int i = 0; i < half; ++i) {
-                const float send = upper ? red[i] : red[i + half];
-                const float keep = upper ? red[i + half] : red[i];
-                red[i] = keep + __shfl_xor_sync(0xffffffffu, send, offs);
+            for (int r = 0; r < half; ++r) {
+                const float send = upper ? red[r] : red[r + half];
+                const float keep = upper ? red[r + half] : red[r];
+                red[r] = keep + __shfl_xor_sync(0xffffffffu, send, offs);
             }
         }
 #pragma unroll
-        for (int st = kSteps; st < 5; ++st) red[0] += __shfl_xor_sync(0xffffffffu, red[0], 16 >> st);
-        // lane holding score i: its bits map to lane bits 4, 3, ... from the top
+        for (int k = kSteps; k < 5; ++k) red[0] += __shfl_xor_sync(0xffffffffu, red[0], 16 >> k);
+        // After the butterfly, score r = u * G + j sits in the lanes whose bits
+        // 4, 3, ... (from the top) spell r.  The softmax arithmetic runs there,
+        // once per score: the chunk's max per head (over the lanes that differ
+        // in the u bits), the head's new running max, its weight 2^(s - max) and
+        // the rescale factor of the old sums; the weights, maxima and factors
+        // are then broadcast to every lane.
+        constexpr int kLogT = T >= 8 ? 3 : (T >= 4 ? 2 : (T >= 2 ? 1 : 0));
+        const int r_lane = (lane >> (5 - kSteps)) & (V - 1);
+        const int u_lane = r_lane / G;
+        const int j_lane = r_lane - u_lane * G;
+        const bool v_lane = ((okb >> u_lane) & 1u) != 0;
+        const float s_l = v_lane ? red[0] : -INFINITY;
+        float cm = s_l;
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            int src = 0;
+        for (int k = 0; k < kLogT; ++k) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16 >> k));
+        float m_old = m[0];
 #pragma unroll
-            for (int st = 0; st < kSteps; ++st)
-                if (i & (V >> (st + 1))) src |= 16 >> st;
-            sc[i] = __shfl_sync(0xffffffffu, red[0], src);
-        }
-        // online softmax, once per T tokens; rescale only when the max moves
+        for (int j = 1; j < G; ++j)
+            if (j_lane == j) m_old = m[j];
+        const float m_new = fmaxf(m_old, cm);
+        const float p_l = v_lane ? exp2_weight(s_l - m_new) : 0.f;
+        const float c_l = m_new == -INFINITY ? 1.f : exp2_weight(m_old - m_new);
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            float cm = -INFINITY;
+            const int src = j << (5 - kSteps);
+            const float mj = __shfl_sync(0xffffffffu, m_new, src);
+            const float cj = __shfl_sync(0xffffffffu, c_l, src);
+            if (mj > m[j]) {   // the same in every lane
+                l[j] *= cj;
+                const float2 c2 = make_float2(cj, cj);
+                const float2 z2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < T; ++u)
-                if (ok[u]) cm = fmaxf(cm, sc[u * G + j]);
-            if (cm == -INFINITY) continue;
-            if (cm > m[j]) {
-                const float corr = exp2f(m[j] - cm);
-                l[j] *= corr;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) o[j][e] *= corr;
-                m[j] = cm;
+                for (int e = 0; e < P; ++e) o[j][e] = ffma2(c2, o[j][e], z2);
+                m[j] = mj;
             }
+        }
 #pragma unroll
-            for (int u = 0; u < T; ++u) {
-                const float pu = ok[u] ? exp2f(sc[u * G + j] - m[j]) : 0.f;
+        for (int u = 0; u < T; ++u) {
+            if (!(okb & (1u << u))) continue;
+            float2 vf[P];
+            widen2<EPL>(stage + (T + u) * SM::kRow, vf);
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const float pu = __shfl_sync(0xffffffffu, p_l, (u * G + j) << (5 - kSteps));
                 l[j] += pu;
-                float vf[EPL];
-                widen<EPL>(vv[u], vf);
+                const float2 p2 = make_float2(pu, pu);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(pu, vf[e], o[j][e]);
+                for (int e = 0; e < P; ++e) o[j][e] = ffma2(p2, vf[e], o[j][e]);
             }
         }
     }
+    cp_async_wait<0>();   // the trailing (empty) groups; the ring is reused below
 
-    // combine the warps' states
+    // combine the warps' states (the ring area now holds the warps' outputs)
+    __syncthreads();
+    float* s_o = reinterpret_cast<float*>(smem);   // [kAttnWarps][G][HD]
     if (lane == 0) {
 #pragma unroll
         for (int j = 0; j < G; ++j) {
@@ -247,7 +391,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
 #pragma unroll
     for (int j = 0; j < G; ++j)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) s_o[(warp * G + j) * HD + lane * EPL + e] = o[j][e];
+        for (int e = 0; e < P; ++e) {
+            s_o[(warp * G + j) * HD + lane * EPL + 2 * e] = o[j][e].x;
+            s_o[(warp * G + j) * HD + lane * EPL + 2 * e + 1] = o[j][e].y;
+        }
     __syncthreads();
 
     float* out = p.partial +
@@ -277,37 +424,94 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     }
 }
 
+// Block-wide reductions for the merge kernel (blockDim.x a multiple of 32, <= 1024).
+__device__ __forceinline__ float block_max(float v, float* s_red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    float r = -INFINITY;
+    for (int w = 0; w < nw; ++w) r = fmaxf(r, s_red[w]);
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* s_red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    float r = 0.f;
+    for (int w = 0; w < nw; ++w) r += s_red[w];
+    __syncthreads();
+    return r;
+}
+
+constexpr int kMergeWarps = 8;
+
+// One CTA per (query head x sequence, 32 output elements): M = max_s m_s,
+// weights w_s = 2^(m_s - M) (in shared memory), L = sum_s w_s l_s, then each
+// warp sums w_s o_s[e] over every 8th segment for the CTA's 32 elements (one
+// per lane) and the eight partial sums are added: out[e] = sum / L.
 template <int HD>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kMergeWarps * 32)
     attn_merge_kernel(const float* __restrict__ partial, __nv_bfloat16* __restrict__ out, int num_segments)
 {
+    extern __shared__ float s_w[];   // [num_segments]
+    __shared__ float s_red[32];
+    __shared__ float s_acc[kMergeWarps][32];
     const int head = blockIdx.x;   // seq * num_q_heads + q head
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const float* base = partial + static_cast<long long>(head) * num_segments * (HD + 2);
-    float M = -INFINITY;
-    for (int s = 0; s < num_segments; ++s) M = fmaxf(M, base[static_cast<long long>(s) * (HD + 2)]);
-    float Lsum = 0.f;
-    if (M != -INFINITY)
-        for (int s = 0; s < num_segments; ++s) {
-            const float* ps = base + static_cast<long long>(s) * (HD + 2);
-            Lsum = fmaf(exp2f(ps[0] - M), ps[1], Lsum);
-        }
-    for (int e = threadIdx.x; e < HD; e += blockDim.x) {
-        float O = 0.f;
-        if (M != -INFINITY)
-            for (int s = 0; s < num_segments; ++s) {
-                const float* ps = base + static_cast<long long>(s) * (HD + 2);
-                O = fmaf(exp2f(ps[0] - M), ps[2 + e], O);
-            }
-        out[static_cast<long long>(head) * HD + e] = __float2bfloat16_rn(Lsum > 0.f ? O / Lsum : 0.f);
+    float mx = -INFINITY;
+    for (int s = threadIdx.x; s < num_segments; s += blockDim.x)
+        mx = fmaxf(mx, base[static_cast<long long>(s) * (HD + 2)]);
+    const float M = block_max(mx, s_red);
+    float lsum = 0.f;
+    for (int s = threadIdx.x; s < num_segments; s += blockDim.x) {
+        const float* ps = base + static_cast<long long>(s) * (HD + 2);
+        const float w = M == -INFINITY ? 0.f : exp2f(ps[0] - M);
+        s_w[s] = w;
+        lsum = fmaf(w, ps[1], lsum);
+    }
+    const float Lsum = block_sum(lsum, s_red);   // its barriers also publish s_w
+    const int e = blockIdx.y * 32 + lane;
+    const float* po = base + 2 + e;
+    float O = 0.f;
+    int s = warp;
+    for (; s + 3 * kMergeWarps < num_segments; s += 4 * kMergeWarps) {
+        const float o0 = po[static_cast<long long>(s) * (HD + 2)];
+        const float o1 = po[static_cast<long long>(s + kMergeWarps) * (HD + 2)];
+        const float o2 = po[static_cast<long long>(s + 2 * kMergeWarps) * (HD + 2)];
+        const float o3 = po[static_cast<long long>(s + 3 * kMergeWarps) * (HD + 2)];
+        O = fmaf(s_w[s], o0, O);
+        O = fmaf(s_w[s + kMergeWarps], o1, O);
+        O = fmaf(s_w[s + 2 * kMergeWarps], o2, O);
+        O = fmaf(s_w[s + 3 * kMergeWarps], o3, O);
+    }
+    for (; s < num_segments; s += kMergeWarps) O = fmaf(s_w[s], po[static_cast<long long>(s) * (HD + 2)], O);
+    s_acc[warp][lane] = O;
+    __syncthreads();
+    if (warp == 0) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) sum += s_acc[w][lane];
+        out[static_cast<long long>(head) * HD + e] = __float2bfloat16_rn(Lsum > 0.f ? sum / Lsum : 0.f);
     }
 }
 
 template <int HD, int G>
 int launch_split(const AttnLaunch& a, const AttnParams& p, cudaStream_t stream, char* msg, size_t msg_len)
 {
-    const size_t smem = static_cast<size_t>(kAttnWarps) * G * HD * sizeof(float);
+    const int smem = SplitSmem<HD, G>::kBytes;
     auto kern = attn_split_kernel<HD, G>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static SmemOptIn smem_opt;
+    cudaError_t e = smem_opt.ensure(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 1;
@@ -319,8 +523,8 @@ int launch_split(const AttnLaunch& a, const AttnParams& p, cudaStream_t stream, 
         snprintf(msg, msg_len, "attention launch failed: %s", cudaGetErrorString(e));
         return 1;
     }
-    const int merge_threads = HD < 256 ? HD : 256;
-    attn_merge_kernel<HD><<<a.num_seqs * a.num_q_heads, merge_threads, 0, stream>>>(
+    const dim3 merge_grid(a.num_seqs * a.num_q_heads, HD / 32, 1);
+    attn_merge_kernel<HD><<<merge_grid, kMergeWarps * 32, a.num_segments * sizeof(float), stream>>>(
         p.partial, reinterpret_cast<__nv_bfloat16*>(a.out), a.num_segments);
     e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -11,31 +11,51 @@ namespace {
 // needs 16-byte aligned bases and leading dimensions; the pack gives unaligned
 // operands that shape in a workspace without touching the caller's buffers
 // ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 1: inputs may not be modified).
+// Grid: x over 16-byte groups of a line, y over lines (grid-stride).  The
+// source may have any alignment (element loads); the destination lines are
+// 16-byte aligned (base and ld_dst), so each full group is one 16-byte store.
+template <typename T>
 __global__ void __launch_bounds__(256)
-    pack_16bit_kernel(const uint16_t* __restrict__ src, long long ld_src, uint16_t* __restrict__ dst,
-                      long long ld_dst, int inner, int outer)
+    pack_kernel(const T* __restrict__ src, long long ld_src, T* __restrict__ dst, long long ld_dst, int inner,
+                int outer)
 {
-    const long long total = static_cast<long long>(inner) * outer;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
-        const long long j = e / inner;
-        const long long i = e - j * inner;
-        dst[i + j * ld_dst] = src[i + j * ld_src];
+    constexpr int V = 16 / static_cast<int>(sizeof(T));
+    const long long i0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * V;
+    if (i0 >= inner) return;
+    const bool full = i0 + V <= inner;
+    for (long long j = blockIdx.y; j < outer; j += gridDim.y) {
+        const T* s = src + j * ld_src + i0;
+        T* d = dst + j * ld_dst + i0;
+        if (full) {
+            union {
+                uint4 u;
+                T e[V];
+            } pk;
+#pragma unroll
+            for (int t = 0; t < V; ++t) pk.e[t] = s[t];
+            *reinterpret_cast<uint4*>(d) = pk.u;
+        } else {
+            for (long long t = 0; i0 + t < inner; ++t) d[t] = s[t];
+        }
     }
 }
 
-// The same copy for 8-bit elements (FP8 operands).
-__global__ void __launch_bounds__(256)
-    pack_8bit_kernel(const uint8_t* __restrict__ src, long long ld_src, uint8_t* __restrict__ dst, long long ld_dst,
-                     int inner, int outer)
+template <typename T>
+int launch_pack_t(const T* src, long long ld_src, T* dst, long long ld_dst, int inner, int outer, cudaStream_t stream,
+                  char* msg, size_t msg_len)
 {
-    const long long total = static_cast<long long>(inner) * outer;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
-        const long long j = e / inner;
-        const long long i = e - j * inner;
-        dst[i + j * ld_dst] = src[i + j * ld_src];
+    if (inner <= 0 || outer <= 0) return 0;
+    constexpr int V = 16 / static_cast<int>(sizeof(T));
+    const long long groups = (static_cast<long long>(inner) + V - 1) / V;
+    const unsigned gx = static_cast<unsigned>((groups + 255) / 256);
+    const unsigned gy = static_cast<unsigned>(outer < 65535 ? outer : 65535);
+    pack_kernel<T><<<dim3(gx, gy, 1), 256, 0, stream>>>(src, ld_src, dst, ld_dst, inner, outer);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
+        return 1;
     }
+    return 0;
 }
 
 // C(m,n) = bias value (or +0.0) for m < M, n < N, C(m,n) at C[m + n*ldc]: the
@@ -81,33 +101,13 @@ __global__ void wait_timeout_probe_kernel(int* status, unsigned long long limit_
 int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long ld_dst, int inner, int outer,
                 cudaStream_t stream, char* msg, size_t msg_len)
 {
-    const long long total = static_cast<long long>(inner) * outer;
-    if (total <= 0) return 0;
-    long long grid = (total + 255) / 256;
-    if (grid > 4096) grid = 4096;
-    pack_16bit_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(src, ld_src, dst, ld_dst, inner, outer);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
-        return 1;
-    }
-    return 0;
+    return launch_pack_t<uint16_t>(src, ld_src, dst, ld_dst, inner, outer, stream, msg, msg_len);
 }
 
 int launch_pack_8bit(const uint8_t* src, long long ld_src, uint8_t* dst, long long ld_dst, int inner, int outer,
                      cudaStream_t stream, char* msg, size_t msg_len)
 {
-    const long long total = static_cast<long long>(inner) * outer;
-    if (total <= 0) return 0;
-    long long grid = (total + 255) / 256;
-    if (grid > 4096) grid = 4096;
-    pack_8bit_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(src, ld_src, dst, ld_dst, inner, outer);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
-        return 1;
-    }
-    return 0;
+    return launch_pack_t<uint8_t>(src, ld_src, dst, ld_dst, inner, outer, stream, msg, msg_len);
 }
 
 int launch_fill_bias(uint16_t* C, long long ldc, int M, int N, const uint16_t* bias, int bias_mode,

@@ -2,6 +2,7 @@
 // (not installed, not part of the C ABI).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -43,6 +44,27 @@ void record_error(const char* msg);
 
 // cuTensorMapEncodeTiled from the driver (resolved once through the runtime).
 TmapEncodeFn tmap_encoder();
+
+// Raises one kernel's dynamic shared-memory limit, once per device: a launcher
+// keeps one of these in a function-local static next to the kernel it launches,
+// so the attribute call is not repeated on every launch (it costs host time
+// that short kernels would otherwise wait for).
+struct SmemOptIn {
+    static constexpr int kMaxDevices = 128;
+    std::atomic<int> done[kMaxDevices];   // bytes already allowed on each device (static storage: zero)
+
+    cudaError_t ensure(const void* kernel, int bytes)
+    {
+        int dev = -1;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const bool slot = dev >= 0 && dev < kMaxDevices;
+        if (slot && done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess && slot) done[dev].store(bytes, std::memory_order_release);
+        return e;
+    }
+};
 
 // Launch of the tcgen05 GEMM: C (M x N, column-major, m contiguous, leading
 // dimension ldc) = A (M x K) * B (K x N) [+ bias], FP32 accumulation, FP16 or

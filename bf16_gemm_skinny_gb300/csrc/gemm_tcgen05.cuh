@@ -802,7 +802,8 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     p.wait_limit_ns = g.wait_limit_ns;
 
     auto kern = gemm_tcgen05_kernel<BN, A_MN, B_MN, IN, OUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
+    static SmemOptIn smem_opt;
+    cudaError_t e = smem_opt.ensure(reinterpret_cast<const void*>(kern), Cf::kSmemBytes);
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 1;
@@ -845,7 +846,8 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.wait_limit_ns = g.wait_limit_ns;
 
     auto kern = gemm_tcgen05_pair_kernel<A_MN, B_MN, IN, OUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
+    static SmemOptIn smem_opt;
+    cudaError_t e = smem_opt.ensure(reinterpret_cast<const void*>(kern), Cf::kSmemBytes);
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 1;
@@ -862,10 +864,19 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
-        cudaGetLastError();
-        clusters = g.num_sms / 2;
+    // Co-resident clusters of this instance: a property of the kernel and the
+    // device, queried once per device.
+    static std::atomic<int> max_clusters[SmemOptIn::kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= SmemOptIn::kMaxDevices) dev = -1;
+    int clusters = dev >= 0 ? max_clusters[dev].load(std::memory_order_acquire) : 0;
+    if (clusters < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            clusters = g.num_sms / 2;
+        } else if (dev >= 0) {
+            max_clusters[dev].store(clusters, std::memory_order_release);
+        }
     }
     if (clusters > g.num_sms / 2) clusters = g.num_sms / 2;
     if (clusters < 1) clusters = 1;

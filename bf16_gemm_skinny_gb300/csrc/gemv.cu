@@ -634,7 +634,8 @@ int launch_vec(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_l
     if (slab8 >= K8) slab8 = K8;
     if (slab8 < 1) slab8 = 1;
     const size_t smem = static_cast<size_t>(NT) * slab8 * 32;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static SmemOptIn smem_opt;
+    cudaError_t e = smem_opt.ensure(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 1;
@@ -728,7 +729,8 @@ int try_launch_pipe(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t 
     if (warps == 0) return 0;
     const long long smem = pipe_smem(NT, R, D, XF32, K8, warps);
     auto kern = gemv_bf16_pipe_kernel<NT, R, D, XF32>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static SmemOptIn smem_opt;
+    cudaError_t e = smem_opt.ensure(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         *status = 1;
@@ -791,7 +793,8 @@ int try_launch_tokpair(const GemvLaunch& g, cudaStream_t stream, char* msg, size
     if (warps == 0) return 0;
     const long long smem = x_bytes + warps * per_warp_ring;
     auto kern = gemv_bf16_tokpair_kernel<NT, R, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static SmemOptIn smem_opt;
+    cudaError_t e = smem_opt.ensure(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         *status = 1;

@@ -78,7 +78,7 @@ def check(got, ref, q, k, v, hd, scale, n_tok, label):
     vmax = float(np.max(np.abs(oracle.bf16_decode(v))))
     # worst |scale * sum q_e k_e| bound: head_dim * max|q| * max|k| * scale
     sum_abs = hd * float(qv.max()) * float(kv.max()) * abs(scale)
-    eps_w = hd * 2.0 ** -24 * sum_abs + 2.0 ** -22          # + exp rounding
+    eps_w = hd * 2.0 ** -24 * sum_abs + 2.0 ** -21          # + the hardware exp2 approximation
     bound = (2 * eps_w + n_tok * 2.0 ** -24) * vmax + 0.5 * ulp(np.maximum(np.abs(gv), np.abs(rv)), "bf16")
     err = np.abs(gv - rv)
     worst = int(np.argmax(err - bound))
