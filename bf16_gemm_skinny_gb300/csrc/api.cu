@@ -432,7 +432,13 @@ int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, 
         cudaError_t e = cudaMemsetAsync(y, 0, y_bytes, s);
         return e == cudaSuccess ? BSK_OK : fail_cuda(e, "cudaMemsetAsync");
     }
-    if (n <= 8) {
+    // n <= 2: the CUDA-core GEMV.  From n = 3 on the tensor-core skinny GEMM
+    // (128 x 32 tiles, deep TMA ring) streams W at least as fast: the CUDA-core
+    // kernels become FMA- and issue-bound as the token count grows (measured on
+    // GB300 at 34816 x 5120: equal at n = 3, 72 vs 114 us at n = 8).
+    const long long gemv_kernel = opt_or(BSK_OPT_GEMV_KERNEL, 0);
+    const bool cuda_core = n <= 8 && (gemv_kernel == 0 ? n <= 2 : gemv_kernel != 5);
+    if (cuda_core) {
         bsk::GemvLaunch g;
         g.W = W;
         g.x = x;
@@ -699,7 +705,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_FORCE_DIRECT_STORE: ok = value == 0 || value == 1; break;
     case BSK_OPT_GEMV_ROWS: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8; break;
     case BSK_OPT_GEMV_WARPS: ok = value >= 0 && value <= 16; break;
-    case BSK_OPT_GEMV_KERNEL: ok = value >= 0 && value <= 4; break;
+    case BSK_OPT_GEMV_KERNEL: ok = value >= 0 && value <= 5; break;
     case BSK_OPT_GEMM_KERNEL: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;

@@ -7,8 +7,8 @@
  *                      any leading dimensions and an optional fused bias;
  *   gemm_fp8           FP8 (E4M3 / E5M2) GEMM with FP32 accumulation;
  *   gemv_bf16          BF16 linear layer y = x W^T: the HBM-bound decode GEMV for
- *                      n <= 8 tokens (CUDA cores), the tensor-core GEMM for
- *                      larger n (prefill projections);
+ *                      n <= 2 tokens (CUDA cores), the tensor-core GEMM for
+ *                      larger n (skinny decode batches, prefill projections);
  *   decode_attention_bf16  split-KV decode attention over a paged BF16 KV cache.
  *
  * Conventions shared by every call:
@@ -149,10 +149,12 @@ int gemm_fp8(int format, const uint8_t* A, int lda, const uint8_t* B, int ldb, v
  *     y : [n, M] row-major   y(t,j) = y[t*M + j] = sum_k x(t,k) W(j,k)
  * Section 2: n = 1 is the decode GEMV, large n the prefill GEMM.
  *
- * n <= 8 runs the CUDA-core GEMV (128-bit weight stream, warp-shuffle
- * reduction); n > 8 runs the tcgen05 GEMM with both operands K-major.
- * Any M, K, n >= 0 are accepted (unaligned W/x or K % 8 != 0 take slower
- * variants, or the pack workspace for n > 8).  y must not overlap W or x.
+ * n <= 2 runs the CUDA-core GEMV (128-bit weight stream, warp-shuffle
+ * reduction); n >= 3 runs the tcgen05 GEMM with both operands K-major (tiles
+ * as narrow as 128 x 32 for small n).
+ * Any M, K, n >= 0 are accepted (unaligned W/x or K % 8 != 0 take a scalar
+ * CUDA-core variant, or the pack workspace on the tensor-core path).  y must
+ * not overlap W or x.
  */
 int gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);
 
@@ -270,10 +272,12 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_GEMM_KERNEL      GEMM kernel for 256-wide tiles: 1 one CTA per 128 x 256 tile,
  *                            2 CTA pairs on 256 x 256 tiles (default 2; narrower tiles
  *                            always run one CTA per 128 x BN tile)
- *   BSK_OPT_GEMV_KERNEL      GEMV kernel: 1 register streaming, 2 cp.async-pipelined,
- *                            3 pipelined with x kept in BF16, 4 token-paired (n >= 5)
- *                            (default: 1 for n <= 2, 2 for n <= 4, 4 beyond; a kernel
- *                            whose buffers do not fit in shared memory falls back)
+ *   BSK_OPT_GEMV_KERNEL      kernel of gemv_bf16 for n <= 8: 1 register streaming,
+ *                            2 cp.async-pipelined, 3 pipelined with x kept in BF16,
+ *                            4 token-paired (n >= 5) -- the CUDA-core GEMVs -- or 5 the
+ *                            tensor-core skinny GEMM (default: 1 for n <= 2, 5 for
+ *                            n >= 3; a CUDA-core kernel whose buffers do not fit in
+ *                            shared memory falls back to another)
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {

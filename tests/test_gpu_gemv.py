@@ -105,8 +105,8 @@ def test_kernels_rows_per_warp_and_block_shape(kernel, rows, warps, n):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
-@pytest.mark.parametrize("n", [1, 4, 5, 8])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("n", [1, 2, 4, 5, 8])
 def test_all_kernels_full_decode_shape(kernel, n):
     M, K = 34816, 5120
     W, x = operands(M, K, n, False)
@@ -120,12 +120,19 @@ def test_all_kernels_full_decode_shape(kernel, n):
 
 
 @pytest.mark.parametrize("M,K,n,offset", [(517, 1001, 3, 0), (300, 4096, 8, 1), (64, 7, 1, 0)])
-def test_scalar_variant(M, K, n, offset):
-    """K not a multiple of 8, or unaligned pointers: the scalar kernel."""
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_scalar_variant(M, K, n, offset, kernel):
+    """K not a multiple of 8, or unaligned pointers: the scalar CUDA-core kernel
+    (kernel 1 requested), or by default for n >= 3 the tensor-core path on
+    packed operands."""
     W, x = operands(M, K, n, False)
     ref, _ = oracle.linear_bf16(W, x, M, K, n)
-    got = run(W, x, M, K, n, offset=offset)
-    check_tolerance(got, ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), "scalar")
+    bsk.set_option("gemv_kernel", kernel)
+    try:
+        got = run(W, x, M, K, n, offset=offset)
+    finally:
+        bsk.set_option("gemv_kernel", 0)
+    check_tolerance(got, ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"unaligned, kernel {kernel}")
 
 
 @pytest.mark.parametrize("n", [1, 8])
