@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, G >= 8 ? 1 : 2)
     __shared__ float s_m[kAttnWarps][G];
     __shared__ float s_l[kAttnWarps][G];
     extern __shared__ __align__(16) uint8_t smem[];
+    // The merge kernel launched after this one may be scheduled from now on; it
+    // waits on the device for this grid to complete before reading anything.
+    asm volatile("griddepcontrol.launch_dependents;");
 
     int L = p.seq_lens[seq];
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
@@ -452,11 +455,17 @@ __device__ __forceinline__ float block_sum(float v, float* s_red)
 }
 
 constexpr int kMergeWarps = 8;
+constexpr int kMergeLoads = 16;   // o_s loads in flight per lane
 
-// One CTA per (query head x sequence, 32 output elements): M = max_s m_s,
-// weights w_s = 2^(m_s - M) (in shared memory), L = sum_s w_s l_s, then each
-// warp sums w_s o_s[e] over every 8th segment for the CTA's 32 elements (one
-// per lane) and the eight partial sums are added: out[e] = sum / L.
+// One CTA per (query head x sequence, 32 output elements).  It is launched as
+// a programmatic dependent of the split kernel, so it may be scheduled while
+// the split kernel's last CTAs still run; griddepcontrol.wait holds it until
+// that grid has completed and its partials are visible.  Then: each thread
+// loads (m_s, l_s) of its segments in one round, M = max_s m_s, weights
+// w_s = 2^(m_s - M) (in shared memory), L = sum_s w_s l_s; each warp sums
+// w_s o_s[e] over every 8th segment for the CTA's 32 elements (one per lane),
+// all of its loads issued before the sums, and the eight partial sums are
+// added: out[e] = sum / L.
 template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     attn_merge_kernel(const float* __restrict__ partial, __nv_bfloat16* __restrict__ out, int num_segments)
@@ -464,37 +473,55 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     extern __shared__ float s_w[];   // [num_segments]
     __shared__ float s_red[32];
     __shared__ float s_acc[kMergeWarps][32];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int head = blockIdx.x;   // seq * num_q_heads + q head
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    constexpr int kThreads = kMergeWarps * 32;
+    constexpr int kPerThread = 1024 / kThreads;   // num_segments <= 1024
     const float* base = partial + static_cast<long long>(head) * num_segments * (HD + 2);
+    float ms[kPerThread], ls[kPerThread];
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int s = threadIdx.x + i * kThreads;
+        ms[i] = -INFINITY;
+        ls[i] = 0.f;
+        if (s < num_segments) {
+            ms[i] = base[static_cast<long long>(s) * (HD + 2)];
+            ls[i] = base[static_cast<long long>(s) * (HD + 2) + 1];
+        }
+    }
     float mx = -INFINITY;
-    for (int s = threadIdx.x; s < num_segments; s += blockDim.x)
-        mx = fmaxf(mx, base[static_cast<long long>(s) * (HD + 2)]);
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) mx = fmaxf(mx, ms[i]);
     const float M = block_max(mx, s_red);
     float lsum = 0.f;
-    for (int s = threadIdx.x; s < num_segments; s += blockDim.x) {
-        const float* ps = base + static_cast<long long>(s) * (HD + 2);
-        const float w = M == -INFINITY ? 0.f : exp2f(ps[0] - M);
-        s_w[s] = w;
-        lsum = fmaf(w, ps[1], lsum);
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int s = threadIdx.x + i * kThreads;
+        if (s < num_segments) {
+            const float w = M == -INFINITY ? 0.f : exp2f(ms[i] - M);
+            s_w[s] = w;
+            lsum = fmaf(w, ls[i], lsum);
+        }
     }
     const float Lsum = block_sum(lsum, s_red);   // its barriers also publish s_w
     const int e = blockIdx.y * 32 + lane;
     const float* po = base + 2 + e;
     float O = 0.f;
-    int s = warp;
-    for (; s + 3 * kMergeWarps < num_segments; s += 4 * kMergeWarps) {
-        const float o0 = po[static_cast<long long>(s) * (HD + 2)];
-        const float o1 = po[static_cast<long long>(s + kMergeWarps) * (HD + 2)];
-        const float o2 = po[static_cast<long long>(s + 2 * kMergeWarps) * (HD + 2)];
-        const float o3 = po[static_cast<long long>(s + 3 * kMergeWarps) * (HD + 2)];
-        O = fmaf(s_w[s], o0, O);
-        O = fmaf(s_w[s + kMergeWarps], o1, O);
-        O = fmaf(s_w[s + 2 * kMergeWarps], o2, O);
-        O = fmaf(s_w[s + 3 * kMergeWarps], o3, O);
+    for (int s0 = warp; s0 < num_segments; s0 += kMergeWarps * kMergeLoads) {
+        float v[kMergeLoads];
+#pragma unroll
+        for (int u = 0; u < kMergeLoads; ++u) {
+            const int s = s0 + u * kMergeWarps;
+            v[u] = s < num_segments ? po[static_cast<long long>(s) * (HD + 2)] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeLoads; ++u) {
+            const int s = s0 + u * kMergeWarps;
+            if (s < num_segments) O = fmaf(s_w[s], v[u], O);
+        }
     }
-    for (; s < num_segments; s += kMergeWarps) O = fmaf(s_w[s], po[static_cast<long long>(s) * (HD + 2)], O);
     s_acc[warp][lane] = O;
     __syncthreads();
     if (warp == 0) {
@@ -523,10 +550,21 @@ int launch_split(const AttnLaunch& a, const AttnParams& p, cudaStream_t stream, 
         snprintf(msg, msg_len, "attention launch failed: %s", cudaGetErrorString(e));
         return 1;
     }
-    const dim3 merge_grid(a.num_seqs * a.num_q_heads, HD / 32, 1);
-    attn_merge_kernel<HD><<<merge_grid, kMergeWarps * 32, a.num_segments * sizeof(float), stream>>>(
-        p.partial, reinterpret_cast<__nv_bfloat16*>(a.out), a.num_segments);
-    e = cudaGetLastError();
+    // The merge is a programmatic dependent of the split kernel: it may be
+    // scheduled before the split grid has finished and waits on the device.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_seqs * a.num_q_heads, HD / 32, 1);
+    cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = a.num_segments * sizeof(float);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, static_cast<const float*>(p.partial),
+                           reinterpret_cast<__nv_bfloat16*>(a.out), a.num_segments);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "attention merge launch failed: %s", cudaGetErrorString(e));
         return 1;
