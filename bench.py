@@ -139,21 +139,30 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# The device code each measured kernel is built from: (file, text that starts
+# the file's host-only part or None).  Host-side launch code does not change
+# the kernel, so it is left out of the digest.
 KERNEL_SOURCES = {
-    "gemm": ("gemm_tcgen05.cuh", "gemm_tcgen05.cu", "ptx.cuh", "bsk_internal.h"),
-    "fp8": ("gemm_tcgen05.cuh", "gemm_fp8.cu", "ptx.cuh", "bsk_internal.h"),
-    "gemv": ("gemv.cu", "bsk_internal.h"),
+    "gemm": (("gemm_tcgen05.cuh", "inline CUtensorMapDataType tmap_type("), ("ptx.cuh", None),
+             ("bsk_internal.h", "using TmapEncodeFn")),
+    "gemv": (("gemv.cu", "int launch_vec(const GemvLaunch& g"), ("bsk_internal.h", "using TmapEncodeFn")),
 }
 
 
 def source_digest(kernel: str) -> str:
-    """Hash of one kernel's sources; a committed traffic figure is only reported
-    while that kernel is unchanged since it was measured."""
+    """Hash of one kernel's device code; a committed traffic figure is only
+    reported while that code is unchanged since it was measured."""
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "bf16_gemm_skinny_gb300", "csrc")
-    for name in KERNEL_SOURCES[kernel]:
+    for name, host_start in KERNEL_SOURCES[kernel]:
         with open(os.path.join(cdir, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+            text = f.read()
+        if host_start is not None:
+            cut = text.find(host_start.encode())
+            if cut < 0:
+                raise RuntimeError(f"{name}: host-code marker {host_start!r} not found")
+            text = text[:cut]
+        h.update(name.encode() + b"\0" + text)
     return h.hexdigest()[:16]
 
 
@@ -244,11 +253,52 @@ def oracle_gemm_sample(A, B, seconds: float, max_cols: int = 4096):
     return 2 * GEMM_M * GEMM_K * done, elapsed, done, threads
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, else the implementer/part codes)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model name", "CPU part"):
+        for line in info:
+            if line.split(":")[0].strip() == key:
+                value = line.split(":", 1)[1].strip()
+                if key == "CPU part":
+                    impl = next((ln.split(":", 1)[1].strip() for ln in info
+                                 if ln.split(":")[0].strip() == "CPU implementer"), "?")
+                    return f"implementer {impl}, part {value}"
+                return value
+    return "unknown"
+
+
+def single_thread_rates():
+    """The oracle on one thread: the whole 256^3 GEMM, and 64 output features of
+    the n = 1 GEMV at 34816x5120 (about a second each)."""
+    import oracle
+    from bf16_gemm_skinny_gb300 import inputs
+
+    A, B = inputs.gemm_operands(256, 256, 256, "uniform")
+    t0 = time.perf_counter()
+    oracle.gemm_f16_colmajor(A, B, 256, 256, 256, threads=1)
+    t_gemm = time.perf_counter() - t0
+    W, x = inputs.linear_operands(GEMV_M, GEMV_K, 1, "normal0.02", "normal1")
+    js = list(range(0, GEMV_M, GEMV_M // 64))[:64]
+    t0 = time.perf_counter()
+    oracle.linear_bf16(W, x, GEMV_M, GEMV_K, 1, js=js, threads=1)
+    t_gemv = time.perf_counter() - t0
+    return {"gemm_256_ms": round(t_gemm * 1e3, 2),
+            "gemm_256_gflops": round(2 * 256 ** 3 / t_gemm / 1e9, 3),
+            "gemv_n1_gbs": round(len(js) * GEMV_K * 2 / t_gemv / 1e9, 3),
+            "gemv_n1_sample": f"{len(js)} output features of 34816 (K = 5120)"}
+
+
 def cpu_baseline(A, B, seconds: float):
     flops, elapsed, cols, threads = oracle_gemm_sample(A, B, seconds)
     return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{cols} output columns of the 8192x8192x16384 GEMM (each 8192x16384 FMAs, FP64), "
-                      f"{elapsed:.1f} s"}
+                      f"{elapsed:.1f} s",
+            "cpu": cpu_model(), "single_thread": single_thread_rates()}
 
 
 # ---------------------------------------------------------------------------
@@ -464,6 +514,14 @@ def run_ours(args):
     gemm_ms = [e["g0"].elapsed_time(e["g1"]) for e in evs]
     gemv_ms = {n: [e[f"v0_{n}"].elapsed_time(e[f"v1_{n}"]) for e in evs] for n in GEMV_NS}
     gemm_ms_mean = statistics.fmean(gemm_ms)
+
+    def pct(values):
+        v = sorted(values)
+        q = lambda f: v[min(len(v) - 1, int(round(f * (len(v) - 1))))]  # noqa: E731
+        return {"mean": round(statistics.fmean(v) * 1e3, 2), "p10": round(q(0.1) * 1e3, 2),
+                "p50": round(q(0.5) * 1e3, 2), "p90": round(q(0.9) * 1e3, 2)}
+
+    timing_us = {"gemm": pct(gemm_ms), **{f"gemv_n{n}": pct(v) for n, v in gemv_ms.items()}}
     total_ms_max = max_over_ranks(total_ms, dist, dev)
     gemv_ms_mean = {n: max_over_ranks(statistics.fmean(v), dist, dev) for n, v in gemv_ms.items()}
 
@@ -491,6 +549,14 @@ def run_ours(args):
             if it:
                 e2e_gemv[n].append(time.perf_counter() - t0)
     e2e_gemm_s = max_over_ranks(statistics.median(e2e_gemm), dist, dev)
+    # the blocking call alone (device buffers, host sync inside), wall clock
+    blocking = []
+    for it in range(e2e_steps + 1):
+        t0 = time.perf_counter()
+        bsk.gemm_f16_colmajor(A, B, C, GEMM_M, GEMM_N, GEMM_K, stream)
+        if it:
+            blocking.append(time.perf_counter() - t0)
+    blocking_ms = max_over_ranks(statistics.median(blocking), dist, dev) * 1e3
     e2e_gemv_s = {n: max_over_ranks(statistics.median(v), dist, dev) for n, v in e2e_gemv.items()}
 
     peaks, peak_src = load_peaks()
@@ -526,6 +592,8 @@ def run_ours(args):
                    "gemm_stage_bytes_per_sm": tile_stage_bytes(128, 128, 64),
                    "l2": "inputs larger than L2 (GEMM operands 537 MB; each GEMV reads its own 356 MB weight copy)"},
         "gemv": gemv,
+        "timing_us": timing_us,
+        "blocking_call_ms": {"gemm_f16_colmajor": round(blocking_ms, 4)},
         "e2e": {"value": round(world * gemm_flops() / e2e_gemm_s / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "gemv_gbs": {f"n{n}": gemv[f"n{n}"]["e2e_gbs"] for n in GEMV_NS},
