@@ -122,11 +122,30 @@ def _addr(t) -> int | None:
     return int(t.data_ptr())
 
 
-def _stream(stream) -> int | None:
-    if stream is None:
+_torch = None
+_raw_stream = None
+
+
+def _current_stream_handle() -> int:
+    """cudaStream_t of torch's current stream on the current device.  Uses torch's
+    direct accessor when it has one (a plain call instead of a Stream object)."""
+    global _torch, _raw_stream
+    if _torch is None:
         import torch
 
-        return int(torch.cuda.current_stream().cuda_stream)
+        _torch = torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        get_dev = getattr(torch._C, "_cuda_getDevice", None)
+        if raw is not None and get_dev is not None:
+            _raw_stream = lambda: raw(get_dev())  # noqa: E731
+    if _raw_stream is not None:
+        return int(_raw_stream())
+    return int(_torch.cuda.current_stream().cuda_stream)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return _current_stream_handle()
     if isinstance(stream, int):
         return stream
     return int(stream.cuda_stream)

@@ -215,3 +215,27 @@ def test_watchdog_gives_up_and_library_stays_usable():
     assert bsk.test_wait_timeout(2000) == 4
     assert "gave up" in bsk.last_error()
     test_integer_inputs_bit_exact(129, 257, 65)
+
+
+def test_binding_uses_the_current_torch_stream():
+    """Without an explicit stream the binding launches on torch's current stream
+    (here a side stream); the work is ordered on that stream."""
+    import torch
+
+    M, N, K = 512, 384, 320
+    A, B = operands(M, N, K, "int2")
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    Ad, Bd = to_dev(A), to_dev(B)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        assert bsk._stream(None) == side.cuda_stream
+        C = torch.full((M * N,), FP16_NAN, dtype=torch.int16, device="cuda")
+        bsk.gemm_f16_colmajor_enqueue(Ad, Bd, C, M, N, K)
+    side.synchronize()
+    assert np.array_equal(from_dev(C), want)
+    assert bsk._stream(None) == torch.cuda.current_stream().cuda_stream
+    C2 = torch.empty(M * N, dtype=torch.int16, device="cuda")
+    bsk.gemm_f16_colmajor_enqueue(Ad, Bd, C2, M, N, K, stream=side)
+    side.synchronize()
+    assert np.array_equal(from_dev(C2), want)
