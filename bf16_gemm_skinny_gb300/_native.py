@@ -38,6 +38,7 @@ OPTIONS = {
     "num_sms": 8,
     "gemv_kernel": 9,
     "gemm_kernel": 10,
+    "stream_k": 11,
 }
 
 # Every symbol include/bsk.h declares.

@@ -44,7 +44,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 11;
+constexpr int kNumOpts = 12;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -218,13 +218,53 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     size_t a_bytes = a_ok ? 0 : static_cast<size_t>(lda_p) * a_outer * eb;
     size_t b_bytes = b_ok ? 0 : static_cast<size_t>(ldb_p) * b_outer * eb;
     a_bytes = (a_bytes + 255) / 256 * 256;
+    b_bytes = (b_bytes + 255) / 256 * 256;
+
+    // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
+    // tile, deep ring: the weight stream sets the pace), else 256 on CTA pairs.
+    // An MN-major B is staged in 64-column swizzle atoms: at least 64 wide.
+    const long long bn_opt = opt_or(BSK_OPT_BLOCK_N, 0);
+    const int bn_auto = op.N <= 32 ? 32 : op.N <= 64 ? 64 : op.N <= 128 ? 128 : 256;
+    int block_n = static_cast<int>(bn_opt > 0 ? bn_opt : bn_auto);
+    if (op.b_mn_major && block_n < 64) block_n = 64;
+    const long long gemm_kernel = opt_or(BSK_OPT_GEMM_KERNEL, 0);
+    bool pair = block_n == 256 && gemm_kernel != 1;
+    // Stream-K (one-CTA-per-tile kernel) when whole tiles would leave more than
+    // a quarter of the SM slots idle and each tile has at least 32 k-blocks to
+    // share.  Its fixed costs (workspace, flag reset, cooperative launch: about
+    // 13 us of host and device time per call on GB300) outweigh the gain on
+    // short problems and when the waves are already nearly full (measured: 272
+    // tiles on 152 SMs 8% slower split; 4096 x 256 x 8192 13% faster split than
+    // on CTA pairs; 256^3 and 1024^3 twice as slow).  A 256-wide shape whose
+    // CTA-pair tiles would fill under three quarters of the pairs runs split on
+    // single CTAs instead.
+    const long long kbs = (op.K + (fp8 ? 127LL : 63LL)) / (fp8 ? 128 : 64);
+    const long long sk_opt = opt_or(BSK_OPT_STREAM_K, 0);
+    auto fill = [&](long long tiles, long long slots) {
+        const long long waves = (tiles + slots - 1) / slots;
+        return static_cast<double>(tiles) / static_cast<double>(waves * slots);
+    };
+    const long long m_tiles = (op.M + 127LL) / 128;
+    if (pair && gemm_kernel == 0 && sk_opt != 1 && kbs >= 32) {
+        const long long pair_tiles = ((op.M + 255LL) / 256) * ((op.N + 255LL) / 256);
+        if (fill(pair_tiles, sms / 2 > 0 ? sms / 2 : 1) < 0.75) pair = false;
+    }
+    bool stream_k = false;
+    if (!pair && sk_opt != 1) {
+        const long long tiles = m_tiles * ((op.N + block_n - 1LL) / block_n);
+        stream_k = sk_opt == 2 || (fill(tiles, sms) < 0.75 && kbs >= 32);
+    }
+    const size_t sk_part_bytes = stream_k ? static_cast<size_t>(sms) * block_n * 128 * sizeof(float) : 0;
+    const size_t sk_flag_bytes = stream_k ? static_cast<size_t>(sms) * sizeof(int) : 0;
 
     Workspace ws;
     const void* Ause = op.A;
     const void* Buse = op.B;
+    float* sk_part = nullptr;
+    int* sk_flag = nullptr;
     char msg[512] = "";
-    if (a_bytes + b_bytes > 0) {
-        int st = alloc_workspace(ws, a_bytes + b_bytes, s);
+    if (a_bytes + b_bytes + sk_part_bytes + sk_flag_bytes > 0) {
+        int st = alloc_workspace(ws, a_bytes + b_bytes + sk_part_bytes + sk_flag_bytes, s);
         if (st != BSK_OK) return st;
         uint8_t* base = static_cast<uint8_t*>(ws.ptr);
         if (!a_ok) {
@@ -236,6 +276,12 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
             if (pack_operand(op.B, op.ldb, base + a_bytes, ldb_p, b_inner, b_outer, eb, s, msg, sizeof(msg)))
                 return fail(BSK_ERR_CUDA, "%s", msg);
             Buse = base + a_bytes;
+        }
+        if (stream_k) {
+            sk_part = reinterpret_cast<float*>(base + a_bytes + b_bytes);
+            sk_flag = reinterpret_cast<int*>(base + a_bytes + b_bytes + sk_part_bytes);
+            cudaError_t e = cudaMemsetAsync(sk_flag, 0, sk_flag_bytes, s);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(stream-K flags)");
         }
     }
 
@@ -256,14 +302,11 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     g.alpha = op.alpha;
     g.bias = op.bias_mode != 0 ? op.bias : nullptr;
     g.bias_mode = op.bias_mode;
-    // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
-    // tile, deep ring: the weight stream sets the pace), else 256 on CTA pairs.
-    // An MN-major B is staged in 64-column swizzle atoms: at least 64 wide.
-    const long long bn_opt = opt_or(BSK_OPT_BLOCK_N, 0);
-    const int bn_auto = op.N <= 32 ? 32 : op.N <= 64 ? 64 : op.N <= 128 ? 128 : 256;
-    g.block_n = static_cast<int>(bn_opt > 0 ? bn_opt : bn_auto);
-    if (op.b_mn_major && g.block_n < 64) g.block_n = 64;
-    g.pair = g.block_n == 256 && opt_or(BSK_OPT_GEMM_KERNEL, 2) == 2;
+    g.block_n = block_n;
+    g.pair = pair;
+    g.stream_k = stream_k;
+    g.sk_part = sk_part;
+    g.sk_flag = sk_flag;
     // Tile-row group: measured best on GB300 for 8192^3-class and prefill shapes.
     g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, g.pair && g.block_n == 256 ? 2 : 16));
     // TMA store of C: 16-byte aligned base and ldc, and M a multiple of 8.  With
@@ -707,6 +750,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_GEMV_WARPS: ok = value >= 0 && value <= 16; break;
     case BSK_OPT_GEMV_KERNEL: ok = value >= 0 && value <= 5; break;
     case BSK_OPT_GEMM_KERNEL: ok = value >= 0 && value <= 2; break;
+    case BSK_OPT_STREAM_K: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

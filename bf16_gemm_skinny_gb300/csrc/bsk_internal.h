@@ -97,6 +97,9 @@ struct GemmLaunch {
     const uint16_t* bias = nullptr;  // optional, output precision
     int bias_mode = 0;       // 1: bias[m] per row, 2: bias[n] per column
     int num_sms = 1;         // persistent grid size cap
+    bool stream_k = false;   // one-CTA-per-tile kernel only: stream-K schedule over num_sms CTAs
+    float* sk_part = nullptr;  // stream-K: num_sms * block_n * 128 floats of workspace
+    int* sk_flag = nullptr;    // stream-K: num_sms ints, zero before the launch
     int* status = nullptr;   // device status word
     unsigned long long wait_limit_ns = 2000000000ull;
 };

@@ -94,9 +94,57 @@ struct Params {
     const uint16_t* bias;   // optional, output precision: bias[m] (mode 1) or bias[n] (mode 2)
     int bias_mode;
     float alpha;            // FP8 inputs: scale of the FP32 accumulator
+    // Stream-K schedule (one-CTA-per-tile kernel only): CTA c of the grid takes
+    // iterations [c*I/G, (c+1)*I/G) of the I = num_tiles * num_kb (tile, k-block)
+    // iterations in tile order.  A tile split between CTAs is finished by the CTA
+    // that holds its first k-block; the others leave FP32 partials in their slot.
+    int sk;                 // 1: stream-K, 0: whole tiles, blockIdx.x + j * gridDim.x
+    long long sk_iters;     // num_tiles * num_kb
+    float* sk_part;         // [gridDim.x][BN][128]: column-major partial tile per CTA
+    int* sk_flag;           // [gridDim.x], zero at launch: set once a CTA's slot is written
     int* status;
     unsigned long long wait_limit_ns;
 };
+
+// A CTA's work as a sequence of segments (tile, k-blocks [kb0, kb1)).
+struct SegCursor {
+    long long pos, end;
+};
+
+__device__ __forceinline__ SegCursor seg_first(const Params& p)
+{
+    if (p.sk) {
+        const long long g = gridDim.x;
+        return {static_cast<long long>(blockIdx.x) * p.sk_iters / g,
+                static_cast<long long>(blockIdx.x + 1) * p.sk_iters / g};
+    }
+    return {static_cast<long long>(blockIdx.x), static_cast<long long>(p.num_tiles)};
+}
+
+__device__ __forceinline__ bool seg_next(const Params& p, SegCursor& c, int& tile, int& kb0, int& kb1)
+{
+    if (c.pos >= c.end) return false;
+    if (!p.sk) {
+        tile = static_cast<int>(c.pos);
+        kb0 = 0;
+        kb1 = p.num_kb;
+        c.pos += gridDim.x;
+        return true;
+    }
+    tile = static_cast<int>(c.pos / p.num_kb);
+    const long long t0 = static_cast<long long>(tile) * p.num_kb;
+    const long long e = c.end < t0 + p.num_kb ? c.end : t0 + p.num_kb;
+    kb0 = static_cast<int>(c.pos - t0);
+    kb1 = static_cast<int>(e - t0);
+    c.pos = e;
+    return true;
+}
+
+// The CTA whose stream-K share holds iteration i: the largest c with c*I/G <= i.
+__device__ __forceinline__ int sk_cta_of(const Params& p, long long i)
+{
+    return static_cast<int>(((i + 1) * static_cast<long long>(gridDim.x) + p.sk_iters - 1) / p.sk_iters) - 1;
+}
 
 // Identifiers of the waits, reported in the status word on a timeout.
 enum WaitSite {
@@ -106,6 +154,7 @@ enum WaitSite {
     kSiteEpilogueTmemFull = 4,
     kSiteMmaDrain = 5,
     kSiteProducerDrain = 6,
+    kSiteStreamKPartial = 7,
 };
 
 // One rounding of the FP32 accumulator to a 16-bit output type.
@@ -278,12 +327,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            SegCursor cur = seg_first(p);
+            int tile, kb0, kb1;
+            while (ok && seg_next(p, cur, tile, kb0, kb1)) {
                 int pm, pn;
                 tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
                 const int m0 = pm * kBM;
                 const int n0 = pn * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -334,8 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             bool issued_any = false;
-            int it = 0;
-            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+            SegCursor cur = seg_first(p);
+            int tile, kb0, kb1;
+            for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
                 const int acc = it & 1;
                 const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
                 if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
@@ -344,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
                         ok = false;
                         break;
@@ -360,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  : smem_desc_sw128(a_base + kk * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
                                                  : smem_desc_sw128(b_base + kk * 32, 16, 1024);
-                        mma_issue<Ty::kFp8>(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        mma_issue<Ty::kFp8>(d_tmem, ad, bd, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     mma_commit(empty0 + 8 * stage);
                     issued_any = true;
@@ -386,8 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;             // TMEM lanes this warp may read
         const int ew = warp - 2;                  // owner of a staging buffer pair
         uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
-        int it = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+        SegCursor cur = seg_first(p);
+        int tile, kb0, kb1;
+        for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
             const int acc = it & 1;
             const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
             bool ok = mbar_wait(tfull0 + 8 * acc, aph, wc, kSiteEpilogueTmemFull);
@@ -400,6 +453,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n0 = pn * BN;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
+            // Stream-K roles: a segment that does not start the tile leaves its
+            // partial in this CTA's slot; one that starts it but does not end it
+            // adds the slots of the CTAs holding the rest of the tile.
+            const bool to_slot = p.sk && kb0 != 0;
+            int q_last = static_cast<int>(blockIdx.x);
+            if (p.sk && kb0 == 0 && kb1 != p.num_kb) {
+                q_last = sk_cta_of(p, static_cast<long long>(tile + 1) * p.num_kb - 1);
+                bool fok = true;
+                for (int q = static_cast<int>(blockIdx.x) + 1; fok && q <= q_last; ++q)
+                    fok = flag_wait_acquire(p.sk_flag + q, wc, kSiteStreamKPartial);
+                (void)__all_sync(0xffffffffu, fok);   // on a timeout the status word is set; the output is undefined
+            }
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
@@ -410,6 +475,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+                }
+                const long long slot_col = static_cast<long long>(c * 32) * kBM + quarter * 32 + lane;
+                if (to_slot) {
+                    float* ps = p.sk_part + static_cast<long long>(blockIdx.x) * BN * kBM + slot_col;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ps[j * kBM] = __uint_as_float(r[j]);
+                    continue;
+                }
+                for (int q = static_cast<int>(blockIdx.x) + 1; q <= q_last; ++q) {
+                    const float* pq = p.sk_part + static_cast<long long>(q) * BN * kBM + slot_col;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + pq[j * kBM]);
                 }
                 finish_acc<IN, OUT>(r, p, m0 + lane, n0 + c * 32);
                 if (Ty::kOutBytes == 2 && p.tma_store) {
@@ -428,6 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     store_row<OUT>(r, p, m0 + lane, n0 + c * 32);
                 }
+            }
+            if (to_slot) {
+                // every epilogue warp's part of the slot is written before the flag is released
+                __threadfence();
+                asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+                if (warp == 2 && lane == 0) flag_set_release(p.sk_flag + blockIdx.x);
             }
         }
         if (lane == 0) bulk_wait_group<0>();
@@ -808,9 +891,42 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 1;
     }
+    int grid = 0;
+    p.sk = 0;
+    p.sk_iters = 0;
+    p.sk_part = nullptr;
+    p.sk_flag = nullptr;
+    if (g.stream_k && g.sk_part != nullptr && g.sk_flag != nullptr) {
+        // Every SM takes an equal share of the (tile, k-block) iterations.  The CTAs
+        // of a split tile wait on one another, so they must all be resident: the
+        // launch is cooperative (it fails rather than run them in waves).
+        p.sk = 1;
+        p.sk_iters = static_cast<long long>(p.num_tiles) * p.num_kb;
+        grid = g.num_sms;
+        if (grid > p.sk_iters) grid = static_cast<int>(p.sk_iters);
+        p.sk_part = g.sk_part;
+        p.sk_flag = g.sk_flag;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cf::kSmemBytes;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "GEMM (stream-K) launch failed: %s", cudaGetErrorString(e));
+            return 1;
+        }
+        return 0;
+    }
     // Every CTA gets the same number of tiles (the last wave is not left partial).
     const int per_cta = (p.num_tiles + g.num_sms - 1) / g.num_sms;
-    const int grid = (p.num_tiles + per_cta - 1) / per_cta;
+    grid = (p.num_tiles + per_cta - 1) / per_cta;
     kern<<<grid, kThreads, Cf::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -842,6 +958,10 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.bias = g.bias;
     p.bias_mode = g.bias != nullptr ? g.bias_mode : 0;
     p.alpha = g.alpha;
+    p.sk = 0;
+    p.sk_iters = 0;
+    p.sk_part = nullptr;
+    p.sk_flag = nullptr;
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
 

@@ -98,6 +98,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// Wait until the global flag word reads nonzero (acquire at GPU scope: what
+// the writer stored before releasing the flag is visible afterwards).  Same
+// bounds and failure reporting as mbar_wait.
+__device__ __forceinline__ bool flag_wait_acquire(const int* flag, const WaitCtl& w, int site)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v != 0) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v != 0) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            *w.abort_flag = 1u;
+            *reinterpret_cast<volatile int*>(w.status) = kDevErrTimeoutBase + site;
+            return false;
+        }
+    }
+}
+
+// Sets a global flag word with release semantics at GPU scope.
+__device__ __forceinline__ void flag_set_release(int* flag)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
+
 // Same wait with cluster-scope acquire, for barriers that other CTAs of the
 // cluster arrive on remotely.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)

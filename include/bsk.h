@@ -278,6 +278,11 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *                            tensor-core skinny GEMM (default: 1 for n <= 2, 5 for
  *                            n >= 3; a CUDA-core kernel whose buffers do not fit in
  *                            shared memory falls back to another)
+ *   BSK_OPT_STREAM_K         schedule of the one-CTA-per-tile GEMM kernel: 1 whole tiles,
+ *                            2 stream-K (every SM an equal share of the tile x k-block
+ *                            iterations; split tiles are summed in FP32 by the CTA that
+ *                            holds their first k-block), 0 automatic: stream-K when whole
+ *                            tiles would leave the last wave under 90% full
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
@@ -290,7 +295,8 @@ enum {
     BSK_OPT_WAIT_LIMIT_US = 7,
     BSK_OPT_NUM_SMS = 8,
     BSK_OPT_GEMV_KERNEL = 9,
-    BSK_OPT_GEMM_KERNEL = 10
+    BSK_OPT_GEMM_KERNEL = 10,
+    BSK_OPT_STREAM_K = 11
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);

@@ -252,3 +252,19 @@ def test_large_sampled(fmt, out, M, N, K):
     amax, bmax = absmax(A2, fmt), absmax(B2, fmt)
     check(got[rows, :], ref_r, out, K, amax, bmax, alpha, "sampled rows")
     check(got[:, cols], ref_c, out, K, amax, bmax, alpha, "sampled columns")
+
+
+@pytest.mark.parametrize("M,N,K,stream_k", [(34816, 16, 5120, 0), (34816, 16, 5120, 1), (1000, 40, 4096, 2),
+                                            (512, 100, 8192, 2)])
+def test_stream_k_schedule(M, N, K, stream_k):
+    """FP8 skinny shapes take stream-K by default (272 row tiles on the SMs);
+    forced on or off, integer inputs give the oracle's bits."""
+    A2, B2 = operands(M, N, K, "int2", "e4m3")
+    bsk.set_option("stream_k", stream_k)
+    try:
+        got, Af, lda, Bf, ldb = run(A2, B2, "e4m3", "f32")
+    finally:
+        bsk.set_option("stream_k", 0)
+    cols = sorted({0, N // 2, N - 1})
+    _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", "f32", cols=cols)
+    assert np.array_equal(got[:, cols], bits)
