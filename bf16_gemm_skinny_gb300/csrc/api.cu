@@ -563,7 +563,9 @@ int enqueue_decode_attention(const uint16_t* q, const uint16_t* k_cache, const u
     int segs = num_segments;
     if (segs <= 0) {
         const long long heads = static_cast<long long>(num_seqs) * num_kv_heads;
-        long long want = (2LL * sms + heads - 1) / heads;
+        // one full wave of the split kernel: as many CTAs as fit on the SMs
+        const long long per_sm = bsk::attention_ctas_per_sm(head_dim, num_q_heads / num_kv_heads);
+        long long want = (per_sm * sms + heads - 1) / heads;
         const long long cap = (max_seq_len + 63) / 64;
         if (want > cap) want = cap;
         if (want < 1) want = 1;

@@ -13,13 +13,13 @@
 //     16 segments, or 32 once the longest sequence reaches 12,288 tokens.
 //
 // Kernel 1 (one CTA per segment x KV head x sequence): the CTA owns the G query
-// heads that read its KV head.  Each lane holds head_dim/32 consecutive
-// elements of every q, k and v row; warps take tokens in turn, T at a time,
-// streamed through a per-warp cp.async ring in shared memory, compute the G
-// dot products with warp shuffles and keep an online softmax state (running
-// max m, sum l, unnormalised output o) per head in base-2 (scores
-// pre-multiplied by scale * log2 e).  The warps' states are combined in shared
-// memory and the segment's (m, l, o) go to a workspace.
+// heads that read its KV head.  Its warps take tokens in turn, 8 at a time,
+// streamed through a per-warp cp.async ring in shared memory; the G x 8 scores
+// of a chunk come from tensor-core MMAs (BF16 products, FP32 sums), and an
+// online softmax state (running max m, sum l, unnormalised output o) per head
+// is kept in base 2 (scores multiplied by scale * log2 e); each lane holds
+// head_dim/32 consecutive elements of every head's output.  The warps' states
+// are combined in shared memory and the segment's (m, l, o) go to a workspace.
 // Kernel 2 (one CTA per query head x sequence x 32 output elements) merges the
 // segments:
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  out = sum_s o_s 2^(m_s - M) / L.
@@ -35,8 +35,8 @@
 namespace bsk {
 namespace {
 
-constexpr int kAttnWarps = 8;
-constexpr int kAttnTokens = 4;   // tokens per warp per ring stage
+constexpr int kAttnWarps = 4;
+constexpr int kAttnTokens = 8;   // tokens per warp per ring stage: the N of the score MMA
 constexpr int kAttnStages = 3;   // cp.async ring depth per warp
 
 template <int EPL>
@@ -131,7 +131,9 @@ struct AttnParams {
 };
 
 // Shared memory of the split kernel: the warps' cp.async rings, reused after
-// the token loop for the warps' (unnormalised) outputs.
+// the token loop for the warps' (unnormalised) outputs.  Rows of a stage are
+// stored with their 16-byte chunks permuted (chunk c of row r at c ^ (r & 7))
+// so that the eight rows an ldmatrix reads at once fall in distinct banks.
 template <int HD, int G>
 struct SplitSmem {
     static constexpr int kRow = HD * 2;                          // bytes of one K or V row
@@ -142,30 +144,72 @@ struct SplitSmem {
     static constexpr int kBytes = kRing > kOut ? kRing : kOut;
 };
 
-// Each warp streams its chunks (T tokens each; the warps take chunks in turn)
-// through a private D-stage ring in shared memory: the copies for chunk i+D-1
-// are issued before chunk i is consumed, so the bytes in flight do not depend
-// on where the warp is in its arithmetic.  Each lane copies, and later reads,
-// only its own slice (head_dim/32 values) of every row, so cp.async.wait_group
-// is the only synchronisation the ring needs.
+// Byte offset of byte b of row r inside a stage.
+template <int ROW>
+__device__ __forceinline__ uint32_t swz(int r, int b)
+{
+    return static_cast<uint32_t>(r * ROW + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D (16 x 8, FP32) += A (16 x 16, BF16, row-major) * B (16 x 8, BF16, column-major).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Each warp streams its chunks (T = 8 tokens each; the warps take chunks in
+// turn) through a private D-stage ring in shared memory: the copies for chunk
+// i+D-1 are issued before chunk i is consumed.  Each lane copies its own slice
+// (head_dim/32 values) of every K and V row.
+//
+// Scores on the tensor cores: S (heads x 8 tokens) = Q (heads x head_dim) K^T
+// as head_dim/16 mma.sync m16n8k16 steps, the G query heads as rows 0..G-1 of
+// A (held in registers for the whole kernel), the chunk's K rows as B (loaded
+// with ldmatrix).  BF16 products are exact and the sums are FP32, as before.
+// Lane 4g + c then holds head g's scores for tokens 2c, 2c+1: the four lanes of
+// a head find the chunk max, the head's new running max, the weights
+// 2^(s - max), their sum and the rescale factor of the old sums, and put the
+// weights and factors in shared memory.  The output update stays on the CUDA
+// cores in FP32: every lane owns head_dim/32 values of each head's output and
+// adds weight x V row (packed FMAs) for the chunk's tokens.
 template <int HD, int G>
-__global__ void __launch_bounds__(kAttnWarps * 32, G >= 8 ? 1 : 2)
+__global__ void __launch_bounds__(kAttnWarps * 32, 2)
     attn_split_kernel(const AttnParams p)
 {
     constexpr int EPL = HD / 32;
     constexpr int LB = EPL * 2;   // bytes per lane per row
     constexpr int T = kAttnTokens;
     constexpr int D = kAttnStages;
+    constexpr int KS = HD / 16;   // MMA k-steps
     using SM = SplitSmem<HD, G>;
-    using Vec = typename RowVec<EPL>::T;
+    static_assert(G <= 8, "at most 8 query heads per KV head (rows of the score MMA)");
+    static_assert(KS % 2 == 0, "k-steps are loaded two at a time");
     const int seg = blockIdx.x;
     const int kvh = blockIdx.y;
     const int seq = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2;      // MMA group: the head this lane's scores belong to
+    const int cq = lane & 3;       // position in the group: tokens 2cq, 2cq+1
 
     __shared__ float s_m[kAttnWarps][G];
     __shared__ float s_l[kAttnWarps][G];
+    // weights of the chunk and rescale factors, each stored twice ({w, w}): the
+    // packed FMAs of the output update take them as pairs straight from memory
+    __shared__ __align__(16) float2 s_p[kAttnWarps][T][G];
+    __shared__ __align__(16) float2 s_c[kAttnWarps][G];
     extern __shared__ __align__(16) uint8_t smem[];
     // The merge kernel launched after this one may be scheduled from now on; it
     // waits on the device for this grid to complete before reading anything.
@@ -177,37 +221,37 @@ __global__ void __launch_bounds__(kAttnWarps * 32, G >= 8 ? 1 : 2)
     const int t0 = seg * seg_len;
     const int t1 = (t0 + seg_len < L) ? t0 + seg_len : L;
 
-    // this lane's slice of the G query rows, pre-scaled into the base-2 domain,
-    // as FP32 pairs (the dot products and the output run on packed FMAs)
-    constexpr int P = EPL / 2;
-    float2 qf[G][P];
+    // A fragments of the query rows: lane (g, c) holds q[g][16s + 2c, +1] and
+    // q[g][16s + 2c + 8, +9] for every k-step s (rows 8..15 of A are zero)
+    uint32_t qa[KS][2];
+    {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + (gq < G ? gq : 0)) * HD);
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-        widen2<EPL>(reinterpret_cast<const uint8_t*>(
-                        p.q + (static_cast<long long>(seq) * p.num_q_heads + kvh * G + j) * HD + lane * EPL),
-                    qf[j]);
-#pragma unroll
-        for (int e = 0; e < P; ++e) {
-            qf[j][e].x *= p.scale_log2;
-            qf[j][e].y *= p.scale_log2;
+        for (int k = 0; k < KS; ++k) {
+            qa[k][0] = gq < G ? qrow[8 * k + cq] : 0u;
+            qa[k][1] = gq < G ? qrow[8 * k + 4 + cq] : 0u;
         }
     }
 
-    float m[G], l[G];
+    constexpr int P = EPL / 2;
+    float m_h = -INFINITY, l_h = 0.f;   // running max and sum of head gq (lanes of a head agree)
     float2 o[G][P];
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-        m[j] = -INFINITY;
-        l[j] = 0.f;
+    for (int j = 0; j < G; ++j)
 #pragma unroll
         for (int e = 0; e < P; ++e) o[j][e] = make_float2(0.f, 0.f);
-    }
 
     const int32_t* bt = p.block_tables + static_cast<long long>(seq) * p.max_blocks;
     const long long tok_stride = static_cast<long long>(p.num_kv_heads) * HD;   // elements between tokens
     const long long head_off = static_cast<long long>(kvh) * HD + lane * EPL;
-    uint8_t* wring = smem + warp * SM::kWarpRing;                 // this warp's ring
-    const uint32_t ring = smem_addr(wring) + lane * LB;            // this lane's slice of it
+    uint8_t* wring = smem + warp * SM::kWarpRing;   // this warp's ring
+    const uint32_t ring = smem_addr(wring);
+    // this lane's slice of row r (< 8) of a stage, and of row 8 + r, relative to
+    // row 0 and row 8: slice_off[r] (the row offset r * kRow included)
+    uint32_t slice_off[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) slice_off[r] = swz<SM::kRow>(r, lane * LB);
     constexpr int kChunkStep = kAttnWarps * T;
     const int first = t0 + warp * T;
     const int nch = first < t1 ? (t1 - first + kChunkStep - 1) / kChunkStep : 0;
@@ -228,8 +272,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, G >= 8 ? 1 : 2)
                 const uint16_t* vs = p.v + row;
 #pragma unroll
                 for (int u = 0; u < T; ++u) {
-                    cp_async<LB>(dst0 + u * SM::kRow, ks + u * tok_stride, LB);
-                    cp_async<LB>(dst0 + (T + u) * SM::kRow, vs + u * tok_stride, LB);
+                    cp_async<LB>(dst0 + slice_off[u], ks, LB);
+                    cp_async<LB>(dst0 + T * SM::kRow + slice_off[u], vs, LB);
+                    ks += tok_stride;
+                    vs += tok_stride;
                 }
                 cp_async_commit();
                 return (1u << T) - 1u;
@@ -253,9 +299,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, G >= 8 ? 1 : 2)
                     vs = p.v + row;
                 }
             }
-            const uint32_t dst = dst0 + u * SM::kRow;
-            cp_async<LB>(dst, ks, ok ? LB : 0u);
-            cp_async<LB>(dst + T * SM::kRow, vs, ok ? LB : 0u);
+            cp_async<LB>(dst0 + slice_off[u], ks, ok ? LB : 0u);
+            cp_async<LB>(dst0 + T * SM::kRow + slice_off[u], vs, ok ? LB : 0u);
             bits |= (ok ? 1u : 0u) << u;
             if (++off == p.block_size) {
                 off = 0;
@@ -279,7 +324,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, G >= 8 ? 1 : 2)
         vbits |= b << (i * T);
     }
 
-    constexpr int V = T * G;   // scores per chunk, index u * G + j
     for (int i = 0; i < nch; ++i) {
         const int st = i % D;
         const int in = i + D - 1;
@@ -291,105 +335,82 @@ __global__ void __launch_bounds__(kAttnWarps * 32, G >= 8 ? 1 : 2)
             cp_async_commit();
         }
         vbits = (vbits & ~(kMask << (sn * T))) | (b << (sn * T));
-        cp_async_wait<D - 1>();   // chunk i has landed (this lane's slices)
+        cp_async_wait<D - 1>();   // chunk i has landed (this lane's copies) ...
+        __syncwarp();             // ... and every lane's: the score MMA reads all of them
         const uint32_t okb = (vbits >> (st * T)) & kMask;
-        const uint8_t* stage = wring + st * SM::kStage + lane * LB;
+        const uint32_t stage = ring + st * SM::kStage;
 
-        // partial dot products, then a butterfly that leaves each lane pair (or
-        // group) one full score
-        float sc[V];
+        // scores: head_dim/16 MMA steps, B fragments (K rows) two steps per ldmatrix
+        float sd[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            // two accumulators (even and odd k-steps) halve the chain of dependent MMAs
+            float se[4] = {0.f, 0.f, 0.f, 0.f};
+            const int tk = lane & 7;   // the K row (token) this lane addresses for ldmatrix
 #pragma unroll
-        for (int u = 0; u < T; ++u) {
-            float2 kf[P];
-            widen2<EPL>(stage + u * SM::kRow, kf);
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                float2 d = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int e = 0; e < P; ++e) d = ffma2(qf[j][e], kf[e], d);
-                sc[u * G + j] = d.x + d.y;
+            for (int k = 0; k + 1 < KS; k += 2) {
+                const int chunk = 2 * k + (lane >> 3);   // 16-byte chunk: 8 dims each
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(stage + tk * SM::kRow + (((chunk ^ tk) & (HD / 8 - 1)) << 4), b0, b1, b2, b3);
+                mma_bf16_16816(sd, qa[k][0], 0u, qa[k][1], 0u, b0, b1);
+                mma_bf16_16816(se, qa[k + 1][0], 0u, qa[k + 1][1], 0u, b2, b3);
             }
+            sd[0] += se[0];
+            sd[1] += se[1];
         }
-        float red[V];
-#pragma unroll
-        for (int r = 0; r < V; ++r) red[r] = sc[r];
-        constexpr int kSteps = V >= 32 ? 5 : (V >= 16 ? 4 : (V >= 8 ? 3 : (V >= 4 ? 2 : (V >= 2 ? 1 : 0))));
-#pragma unroll
-        for (int k = 0; k < kSteps; ++k) {
-            const int offs = 16 >> k;
-            const int half = V >> (k + 1);
-            const bool upper = (lane & offs) != 0;
-#pragma unroll
-            for (int r = 0; r < half; ++r) {
-                const float send = upper ? red[r] : red[r + half];
-                const float keep = upper ? red[r + half] : red[r];
-                red[r] = keep + __shfl_xor_sync(0xffffffffu, send, offs);
-            }
+        // softmax arithmetic in the lanes of each head (lane 4g + c: tokens 2c, 2c+1)
+        const bool v0 = ((okb >> (2 * cq)) & 1u) != 0;
+        const bool v1 = ((okb >> (2 * cq + 1)) & 1u) != 0;
+        const float s0 = v0 ? sd[0] * p.scale_log2 : -INFINITY;
+        const float s1 = v1 ? sd[1] * p.scale_log2 : -INFINITY;
+        float cm = fmaxf(s0, s1);
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+        const float m_new = fmaxf(m_h, cm);
+        const float p0 = v0 ? exp2_weight(s0 - m_new) : 0.f;
+        const float p1 = v1 ? exp2_weight(s1 - m_new) : 0.f;
+        const float corr = m_new == -INFINITY ? 1.f : exp2_weight(m_h - m_new);
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        l_h = l_h * corr + ps;
+        m_h = m_new;
+        if (gq < G) {
+            s_p[warp][2 * cq][gq] = make_float2(p0, p0);
+            s_p[warp][2 * cq + 1][gq] = make_float2(p1, p1);
+            if (cq == 0) s_c[warp][gq] = make_float2(corr, corr);
         }
-#pragma unroll
-        for (int k = kSteps; k < 5; ++k) red[0] += __shfl_xor_sync(0xffffffffu, red[0], 16 >> k);
-        // After the butterfly, score r = u * G + j sits in the lanes whose bits
-        // 4, 3, ... (from the top) spell r.  The softmax arithmetic runs there,
-        // once per score: the chunk's max per head (over the lanes that differ
-        // in the u bits), the head's new running max, its weight 2^(s - max) and
-        // the rescale factor of the old sums; the weights, maxima and factors
-        // are then broadcast to every lane.
-        constexpr int kLogT = T >= 8 ? 3 : (T >= 4 ? 2 : (T >= 2 ? 1 : 0));
-        const int r_lane = (lane >> (5 - kSteps)) & (V - 1);
-        const int u_lane = r_lane / G;
-        const int j_lane = r_lane - u_lane * G;
-        const bool v_lane = ((okb >> u_lane) & 1u) != 0;
-        const float s_l = v_lane ? red[0] : -INFINITY;
-        float cm = s_l;
-#pragma unroll
-        for (int k = 0; k < kLogT; ++k) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16 >> k));
-        float m_old = m[0];
-#pragma unroll
-        for (int j = 1; j < G; ++j)
-            if (j_lane == j) m_old = m[j];
-        const float m_new = fmaxf(m_old, cm);
-        const float p_l = v_lane ? exp2_weight(s_l - m_new) : 0.f;
-        const float c_l = m_new == -INFINITY ? 1.f : exp2_weight(m_old - m_new);
+        __syncwarp();
+        // output update: rescale, then weight x V row for each token of the chunk
+        const float2 z2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            const int src = j << (5 - kSteps);
-            const float mj = __shfl_sync(0xffffffffu, m_new, src);
-            const float cj = __shfl_sync(0xffffffffu, c_l, src);
-            if (mj > m[j]) {   // the same in every lane
-                l[j] *= cj;
-                const float2 c2 = make_float2(cj, cj);
-                const float2 z2 = make_float2(0.f, 0.f);
+            const float2 c2 = s_c[warp][j];
 #pragma unroll
-                for (int e = 0; e < P; ++e) o[j][e] = ffma2(c2, o[j][e], z2);
-                m[j] = mj;
-            }
+            for (int e = 0; e < P; ++e) o[j][e] = ffma2(c2, o[j][e], z2);
         }
+        const uint8_t* vstage = wring + st * SM::kStage + T * SM::kRow;
 #pragma unroll
         for (int u = 0; u < T; ++u) {
             if (!(okb & (1u << u))) continue;
             float2 vf[P];
-            widen2<EPL>(stage + (T + u) * SM::kRow, vf);
+            widen2<EPL>(vstage + slice_off[u], vf);
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                const float pu = __shfl_sync(0xffffffffu, p_l, (u * G + j) << (5 - kSteps));
-                l[j] += pu;
-                const float2 p2 = make_float2(pu, pu);
+                const float2 p2 = s_p[warp][u][j];
 #pragma unroll
                 for (int e = 0; e < P; ++e) o[j][e] = ffma2(p2, vf[e], o[j][e]);
             }
         }
+        __syncwarp();   // s_p and the stage are free for the next chunk
     }
     cp_async_wait<0>();   // the trailing (empty) groups; the ring is reused below
 
     // combine the warps' states (the ring area now holds the warps' outputs)
     __syncthreads();
     float* s_o = reinterpret_cast<float*>(smem);   // [kAttnWarps][G][HD]
-    if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-            s_m[warp][j] = m[j];
-            s_l[warp][j] = l[j];
-        }
+    if (gq < G && cq == 0) {
+        s_m[warp][gq] = m_h;
+        s_l[warp][gq] = l_h;
     }
 #pragma unroll
     for (int j = 0; j < G; ++j)
@@ -572,6 +593,40 @@ int launch_split(const AttnLaunch& a, const AttnParams& p, cudaStream_t stream, 
     return 0;
 }
 
+// CTAs of the split kernel that fit on one SM (its shared memory and
+// registers), queried once per instance and device.
+template <int HD, int G>
+int split_ctas_per_sm()
+{
+    static std::atomic<int> cached[SmemOptIn::kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= SmemOptIn::kMaxDevices) dev = -1;
+    int n = dev >= 0 ? cached[dev].load(std::memory_order_acquire) : 0;
+    if (n > 0) return n;
+    const int smem = SplitSmem<HD, G>::kBytes;
+    auto kern = attn_split_kernel<HD, G>;
+    static SmemOptIn smem_opt;
+    if (smem_opt.ensure(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kAttnWarps * 32, smem) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return 1;
+    }
+    if (dev >= 0) cached[dev].store(n, std::memory_order_release);
+    return n;
+}
+
+template <int HD>
+int ctas_per_sm_hd(int group)
+{
+    switch (group) {
+    case 1: return split_ctas_per_sm<HD, 1>();
+    case 2: return split_ctas_per_sm<HD, 2>();
+    case 4: return split_ctas_per_sm<HD, 4>();
+    case 8: return split_ctas_per_sm<HD, 8>();
+    default: return 1;
+    }
+}
+
 template <int HD>
 int launch_hd(const AttnLaunch& a, const AttnParams& p, cudaStream_t stream, char* msg, size_t msg_len)
 {
@@ -587,6 +642,16 @@ int launch_hd(const AttnLaunch& a, const AttnParams& p, cudaStream_t stream, cha
 }
 
 }  // namespace
+
+int attention_ctas_per_sm(int head_dim, int q_per_kv)
+{
+    switch (head_dim) {
+    case 64: return ctas_per_sm_hd<64>(q_per_kv);
+    case 128: return ctas_per_sm_hd<128>(q_per_kv);
+    case 256: return ctas_per_sm_hd<256>(q_per_kv);
+    default: return 1;
+    }
+}
 
 int launch_decode_attention(const AttnLaunch& a, cudaStream_t stream, char* msg, size_t msg_len)
 {

@@ -139,6 +139,8 @@ struct AttnLaunch {
     int* status;
 };
 int launch_decode_attention(const AttnLaunch& a, cudaStream_t stream, char* msg, size_t msg_len);
+// CTAs of the attention's split kernel resident per SM for this head shape (>= 1).
+int attention_ctas_per_sm(int head_dim, int q_per_kv);
 
 // Copy an `outer` x `inner` matrix of 16-bit elements (inner contiguous) from
 // leading dimension ld_src to ld_dst.  The source is only read.

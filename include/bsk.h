@@ -177,8 +177,8 @@ int gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, i
  *                [0, max_seq_len]; a sequence of length 0 gives zeros)
  *   out          [num_seqs, num_q_heads, head_dim] BF16 (device)
  *   num_segments segments per sequence, 1..1024 (the page chooses 16, or 32 once
- *                max_seq_len >= 12288, for its 80-CU part); 0 = automatic: about
- *                two CTAs per SM of this GPU, each segment >= 64 tokens
+ *                max_seq_len >= 12288, for its 80-CU part); 0 = automatic: one
+ *                full wave of the split kernel on this GPU, each segment >= 64 tokens
  * head_dim 64, 128 or 256; num_q_heads / num_kv_heads 1, 2, 4 or 8; q, k_cache,
  * v_cache aligned to head_dim/16 bytes.  FP32 accumulation, output rounded to
  * nearest even.  A workspace of num_seqs * num_q_heads * segments *

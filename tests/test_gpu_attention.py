@@ -1,11 +1,13 @@
 """GPU parity of decode_attention_bf16 (split-KV decode attention over a paged
 BF16 cache) against the oracle, through the C ABI.
 
-Tolerance, derived from FP32 arithmetic on BF16 inputs: a score carries at most
-head_dim * 2^-24 * scale * sum|q_e k_e| of accumulation error, which perturbs each
-softmax weight by that much relatively (in base e); the output, a weighted mean
-of V rows, then moves by at most twice that times max|v|, plus the FP32
-accumulation over the tokens and one BF16 rounding:
+Tolerance, derived from FP32 arithmetic on BF16 inputs: a score is a sum of
+head_dim exact products formed by the tensor cores, whose FP32 additions need
+not round to nearest, so it carries at most head_dim * 2^-23 * scale *
+sum|q_e k_e| of accumulation error (one ulp per addition), plus 2^-21 for the
+hardware exp2; that perturbs each softmax weight by that much relatively; the
+output, a weighted mean of V rows, then moves by at most twice that times
+max|v|, plus the FP32 accumulation over the tokens and one BF16 rounding:
     |out - exact| <= (2 * eps_w + n_tok * 2^-24) * max|v| + ulp_bf16 / 2,
 with eps_w the worst weight error over the tokens of the call.
 """
@@ -78,7 +80,7 @@ def check(got, ref, q, k, v, hd, scale, n_tok, label):
     vmax = float(np.max(np.abs(oracle.bf16_decode(v))))
     # worst |scale * sum q_e k_e| bound: head_dim * max|q| * max|k| * scale
     sum_abs = hd * float(qv.max()) * float(kv.max()) * abs(scale)
-    eps_w = hd * 2.0 ** -24 * sum_abs + 2.0 ** -21          # + the hardware exp2 approximation
+    eps_w = hd * 2.0 ** -23 * sum_abs + 2.0 ** -21          # tensor-core sums; + the hardware exp2
     bound = (2 * eps_w + n_tok * 2.0 ** -24) * vmax + 0.5 * ulp(np.maximum(np.abs(gv), np.abs(rv)), "bf16")
     err = np.abs(gv - rv)
     worst = int(np.argmax(err - bound))

@@ -129,7 +129,7 @@ def test_attention_cache_past_2_31_elements():
     vmax = float(np.max(np.abs(oracle.bf16_decode(v_small))))
     sum_abs = hd * float(np.max(np.abs(oracle.bf16_decode(q)))) * float(np.max(np.abs(oracle.bf16_decode(k_small)))) \
         * scale
-    eps_w = hd * 2.0 ** -24 * sum_abs + 2.0 ** -21
+    eps_w = hd * 2.0 ** -23 * sum_abs + 2.0 ** -21
     bound = (2 * eps_w + L * 2.0 ** -24) * vmax + 2.0 ** -8 * np.maximum(np.abs(got), np.abs(ref.reshape(-1)))
     assert np.all(err <= bound), f"max err {err.max():.3g}"
     del kd, vd
