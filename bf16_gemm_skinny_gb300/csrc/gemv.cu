@@ -1,4 +1,5 @@
-// gemv.cu -- decode GEMV / skinny GEMM on the CUDA cores: y = x W^T, n <= 8 tokens.
+// gemv.cu -- decode GEMV / skinny GEMM on the CUDA cores: y = x W^T, n <= 8 tokens
+// (by default gemv_bf16 runs n <= 2 here and larger n on the tensor cores).
 //
 // DCU decode-GEMV article (forum.sourcefind.cn): section 6.1 fixes the shapes
 // (X:[n,k], W:[m,k], Y:[n,m], all row-major) and section 6.2 the work split:
