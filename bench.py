@@ -36,6 +36,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -150,8 +151,9 @@ KERNEL_SOURCES = {
 
 
 def source_digest(kernel: str) -> str:
-    """Hash of one kernel's device code; a committed traffic figure is only
-    reported while that code is unchanged since it was measured."""
+    """Hash of one kernel's device code (comments and whitespace left out); a
+    committed traffic figure is only reported while that code is unchanged
+    since it was measured."""
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "bf16_gemm_skinny_gb300", "csrc")
     for name, host_start in KERNEL_SOURCES[kernel]:
@@ -162,7 +164,11 @@ def source_digest(kernel: str) -> str:
             if cut < 0:
                 raise RuntimeError(f"{name}: host-code marker {host_start!r} not found")
             text = text[:cut]
-        h.update(name.encode() + b"\0" + text)
+        # comments and layout do not change the kernel
+        code = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+        code = re.sub(rb"//[^\n]*", b"", code)
+        code = b" ".join(code.split())
+        h.update(name.encode() + b"\0" + code)
     return h.hexdigest()[:16]
 
 
