@@ -94,56 +94,66 @@ struct Params {
     const uint16_t* bias;   // optional, output precision: bias[m] (mode 1) or bias[n] (mode 2)
     int bias_mode;
     float alpha;            // FP8 inputs: scale of the FP32 accumulator
-    // Stream-K schedule (one-CTA-per-tile kernel only): CTA c of the grid takes
-    // iterations [c*I/G, (c+1)*I/G) of the I = num_tiles * num_kb (tile, k-block)
-    // iterations in tile order.  A tile split between CTAs is finished by the CTA
-    // that holds its first k-block; the others leave FP32 partials in their slot.
-    int sk;                 // 1: stream-K, 0: whole tiles, blockIdx.x + j * gridDim.x
-    long long sk_iters;     // num_tiles * num_kb
-    float* sk_part;         // [gridDim.x][BN][128]: column-major partial tile per CTA
+    // Stream-K schedule: the first sk_dp_tiles tiles (whole waves) go to the
+    // units (CTAs, or CTA pairs) whole, unit + j * G, so that the tiles in flight
+    // together stay neighbours in the GROUP_M order; the remaining tiles'
+    // I = (num_tiles - sk_dp_tiles) * num_kb (tile, k-block) iterations are then
+    // shared out: unit c of G takes [c*I/G, (c+1)*I/G) in tile order.  A tile
+    // split between units is finished by the unit that holds its first
+    // k-block; the others leave FP32 partials in their slots (one per CTA).
+    int sk;                 // 1: stream-K, 0: whole tiles, unit + j * units
+    int sk_dp_tiles;        // tiles handed out whole first (a multiple of the unit count)
+    long long sk_iters;     // (num_tiles - sk_dp_tiles) * num_kb
+    float* sk_part;         // [gridDim.x][tile width][128]: a CTA's 128 rows of a tile, column-major
     int* sk_flag;           // [gridDim.x], zero at launch: set once a CTA's slot is written
     int* status;
     unsigned long long wait_limit_ns;
 };
 
-// A CTA's work as a sequence of segments (tile, k-blocks [kb0, kb1)).
+// The work of one unit (a CTA, or a CTA pair) of `units` as a sequence of
+// segments (tile, k-blocks [kb0, kb1)).
 struct SegCursor {
-    long long pos, end;
+    long long tile;       // whole-tile phase: next tile (step `step`) while < dp_end
+    long long dp_end;
+    long long pos, end;   // shared phase: iteration range, counted from the first shared tile
+    int step;
 };
 
-__device__ __forceinline__ SegCursor seg_first(const Params& p)
+__device__ __forceinline__ SegCursor seg_first(const Params& p, int unit, int units)
 {
     if (p.sk) {
-        const long long g = gridDim.x;
-        return {static_cast<long long>(blockIdx.x) * p.sk_iters / g,
-                static_cast<long long>(blockIdx.x + 1) * p.sk_iters / g};
+        return {static_cast<long long>(unit), static_cast<long long>(p.sk_dp_tiles),
+                static_cast<long long>(unit) * p.sk_iters / units,
+                static_cast<long long>(unit + 1) * p.sk_iters / units, units};
     }
-    return {static_cast<long long>(blockIdx.x), static_cast<long long>(p.num_tiles)};
+    return {static_cast<long long>(unit), static_cast<long long>(p.num_tiles), 0, 0, units};
 }
 
 __device__ __forceinline__ bool seg_next(const Params& p, SegCursor& c, int& tile, int& kb0, int& kb1)
 {
-    if (c.pos >= c.end) return false;
-    if (!p.sk) {
-        tile = static_cast<int>(c.pos);
+    if (c.tile < c.dp_end) {
+        tile = static_cast<int>(c.tile);
         kb0 = 0;
         kb1 = p.num_kb;
-        c.pos += gridDim.x;
+        c.tile += c.step;
         return true;
     }
-    tile = static_cast<int>(c.pos / p.num_kb);
-    const long long t0 = static_cast<long long>(tile) * p.num_kb;
+    if (c.pos >= c.end) return false;
+    const int rel = static_cast<int>(c.pos / p.num_kb);
+    const long long t0 = static_cast<long long>(rel) * p.num_kb;
     const long long e = c.end < t0 + p.num_kb ? c.end : t0 + p.num_kb;
+    tile = p.sk_dp_tiles + rel;
     kb0 = static_cast<int>(c.pos - t0);
     kb1 = static_cast<int>(e - t0);
     c.pos = e;
     return true;
 }
 
-// The CTA whose stream-K share holds iteration i: the largest c with c*I/G <= i.
-__device__ __forceinline__ int sk_cta_of(const Params& p, long long i)
+// The unit whose stream-K share holds iteration i of the shared phase: the
+// largest c with c*I/G <= i.
+__device__ __forceinline__ int sk_unit_of(const Params& p, long long i, int units)
 {
-    return static_cast<int>(((i + 1) * static_cast<long long>(gridDim.x) + p.sk_iters - 1) / p.sk_iters) - 1;
+    return static_cast<int>(((i + 1) * static_cast<long long>(units) + p.sk_iters - 1) / p.sk_iters) - 1;
 }
 
 // Identifiers of the waits, reported in the status word on a timeout.
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            SegCursor cur = seg_first(p);
+            SegCursor cur = seg_first(p, blockIdx.x, gridDim.x);
             int tile, kb0, kb1;
             while (ok && seg_next(p, cur, tile, kb0, kb1)) {
                 int pm, pn;
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             bool issued_any = false;
-            SegCursor cur = seg_first(p);
+            SegCursor cur = seg_first(p, blockIdx.x, gridDim.x);
             int tile, kb0, kb1;
             for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
                 const int acc = it & 1;
@@ -438,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;             // TMEM lanes this warp may read
         const int ew = warp - 2;                  // owner of a staging buffer pair
         uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
-        SegCursor cur = seg_first(p);
+        SegCursor cur = seg_first(p, blockIdx.x, gridDim.x);
         int tile, kb0, kb1;
         for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
             const int acc = it & 1;
@@ -459,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool to_slot = p.sk && kb0 != 0;
             int q_last = static_cast<int>(blockIdx.x);
             if (p.sk && kb0 == 0 && kb1 != p.num_kb) {
-                q_last = sk_cta_of(p, static_cast<long long>(tile + 1) * p.num_kb - 1);
+                q_last = sk_unit_of(p, static_cast<long long>(tile - p.sk_dp_tiles + 1) * p.num_kb - 1, gridDim.x);
                 bool fok = true;
                 for (int q = static_cast<int>(blockIdx.x) + 1; fok && q <= q_last; ++q)
                     fok = flag_wait_acquire(p.sk_flag + q, wc, kSiteStreamKPartial);
@@ -634,12 +644,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
+            SegCursor cur = seg_first(p, pair, num_pairs);
+            int tile, kb0, kb1;
+            while (ok && seg_next(p, cur, tile, kb0, kb1)) {
                 int pm, pn;
                 tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
                 const int m0 = pm * T + static_cast<int>(rank) * kBM;
                 const int n0 = pn * T + static_cast<int>(rank) * kBM;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -689,8 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             bool issued_any = false;
-            int it = 0;
-            for (int tile = pair; tile < p.num_tiles; tile += num_pairs, ++it) {
+            SegCursor cur = seg_first(p, pair, num_pairs);
+            int tile, kb0, kb1;
+            for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
                 const int acc = it & 1;
                 const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
                 if (!mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
@@ -699,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * T);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
                         ok = false;
                         break;
@@ -713,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  : smem_desc_sw128(a_base + kk * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
                                                  : smem_desc_sw128(b_base + kk * 32, 16, 1024);
-                        mma_issue_pair<Ty::kFp8>(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        mma_issue_pair<Ty::kFp8>(d_tmem, ad, bd, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     mma_commit_pair_multicast(empty0 + 8 * stage, 0x3);
                     issued_any = true;
@@ -738,8 +751,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int ew = warp - 2;
         uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
-        int it = 0;
-        for (int tile = pair; tile < p.num_tiles; tile += num_pairs, ++it) {
+        SegCursor cur = seg_first(p, pair, num_pairs);
+        int tile, kb0, kb1;
+        for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
             const int acc = it & 1;
             const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
             bool ok = mbar_wait(tfull0 + 8 * acc, aph, wc, kSiteEpilogueTmemFull);
@@ -752,6 +766,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n0 = pn * T;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * T);
+            // Stream-K roles, as in the one-CTA kernel; slots and flags are per CTA
+            // (pair * 2 + rank), each holding this CTA's 128 rows of the tile.
+            const bool to_slot = p.sk && kb0 != 0;
+            const int my_slot = pair * 2 + static_cast<int>(rank);
+            int q_last = pair;
+            if (p.sk && kb0 == 0 && kb1 != p.num_kb) {
+                q_last = sk_unit_of(p, static_cast<long long>(tile - p.sk_dp_tiles + 1) * p.num_kb - 1, num_pairs);
+                bool fok = true;
+                for (int q = pair + 1; fok && q <= q_last; ++q)
+                    fok = flag_wait_acquire(p.sk_flag + q * 2 + static_cast<int>(rank), wc, kSiteStreamKPartial);
+                (void)__all_sync(0xffffffffu, fok);   // on a timeout the status word is set; the output is undefined
+            }
 #pragma unroll 1
             for (int c = 0; c < T / 32; ++c) {
                 uint32_t r[32];
@@ -761,6 +787,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_remote(leader_tempty0 + 8 * acc);
+                }
+                const long long slot_col = static_cast<long long>(c * 32) * kBM + quarter * 32 + lane;
+                if (to_slot) {
+                    float* ps = p.sk_part + static_cast<long long>(my_slot) * T * kBM + slot_col;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ps[j * kBM] = __uint_as_float(r[j]);
+                    continue;
+                }
+                for (int q = pair + 1; q <= q_last; ++q) {
+                    const float* pq = p.sk_part + static_cast<long long>(q * 2 + static_cast<int>(rank)) * T * kBM + slot_col;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + pq[j * kBM]);
                 }
                 finish_acc<IN, OUT>(r, p, m0 + lane, n0 + c * 32);
                 if (Ty::kOutBytes == 2 && p.tma_store) {
@@ -779,6 +817,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     store_row<OUT>(r, p, m0 + lane, n0 + c * 32);
                 }
+            }
+            if (to_slot) {
+                __threadfence();
+                asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+                if (warp == 2 && lane == 0) flag_set_release(p.sk_flag + my_slot);
             }
         }
         if (lane == 0) bulk_wait_group<0>();
@@ -893,6 +936,7 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     }
     int grid = 0;
     p.sk = 0;
+    p.sk_dp_tiles = 0;
     p.sk_iters = 0;
     p.sk_part = nullptr;
     p.sk_flag = nullptr;
@@ -901,8 +945,10 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
         // of a split tile wait on one another, so they must all be resident: the
         // launch is cooperative (it fails rather than run them in waves).
         p.sk = 1;
-        p.sk_iters = static_cast<long long>(p.num_tiles) * p.num_kb;
         grid = g.num_sms;
+        p.sk_dp_tiles = (p.num_tiles / grid) * grid;
+        if (p.sk_dp_tiles == p.num_tiles) p.sk_dp_tiles -= grid;   // keep one wave to share
+        p.sk_iters = static_cast<long long>(p.num_tiles - p.sk_dp_tiles) * p.num_kb;
         if (grid > p.sk_iters) grid = static_cast<int>(p.sk_iters);
         p.sk_part = g.sk_part;
         p.sk_flag = g.sk_flag;
@@ -959,6 +1005,7 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.bias_mode = g.bias != nullptr ? g.bias_mode : 0;
     p.alpha = g.alpha;
     p.sk = 0;
+    p.sk_dp_tiles = 0;
     p.sk_iters = 0;
     p.sk_part = nullptr;
     p.sk_flag = nullptr;
@@ -1000,6 +1047,31 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     }
     if (clusters > g.num_sms / 2) clusters = g.num_sms / 2;
     if (clusters < 1) clusters = 1;
+    if (g.stream_k && g.sk_part != nullptr && g.sk_flag != nullptr) {
+        // Every co-resident pair takes an equal share of the (tile, k-block)
+        // iterations; pairs wait on one another, so the launch is cooperative.
+        p.sk = 1;
+        p.sk_dp_tiles = (p.num_tiles / clusters) * clusters;
+        if (p.sk_dp_tiles == p.num_tiles) p.sk_dp_tiles -= clusters;   // keep one wave to share
+        p.sk_iters = static_cast<long long>(p.num_tiles - p.sk_dp_tiles) * p.num_kb;
+        const int pairs = static_cast<long long>(clusters) < p.sk_iters ? clusters : static_cast<int>(p.sk_iters);
+        p.sk_part = g.sk_part;
+        p.sk_flag = g.sk_flag;
+        cudaLaunchAttribute attr2[2];
+        attr2[0] = attr[0];
+        attr2[1].id = cudaLaunchAttributeCooperative;
+        attr2[1].val.cooperative = 1;
+        cfg.attrs = attr2;
+        cfg.numAttrs = 2;
+        cfg.gridDim = dim3(2 * pairs, 1, 1);
+        e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "GEMM (CTA pair, stream-K) launch failed: %s", cudaGetErrorString(e));
+            return 1;
+        }
+        return 0;
+    }
     const int per_pair = (p.num_tiles + clusters - 1) / clusters;
     const int pairs = (p.num_tiles + per_pair - 1) / per_pair;
     cfg.gridDim = dim3(2 * pairs, 1, 1);

@@ -264,3 +264,24 @@ def test_stream_k_schedule(M, N, K, block_n, sms):
             bsk.set_option(k, 0)
     ref, _ = oracle.gemm_f16_colmajor(Ar, Br, M, N, K)
     check_tolerance(got, ref, "f16", K, absmax_f16(Ar), absmax_f16(Br), f"stream-K {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,sms", [(1000, 777, 1030, 0), (4095, 4097, 4100, 0), (300, 517, 2048, 9),
+                                       (2048, 1024, 8192, 0)])
+def test_stream_k_on_cta_pairs(M, N, K, sms):
+    """Stream-K on the CTA-pair kernel (forced): integer inputs give the oracle's
+    bits; the column-major result repeats bit for bit."""
+    A, B = operands(M, N, K, "int2")
+    opts = {"stream_k": 2, "num_sms": sms}
+    for k, v in opts.items():
+        bsk.set_option(k, v)
+    try:
+        got = run(A, B, M, N, K)
+        again = run(A, B, M, N, K)
+    finally:
+        for k in opts:
+            bsk.set_option(k, 0)
+    assert np.array_equal(got, again)
+    cols = sorted({0, 1, 255, 256, N // 2, N - 1})
+    rows = sorted({0, 127, 128, M // 2, M - 1})
+    sampled_check(got, A, B, M, N, K, cols, rows, True)

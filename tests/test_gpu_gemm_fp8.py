@@ -268,3 +268,16 @@ def test_stream_k_schedule(M, N, K, stream_k):
     cols = sorted({0, N // 2, N - 1})
     _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", "f32", cols=cols)
     assert np.array_equal(got[:, cols], bits)
+
+
+def test_stream_k_on_cta_pairs():
+    """FP8 on CTA pairs with stream-K forced: integer inputs, the oracle's bits."""
+    M, N, K = 1000, 777, 4096
+    A2, B2 = operands(M, N, K, "int2", "e4m3")
+    bsk.set_option("stream_k", 2)
+    try:
+        got, Af, lda, Bf, ldb = run(A2, B2, "e4m3", "bf16")
+    finally:
+        bsk.set_option("stream_k", 0)
+    _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", "bf16")
+    assert np.array_equal(got, bits)
