@@ -254,17 +254,14 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
         const long long tiles = m_tiles * ((op.N + block_n - 1LL) / block_n);
         stream_k = sk_opt == 2 || (fill(tiles, sms) < 0.75 && kbs >= 32);
     } else if (pair && sk_opt != 1) {
-        // CTA pairs: whole waves first, the last (partial) wave shared, only for
-        // deep K.  The pair kernel runs under the power cap, so idle SMs in a
-        // partial wave cost little; interleaved A/B on GB300 (stream-K time over
-        // whole-tile time): 8192^2 x 16384 0.987, 4096^2 x 16384 0.944, but at
-        // K = 8192 or less 0.99 - 1.025 (8192 x 8192, 4096 x 4096, 6144 x 6144,
-        // 4096 x 8192), the ragged 4095 x 4097 x 4100 1.06 and 4096 x 1024 x 4096
-        // 1.43 (fixed costs).
-        const long long pairs = sms / 2 > 0 ? sms / 2 : 1;
-        const long long pair_tiles = ((op.M + 255LL) / 256) * ((op.N + 255LL) / 256);
-        const double flops = 2.0 * op.M * static_cast<double>(op.N) * op.K;
-        stream_k = sk_opt == 2 || (fill(pair_tiles, pairs) < 0.98 && kbs >= 256 && flops >= 2.5e11);
+        // CTA pairs: whole waves first, the last (partial) wave shared -- on
+        // request only.  The pair kernel runs under the power cap, so idle SMs in
+        // a partial wave cost little; interleaved A/B on GB300 (stream-K time over
+        // whole-tile time): 8192^2 x 16384 0.987, 4096^2 x 16384 0.944, at
+        // K = 8192 or less 0.99 - 1.025, the ragged 4095 x 4097 x 4100 1.06 and
+        // 4096 x 1024 x 4096 1.43 (fixed costs); inside a benchmark step of
+        // GEMM + GEMVs the 8192^2 x 16384 gain did not show.
+        stream_k = sk_opt == 2;
     }
     // one slot per CTA: block_n x 128 FP32 (CTA pairs: each CTA's 128 rows of a 256-wide tile)
     const size_t sk_part_bytes = stream_k ? static_cast<size_t>(sms) * block_n * 128 * sizeof(float) : 0;
