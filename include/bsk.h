@@ -278,11 +278,13 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *                            tensor-core skinny GEMM (default: 1 for n <= 2, 5 for
  *                            n >= 3; a CUDA-core kernel whose buffers do not fit in
  *                            shared memory falls back to another)
- *   BSK_OPT_STREAM_K         schedule of the one-CTA-per-tile GEMM kernel: 1 whole tiles,
- *                            2 stream-K (every SM an equal share of the tile x k-block
- *                            iterations; split tiles are summed in FP32 by the CTA that
- *                            holds their first k-block), 0 automatic: stream-K when whole
- *                            tiles would leave the last wave under 90% full
+ *   BSK_OPT_STREAM_K         GEMM schedule: 1 whole tiles, 2 stream-K (every SM -- or CTA
+ *                            pair -- an equal share of the tile x k-block iterations of the
+ *                            last wave; split tiles are summed in FP32 by the unit that
+ *                            holds their first k-block), 0 automatic: stream-K on the
+ *                            one-CTA-per-tile kernel when whole tiles would fill under three
+ *                            quarters of the SMs and a tile has at least 32 k-blocks; whole
+ *                            tiles on CTA pairs
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
