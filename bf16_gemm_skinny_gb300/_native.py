@@ -39,6 +39,7 @@ OPTIONS = {
     "gemv_kernel": 9,
     "gemm_kernel": 10,
     "stream_k": 11,
+    "pdl": 12,
 }
 
 # Every symbol include/bsk.h declares.

@@ -44,7 +44,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 12;
+constexpr int kNumOpts = 13;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -328,6 +328,7 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     g.num_sms = sms;
     g.status = g_status_dev;
     g.wait_limit_ns = static_cast<unsigned long long>(opt_or(BSK_OPT_WAIT_LIMIT_US, kDefaultWaitLimitUs)) * 1000ull;
+    g.pdl = opt_or(BSK_OPT_PDL, 0) != 1;
     if (bsk::launch_gemm(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
     return BSK_OK;
 }
@@ -503,6 +504,7 @@ int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, 
         g.warps_per_block = static_cast<int>(opt_or(BSK_OPT_GEMV_WARPS, 0));
         g.kernel = static_cast<int>(opt_or(BSK_OPT_GEMV_KERNEL, 0));
         g.num_sms = sms;
+        g.pdl = opt_or(BSK_OPT_PDL, 0) != 1;
         char msg[512] = "";
         if (bsk::launch_gemv(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
         return BSK_OK;
@@ -763,6 +765,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_GEMV_KERNEL: ok = value >= 0 && value <= 5; break;
     case BSK_OPT_GEMM_KERNEL: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_STREAM_K: ok = value >= 0 && value <= 2; break;
+    case BSK_OPT_PDL: ok = value == 0 || value == 1; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

@@ -35,6 +35,35 @@ __host__ __device__ inline void tile_coord(int t, int num_m, int num_n, int grou
     *pid_n = r / group_rows;
 }
 
+// Launches `kern` on `stream`; with `pdl` set, as a programmatic dependent of
+// the kernel before it in the stream: its CTAs may be scheduled while that
+// kernel's last CTAs still run, so the kernel must execute griddepcontrol.wait
+// before it reads or writes any memory an earlier stream operation may touch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          Args&&... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// Waits until the grids this one depends on programmatically have completed and
+// their memory operations are visible (returns at once without such grids).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next programmatic dependent in the stream be scheduled now; it still
+// waits for this grid's completion in its own griddep_wait().
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 using TmapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -102,6 +131,7 @@ struct GemmLaunch {
     int* sk_flag = nullptr;    // stream-K: num_sms ints, zero before the launch
     int* status = nullptr;   // device status word
     unsigned long long wait_limit_ns = 2000000000ull;
+    bool pdl = true;         // whole-tile launches: programmatic dependent of the previous kernel
 };
 
 // Returns 0 on success; otherwise an error message is written to `msg`.
@@ -121,6 +151,7 @@ struct GemvLaunch {
     int kernel;           // 0 = auto, 1 = register streaming, 2/3 = cp.async-pipelined (x FP32 / BF16),
                           // 4 = token-paired accumulators
     int num_sms;
+    bool pdl;             // programmatic dependent of the previous kernel in the stream
 };
 int launch_gemv(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
 

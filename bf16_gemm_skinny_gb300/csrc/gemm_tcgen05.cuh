@@ -314,6 +314,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         if (p.tma_store) prefetch_tmap(&tmC);
+        if (p.sk == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
+            // The first tile's first stages into L2 while the kernel before this
+            // one may still be running (a prefetch is coherent: nothing reaches
+            // shared memory before griddep_wait below).
+            int pm, pn;
+            tile_coord(static_cast<int>(blockIdx.x), p.num_m, p.num_n, p.group_m, &pm, &pn);
+            const int kbs = p.num_kb < S ? p.num_kb : S;
+            for (int kb = 0; kb < kbs; ++kb) {
+                const int k0 = kb * Ty::kBK;
+                if constexpr (A_MN) {
+                    tma_prefetch_l2_2d(&tmA, pm * kBM, k0);
+                    tma_prefetch_l2_2d(&tmA, pm * kBM + 64, k0);
+                } else {
+                    tma_prefetch_l2_2d(&tmA, k0, pm * kBM);
+                }
+                if constexpr (B_MN) {
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j) tma_prefetch_l2_2d(&tmB, pn * BN + 64 * j, k0);
+                } else {
+                    tma_prefetch_l2_2d(&tmB, k0, pn * BN);
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), Cf::kTmemCols);
@@ -323,6 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // The prologue touched only shared memory, TMEM and the parameters; global
+    // memory is read and written only once the kernel before this one in the
+    // stream has completed (a no-op unless launched as its dependent).
+    griddep_wait();
+    griddep_launch_dependents();
     const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
     // Waits on the abort path ignore the abort flag but keep the time limit.
     uint32_t never = 0u;
@@ -629,6 +657,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // The prologue touched only shared memory, TMEM and the parameters; global
+    // memory is read and written only once the kernel before this one in the
+    // stream has completed (a no-op unless launched as its dependent).
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t leader_full0 = mapa_shared(full0, 0);
     const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
     const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
@@ -973,8 +1006,8 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     // Every CTA gets the same number of tiles (the last wave is not left partial).
     const int per_cta = (p.num_tiles + g.num_sms - 1) / g.num_sms;
     grid = (p.num_tiles + per_cta - 1) / per_cta;
-    kern<<<grid, kThreads, Cf::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
-    e = cudaGetLastError();
+    e = launch_kernel(kern, dim3(grid), dim3(kThreads), Cf::kSmemBytes, stream, g.pdl, tmA, tmB, tmC, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "GEMM launch failed: %s", cudaGetErrorString(e));
         return 1;
@@ -1075,6 +1108,12 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     const int per_pair = (p.num_tiles + clusters - 1) / clusters;
     const int pairs = (p.num_tiles + per_pair - 1) / per_pair;
     cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cudaLaunchAttribute attr_pdl[2];
+    attr_pdl[0] = attr[0];
+    attr_pdl[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr_pdl[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr_pdl;
+    cfg.numAttrs = g.pdl ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -40,6 +40,11 @@ __device__ __forceinline__ uint4 ld_stream_16B(const uint4* p)
     return v;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // bf16 pair in one 32-bit word -> the two FP32 values (element 0 = low half).
 // A bfloat16 is the upper half of a binary32, so each value is a byte
 // permutation with zero low bytes (prmt keeps this on the integer pipe).
@@ -150,6 +155,23 @@ __global__ void __launch_bounds__(256)
     const int warps = blockDim.x >> 5;
     const int num_groups = (M + R - 1) / R;
     const bool single_slab = slab8 >= K8;
+
+    // Until griddep_wait() the kernel before this one in the stream may still be
+    // running: only L2 prefetches of this warp's first W chunks (coherent, they
+    // deliver nothing to the thread) go out before it.
+    {
+        const int g0 = blockIdx.x * warps + (threadIdx.x >> 5);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = lane + 32 * u;
+                if (g0 < num_groups && g0 * R + r < M && c < K8)
+                    prefetch_l2(W4 + static_cast<long long>(g0 * R + r) * K8 + c);
+            }
+    }
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (single_slab) {
         stage_x<NT>(x4, K8, 0, K8, xs4, slab8);
@@ -304,6 +326,8 @@ __global__ void __launch_bounds__(512, 1)
     uint4* ring = smem4 + x_words + warp * D * R * 32;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + lane * 16u;
 
+    griddep_wait();
+    griddep_launch_dependents();
     stage_x_whole<NT, XF32>(x4, K8, xs4);
     __syncthreads();
 
@@ -484,6 +508,8 @@ __global__ void __launch_bounds__(512, 1)
     uint4* ring = smem4 + K8 * 8 + warp * D * R * 32;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + lane * 16u;
 
+    griddep_wait();
+    griddep_launch_dependents();
     stage_x_token_interleaved<NT>(x, K, K8, xs4);
     __syncthreads();
 
@@ -600,6 +626,8 @@ __global__ void __launch_bounds__(256)
     const int lane = threadIdx.x & 31;
     const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    griddep_wait();
+    griddep_launch_dependents();
     for (long long j = warp0; j < M; j += nwarps) {
         float acc[NT];
 #pragma unroll
@@ -649,10 +677,10 @@ int launch_vec(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_l
     long long grid = static_cast<long long>(g.num_sms) * per_sm;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
-    kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(
-        reinterpret_cast<const uint4*>(g.W), reinterpret_cast<const uint4*>(g.x),
-        reinterpret_cast<__nv_bfloat16*>(g.y), g.M, K8, static_cast<int>(slab8));
-    e = cudaGetLastError();
+    e = launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, g.pdl,
+                      reinterpret_cast<const uint4*>(g.W), reinterpret_cast<const uint4*>(g.x),
+                      reinterpret_cast<__nv_bfloat16*>(g.y), g.M, K8, static_cast<int>(slab8));
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "GEMV launch failed: %s", cudaGetErrorString(e));
         return 1;
@@ -668,9 +696,9 @@ int launch_scalar(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t ms
     const long long cap = static_cast<long long>(g.num_sms) * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    gemv_bf16_scalar_kernel<NT><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-        g.W, g.x, reinterpret_cast<__nv_bfloat16*>(g.y), g.M, g.K);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(gemv_bf16_scalar_kernel<NT>, dim3(static_cast<unsigned>(grid)), dim3(threads), 0,
+                                  stream, g.pdl, g.W, g.x, reinterpret_cast<__nv_bfloat16*>(g.y), g.M, g.K);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "GEMV launch failed: %s", cudaGetErrorString(e));
         return 1;
@@ -742,10 +770,10 @@ int try_launch_pipe(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t 
     const long long per_warp = (groups + max_warps - 1) / max_warps;
     const long long warps_needed = (groups + per_warp - 1) / per_warp;
     const long long grid = (warps_needed + warps - 1) / warps;
-    kern<<<static_cast<unsigned>(grid), warps * 32, smem, stream>>>(
-        reinterpret_cast<const uint4*>(g.W), reinterpret_cast<const uint4*>(g.x),
-        reinterpret_cast<__nv_bfloat16*>(g.y), g.M, K8, static_cast<int>(per_warp));
-    e = cudaGetLastError();
+    e = launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(warps * 32), static_cast<size_t>(smem), stream,
+                      g.pdl, reinterpret_cast<const uint4*>(g.W), reinterpret_cast<const uint4*>(g.x),
+                      reinterpret_cast<__nv_bfloat16*>(g.y), g.M, K8, static_cast<int>(per_warp));
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "GEMV launch failed: %s", cudaGetErrorString(e));
         *status = 1;
@@ -805,10 +833,10 @@ int try_launch_tokpair(const GemvLaunch& g, cudaStream_t stream, char* msg, size
     const long long per_warp = (groups + max_warps - 1) / max_warps;
     const long long warps_needed = (groups + per_warp - 1) / per_warp;
     const long long grid = (warps_needed + warps - 1) / warps;
-    kern<<<static_cast<unsigned>(grid), warps * 32, smem, stream>>>(
-        reinterpret_cast<const uint4*>(g.W), g.x, reinterpret_cast<__nv_bfloat16*>(g.y), g.M, g.K,
-        static_cast<int>(per_warp));
-    e = cudaGetLastError();
+    e = launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(warps * 32), static_cast<size_t>(smem), stream,
+                      g.pdl, reinterpret_cast<const uint4*>(g.W), g.x, reinterpret_cast<__nv_bfloat16*>(g.y), g.M,
+                      g.K, static_cast<int>(per_warp));
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "GEMV launch failed: %s", cudaGetErrorString(e));
         *status = 1;

@@ -194,6 +194,16 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Prefetch of the box at (x, y) into L2 (no shared memory, no completion signal;
+// coherent with any writes that reach L2 later).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled load of the box at coordinates (x, y) (x = innermost) into shared
 // memory at `dst`; completion is signalled on mbarrier `bar` as transaction bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y)

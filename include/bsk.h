@@ -285,6 +285,12 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *                            one-CTA-per-tile kernel when whole tiles would fill under three
  *                            quarters of the SMs and a tile has at least 32 k-blocks; whole
  *                            tiles on CTA pairs
+ *   BSK_OPT_PDL              1: launch the GEMM and GEMV kernels in plain stream order;
+ *                            0 (default): as programmatic dependents of the kernel before
+ *                            them in the stream, so that their prologue (barrier set-up,
+ *                            TMEM allocation, L2 prefetch of the first weight tiles)
+ *                            overlaps that kernel's last CTAs.  Either way no input is read
+ *                            and no output written before the earlier kernel has completed.
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
@@ -298,7 +304,8 @@ enum {
     BSK_OPT_NUM_SMS = 8,
     BSK_OPT_GEMV_KERNEL = 9,
     BSK_OPT_GEMM_KERNEL = 10,
-    BSK_OPT_STREAM_K = 11
+    BSK_OPT_STREAM_K = 11,
+    BSK_OPT_PDL = 12
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);
