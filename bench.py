@@ -4,16 +4,20 @@ the 34816x5120 BF16 decode GEMV (n = 1, 4, 8), on one GB300 per process.
 
 One step = one pass of the whole path on one batch of synthetic input:
     gemm_f16_colmajor(A, B, C, 8192, 8192, 16384)
-    gemv_bf16(W_i, x_n, y_n, 34816, 5120, n)   for n in (1, 4, 8)
-(each GEMV reads its own copy W_i of the weights, so no call finds W in L2;
-the GEMM's operands, 537 MB, are larger than L2 too).  W = warm-up steps are
-run first, then exactly K steps are timed with CUDA events on the launching
+    gemv_bf16(W_i, x_n, y_n, 34816, 5120, n)   4 times back to back, for n in (1, 4, 8)
+(three copies W_i of the weights rotate, so no GEMV launch finds W in L2; the
+GEMM's operands, 537 MB, are larger than L2 too).  W = warm-up steps are run
+first, then exactly K steps are timed with CUDA events on the launching
 stream, bracketed by a barrier and a device synchronize.
 
 Reported (one JSON line, rank 0):
   value      GEMM TFLOP/s: 2*M*N*K / mean GEMM kernel time (events around
              each GEMM launch), times the number of ranks (replicas).
-  gemv       the GEMV's HBM GB/s per n (algorithmic bytes / kernel time).
+  gemv       the GEMV's HBM GB/s per n: algorithmic bytes / average launch
+             time over each chain of 4 launches (events at the chain's ends,
+             as in a decode loop); single_launch_us is one launch after the
+             GEMM with events on both sides (which stops the overlap of the
+             launch with the kernel before it).
   e2e        the same metrics through the blocking C-ABI calls with pinned
              host buffers: H2D of the step's inputs + call + D2H of the result.
   roofline   for the dominant kernel (the GEMM) against the measured bf16
@@ -49,6 +53,10 @@ if ROOT not in sys.path:
 
 GEMM_M, GEMM_N, GEMM_K = 8192, 8192, 16384
 GEMV_M, GEMV_K, GEMV_NS = 34816, 5120, (1, 4, 8)
+# A decode step runs GEMVs back to back: each n is timed over a chain of this
+# many launches (events at the chain's ends only), rotating three weight copies
+# so that no launch finds its W in L2.
+GEMV_CHAIN = 4
 S_PREFILL = 4096
 METRIC = "FP16 GEMM TFLOP/s @8192x8192x16384; BF16 GEMV HBM GB/s (fraction of peak)"
 WORKLOAD = "gemm_f16_colmajor 8192x8192x16384 + gemv_bf16 34816x5120 n=1,4,8"
@@ -472,7 +480,7 @@ def run_ours(args):
     A = A_p.to(dev)
     B = B_p.to(dev)
     C = torch.empty(GEMM_M * GEMM_N, dtype=torch.int16, device=dev)
-    Ws = [W_p.to(dev) for _ in GEMV_NS]           # one weight copy per GEMV call
+    Ws = [W_p.to(dev) for _ in range(3)]          # weight copies, rotated: consecutive launches differ
     xs = {n: x_p[n].to(dev) for n in GEMV_NS}
     ys = {n: torch.empty(n * GEMV_M, dtype=torch.int16, device=dev) for n in GEMV_NS}
     C_p = torch.empty(GEMM_M * GEMM_N, dtype=torch.int16).pin_memory()
@@ -487,10 +495,13 @@ def run_ours(args):
         bsk.gemm_f16_colmajor_enqueue(A, B, C, GEMM_M, GEMM_N, GEMM_K, stream)
         if ev is not None:
             ev["g1"].record(stream)
-        for i, n in enumerate(GEMV_NS):
+        j = 0
+        for n in GEMV_NS:
             if ev is not None:
                 ev[f"v0_{n}"].record(stream)
-            bsk.gemv_bf16_enqueue(Ws[i], xs[n], ys[n], GEMV_M, GEMV_K, n, stream)
+            for _ in range(GEMV_CHAIN):
+                bsk.gemv_bf16_enqueue(Ws[j % len(Ws)], xs[n], ys[n], GEMV_M, GEMV_K, n, stream)
+                j += 1
             if ev is not None:
                 ev[f"v1_{n}"].record(stream)
 
@@ -518,7 +529,7 @@ def run_ours(args):
 
     total_ms = t_start.elapsed_time(t_end)
     gemm_ms = [e["g0"].elapsed_time(e["g1"]) for e in evs]
-    gemv_ms = {n: [e[f"v0_{n}"].elapsed_time(e[f"v1_{n}"]) for e in evs] for n in GEMV_NS}
+    gemv_ms = {n: [e[f"v0_{n}"].elapsed_time(e[f"v1_{n}"]) / GEMV_CHAIN for e in evs] for n in GEMV_NS}
     gemm_ms_mean = statistics.fmean(gemm_ms)
 
     def pct(values):
@@ -564,6 +575,28 @@ def run_ours(args):
             blocking.append(time.perf_counter() - t0)
     blocking_ms = max_over_ranks(statistics.median(blocking), dist, dev) * 1e3
     e2e_gemv_s = {n: max_over_ranks(statistics.median(v), dist, dev) for n, v in e2e_gemv.items()}
+    # one GEMV launch after the GEMM, bracketed on its own (events on both sides
+    # stop the next launch from overlapping this one's tail)
+    single = {n: [] for n in GEMV_NS}
+    single_steps = max(3, min(20, args.steps))
+    sev = []
+    for it in range(single_steps + 1):
+        bsk.gemm_f16_colmajor_enqueue(A, B, C, GEMM_M, GEMM_N, GEMM_K, stream)
+        row = {}
+        for i, n in enumerate(GEMV_NS):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            bsk.gemv_bf16_enqueue(Ws[(it + i) % len(Ws)], xs[n], ys[n], GEMV_M, GEMV_K, n, stream)
+            e1.record(stream)
+            row[n] = (e0, e1)
+        if it:
+            sev.append(row)
+    torch.cuda.synchronize()
+    bsk.stream_check(stream)
+    for row in sev:
+        for n, (e0, e1) in row.items():
+            single[n].append(e0.elapsed_time(e1))
+    single_ms = {n: max_over_ranks(statistics.median(v), dist, dev) for n, v in single.items()}
 
     peaks, peak_src = load_peaks()
     value = whole_job_rate(gemm_flops(), gemm_ms_mean * 1e-3, dist, dev) / 1e12
@@ -575,6 +608,8 @@ def run_ours(args):
         gbs = gemv_bytes(n) / (gemv_ms_mean[n] * 1e-3) / 1e9
         gemv[f"n{n}"] = {"gbs": round(world * gbs, 1), "us": round(gemv_ms_mean[n] * 1e3, 2),
                          "frac_of_hbm": round(gbs / hbm_peak, 4),
+                         "single_launch_us": round(single_ms[n] * 1e3, 2),
+                         "single_launch_frac_of_hbm": round(gemv_bytes(n) / (single_ms[n] * 1e-3) / 1e9 / hbm_peak, 4),
                          "e2e_gbs": round(world * gemv_bytes(n) / e2e_gemv_s[n] / 1e9, 1)}
     gemv_n1_gbs = gemv_bytes(1) / (gemv_ms_mean[1] * 1e-3) / 1e9
 
@@ -596,7 +631,11 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "gemm": [GEMM_M, GEMM_N, GEMM_K], "gemv": [GEMV_M, GEMV_K, list(GEMV_NS)],
                    "parallelism": f"replicas x{world}", "gemm_tile": [256, 256, 64],
                    "gemm_stage_bytes_per_sm": tile_stage_bytes(128, 128, 64),
-                   "l2": "inputs larger than L2 (GEMM operands 537 MB; each GEMV reads its own 356 MB weight copy)"},
+                   "l2": "inputs larger than L2 (GEMM operands 537 MB; consecutive GEMV launches read different "
+                         "356 MB weight copies, three in rotation)",
+                   "gemv_timing": f"per-launch average over a chain of {GEMV_CHAIN} back-to-back launches per n "
+                                  "(events at the chain's ends); single_launch_us: one launch after the GEMM with "
+                                  "events on both sides"},
         "gemv": gemv,
         "timing_us": timing_us,
         "blocking_call_ms": {"gemm_f16_colmajor": round(blocking_ms, 4)},
@@ -615,7 +654,7 @@ def run_ours(args):
                           "frac": round(gemv_n1_gbs / hbm_peak, 4),
                           "traffic": committed_traffic("gemv_bf16_34816x5120_n1"),
                           "peak_source": f"{peak_src} hbm_gbs", "kernel": "gemv_bf16_kernel<1, 4, 4> (n=1, register streaming)"},
-        "gpu_launches": args.steps * (1 + len(GEMV_NS)),
+        "gpu_launches": args.steps * (1 + GEMV_CHAIN * len(GEMV_NS)),
         "clocks": clocks,
     }
     if not args.no_other_configs:
