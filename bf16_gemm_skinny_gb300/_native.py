@@ -40,6 +40,7 @@ OPTIONS = {
     "gemm_kernel": 10,
     "stream_k": 11,
     "pdl": 12,
+    "tile_sched": 13,
 }
 
 # Every symbol include/bsk.h declares.

@@ -44,7 +44,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 13;
+constexpr int kNumOpts = 14;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -263,6 +263,12 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
         // GEMM + GEMVs the 8192^2 x 16384 gain did not show.
         stream_k = sk_opt == 2;
     }
+    // Tile order on CTA pairs (whole tiles): fixed unless the dynamic order --
+    // one cluster per tile launched, a free pair taking the tile of a cluster
+    // whose launch it cancels -- is requested.  Interleaved A/B on GB300
+    // (dynamic time over fixed): 8192^2 x 16384 1.00, 8192^3 0.98, the prefill
+    // shape 1.00, 4095 x 4097 x 4100 and 8192^2 x 4096 1.03.
+    const bool dyn = pair && !stream_k && opt_or(BSK_OPT_TILE_SCHED, 0) == 2;
     // one slot per CTA: block_n x 128 FP32 (CTA pairs: each CTA's 128 rows of a 256-wide tile)
     const size_t sk_part_bytes = stream_k ? static_cast<size_t>(sms) * block_n * 128 * sizeof(float) : 0;
     const size_t sk_flag_bytes = stream_k ? static_cast<size_t>(sms) * sizeof(int) : 0;
@@ -329,6 +335,7 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     g.status = g_status_dev;
     g.wait_limit_ns = static_cast<unsigned long long>(opt_or(BSK_OPT_WAIT_LIMIT_US, kDefaultWaitLimitUs)) * 1000ull;
     g.pdl = opt_or(BSK_OPT_PDL, 0) != 1;
+    g.dyn = dyn;
     if (bsk::launch_gemm(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
     return BSK_OK;
 }
@@ -766,6 +773,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_GEMM_KERNEL: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_STREAM_K: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_PDL: ok = value == 0 || value == 1; break;
+    case BSK_OPT_TILE_SCHED: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

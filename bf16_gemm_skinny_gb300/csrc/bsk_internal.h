@@ -132,6 +132,7 @@ struct GemmLaunch {
     int* status = nullptr;   // device status word
     unsigned long long wait_limit_ns = 2000000000ull;
     bool pdl = true;         // whole-tile launches: programmatic dependent of the previous kernel
+    bool dyn = false;        // CTA pairs, whole tiles: dynamic tile order (one cluster per tile launched)
 };
 
 // Returns 0 on success; otherwise an error message is written to `msg`.

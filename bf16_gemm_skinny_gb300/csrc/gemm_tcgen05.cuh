@@ -108,6 +108,9 @@ struct Params {
     int* sk_flag;           // [gridDim.x], zero at launch: set once a CTA's slot is written
     int* status;
     unsigned long long wait_limit_ns;
+    // CTA pairs, whole tiles: 1 = dynamic tile order (the grid holds one cluster
+    // per tile; later tiles come from clusters whose launch is cancelled)
+    int dyn;
 };
 
 // The work of one unit (a CTA, or a CTA pair) of `units` as a sequence of
@@ -165,7 +168,42 @@ enum WaitSite {
     kSiteMmaDrain = 5,
     kSiteProducerDrain = 6,
     kSiteStreamKPartial = 7,
+    kSiteSchedFull = 8,
+    kSiteSchedEmpty = 9,
 };
+
+// Dynamic tile order of the CTA-pair kernel (Params::dyn).  Cluster c of the
+// grid starts on tile c; each later tile of a pair is the tile of a cluster
+// whose launch the hardware cancels on request (cluster launch control), so
+// tiles go to whichever pairs are free first instead of a fixed share per
+// pair.  The even CTA's producer makes one request per tile, into a ring of
+// kSched response slots that both CTAs receive.  Every role of both CTAs reads
+// each response after its CTA's sched_full barrier completes, then hands the
+// slot back on the even CTA's sched_empty barrier, which needs kSchedReaders
+// arrivals before the slot is reused.
+constexpr int kSched = 4;
+// even CTA: producer, MMA issuer, epilogue warps; odd CTA: producer, epilogue warps
+constexpr int kSchedReaders = 2 + 2 * kEpiWarps + 1;
+
+// Tile of iteration `it` under the dynamic order: 1 with *tile set, 0 when the
+// pair has no tile left, -1 on a timeout.  For it > 0, *slot is the response
+// slot read, which the caller hands back.
+__device__ __forceinline__ int dyn_tile(int it, uint32_t resp0, uint32_t sched_full0, const WaitCtl& wc, int* tile,
+                                        int* slot)
+{
+    if (it == 0) {
+        *tile = static_cast<int>(blockIdx.x >> 1);
+        return 1;
+    }
+    const int u = it - 1;
+    const int s = u % kSched;
+    *slot = s;
+    if (!mbar_wait(sched_full0 + 8 * s, static_cast<uint32_t>(u / kSched) & 1u, wc, kSiteSchedFull)) return -1;
+    int first_x = 0;
+    if (!clc_query(resp0 + 16 * s, &first_x)) return 0;
+    *tile = first_x >> 1;
+    return 1;
+}
 
 // One rounding of the FP32 accumulator to a 16-bit output type.
 template <int OUT>
@@ -588,9 +626,13 @@ struct PairCfg {
     static constexpr int kTile = 256;                      // pair tile is 256 x 256
     static constexpr int kTmemCols = 2 * kTile;
     static constexpr int kNumBars = 2 * kStages + 5;
-    static constexpr int kBarBytes = 256;
+    // barriers, TMEM slot + abort flag, then the dynamic order's 2 x kSched
+    // barriers and kSched 16-byte response slots
+    static constexpr int kSchedBarOffset = kNumBars * 8 + 8;
+    static constexpr int kSchedRespOffset = (kSchedBarOffset + 2 * kSched * 8 + 15) / 16 * 16;
+    static constexpr int kBarBytes = 512;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
-    static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area too small");
+    static_assert(kSchedRespOffset + kSched * 16 <= kBarBytes, "barrier area too small");
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
 };
 
@@ -621,6 +663,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tfull0 = empty0 + 8 * S;
     const uint32_t tempty0 = tfull0 + 16;
     const uint32_t drain_bar = tempty0 + 16;
+    const uint32_t sched_full0 = full0 + Cf::kSchedBarOffset;    // kSched barriers: response landed
+    const uint32_t sched_empty0 = sched_full0 + 8 * kSched;     // kSched barriers: response read by all
+    const uint32_t resp0 = full0 + Cf::kSchedRespOffset;         // kSched 16-byte responses
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -639,6 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty0 + 8 * a, 2 * kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        for (int q = 0; q < kSched; ++q) {
+            mbar_init(sched_full0 + 8 * q, 1);
+            mbar_init(sched_empty0 + 8 * q, kSchedReaders);
+        }
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -664,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_launch_dependents();
     const uint32_t leader_full0 = mapa_shared(full0, 0);
     const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
+    const uint32_t leader_sched_empty0 = mapa_shared(sched_empty0, 0);
     const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
     uint32_t never = 0u;
     const WaitCtl wc_drain{&never, p.status, p.wait_limit_ns};
@@ -677,9 +727,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            int armed = 0, read = 0;   // dynamic order: responses this CTA expects / has read
             SegCursor cur = seg_first(p, pair, num_pairs);
-            int tile, kb0, kb1;
-            while (ok && seg_next(p, cur, tile, kb0, kb1)) {
+            int tile = 0, kb0 = 0, kb1 = 0;
+            for (int it = 0; ok; ++it) {
+                if (p.dyn) {
+                    int slot = 0;
+                    const int r = dyn_tile(it, resp0, sched_full0, wc, &tile, &slot);
+                    if (r < 0) {
+                        ok = false;
+                        break;
+                    }
+                    if (it > 0) {
+                        ++read;
+                        mbar_arrive_remote(leader_sched_empty0 + 8 * slot);
+                    }
+                    if (r == 0) break;
+                    kb0 = 0;
+                    kb1 = p.num_kb;
+                    // ask for the pair's next tile now, so that the answer is in by the
+                    // time this tile's k-blocks are issued
+                    const int q = it % kSched;
+                    if (leader && !mbar_wait_cluster(sched_empty0 + 8 * q, ((it / kSched) & 1) ^ 1u, wc,
+                                                     kSiteSchedEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(sched_full0 + 8 * q, 16);
+                    ++armed;
+                    if (leader) clc_try_cancel_multicast(resp0 + 16 * q, sched_full0 + 8 * q);
+                } else if (!seg_next(p, cur, tile, kb0, kb1)) {
+                    break;
+                }
                 int pm, pn;
                 tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
                 const int m0 = pm * T + static_cast<int>(rank) * kBM;
@@ -713,6 +792,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (armed > read) {
+                // A response is still on its way into this CTA's shared memory
+                // (abort path): wait (bounded) until it has landed.
+                const int u = armed - 1;
+                mbar_wait(sched_full0 + 8 * (u % kSched), static_cast<uint32_t>(u / kSched) & 1u, wc_drain,
+                          kSiteSchedFull);
+            }
             if (!ok && leader) {
                 // Abort: the even CTA's full barriers count both CTAs' bytes; wait
                 // (bounded) until the loads already armed have landed.
@@ -735,8 +821,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             bool issued_any = false;
             SegCursor cur = seg_first(p, pair, num_pairs);
-            int tile, kb0, kb1;
-            for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
+            int tile = 0, kb0 = 0, kb1 = 0;
+            for (int it = 0;; ++it) {
+                if (p.dyn) {
+                    int slot = 0;
+                    const int r = dyn_tile(it, resp0, sched_full0, wc, &tile, &slot);
+                    if (r < 0) {
+                        ok = false;
+                        break;
+                    }
+                    if (it > 0) mbar_arrive_remote(leader_sched_empty0 + 8 * slot);
+                    if (r == 0) break;
+                    kb0 = 0;
+                    kb1 = p.num_kb;
+                } else if (!seg_next(p, cur, tile, kb0, kb1)) {
+                    break;
+                }
                 const int acc = it & 1;
                 const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
                 if (!mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
@@ -785,8 +885,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - 2;
         uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
         SegCursor cur = seg_first(p, pair, num_pairs);
-        int tile, kb0, kb1;
-        for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
+        int tile = 0, kb0 = 0, kb1 = 0;
+        for (int it = 0;; ++it) {
+            if (p.dyn) {
+                int slot = 0;
+                int r = dyn_tile(it, resp0, sched_full0, wc, &tile, &slot);
+                r = __reduce_min_sync(0xffffffffu, r);
+                __syncwarp();   // every lane has read the response before it is handed back
+                if (it > 0 && r >= 0 && lane == 0) mbar_arrive_remote(leader_sched_empty0 + 8 * slot);
+                if (r <= 0) break;
+                kb0 = 0;
+                kb1 = p.num_kb;
+            } else if (!seg_next(p, cur, tile, kb0, kb1)) {
+                break;
+            }
             const int acc = it & 1;
             const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
             bool ok = mbar_wait(tfull0 + 8 * acc, aph, wc, kSiteEpilogueTmemFull);
@@ -959,6 +1071,7 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     p.alpha = g.alpha;
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
+    p.dyn = 0;
 
     auto kern = gemm_tcgen05_kernel<BN, A_MN, B_MN, IN, OUT>;
     static SmemOptIn smem_opt;
@@ -1044,6 +1157,7 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.sk_flag = nullptr;
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
+    p.dyn = 0;
 
     auto kern = gemm_tcgen05_pair_kernel<A_MN, B_MN, IN, OUT>;
     static SmemOptIn smem_opt;
@@ -1108,6 +1222,12 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     const int per_pair = (p.num_tiles + clusters - 1) / clusters;
     const int pairs = (p.num_tiles + per_pair - 1) / per_pair;
     cfg.gridDim = dim3(2 * pairs, 1, 1);
+    if (g.dyn) {
+        // one cluster per tile: the resident clusters take the tiles of those
+        // whose launch they cancel (the kernel's dynamic order)
+        p.dyn = 1;
+        cfg.gridDim = dim3(2 * static_cast<unsigned>(p.num_tiles), 1, 1);
+    }
     cudaLaunchAttribute attr_pdl[2];
     attr_pdl[0] = attr[0];
     attr_pdl[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

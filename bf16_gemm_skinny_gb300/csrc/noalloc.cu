@@ -207,6 +207,7 @@ extern "C" int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, u
     g.status = d->status;
     g.wait_limit_ns = static_cast<unsigned long long>(option_or(BSK_OPT_WAIT_LIMIT_US, 2000000)) * 1000ull;
     g.pdl = option_or(BSK_OPT_PDL, 0) != 1;
+    g.dyn = g.pair && option_or(BSK_OPT_TILE_SCHED, 0) == 2;   // tile order on CTA pairs: fixed unless requested
     if (bsk::launch_gemm(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
 
     int code = 0;

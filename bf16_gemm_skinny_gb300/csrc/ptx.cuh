@@ -204,6 +204,39 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
                  : "memory");
 }
 
+// Cluster launch control (PTX ISA, "clusterlaunchcontrol"): asks for the launch
+// of a cluster of this grid that has not started yet to be cancelled, so that
+// this cluster can do its work instead.  The 16-byte response is written to
+// shared memory at `resp` in every CTA of the cluster, and each CTA's mbarrier
+// at `bar` receives 16 bytes of transaction count.  After a request that came
+// back without a cancelled cluster, no further request may be made.
+__device__ __forceinline__ void clc_try_cancel_multicast(uint32_t resp, uint32_t bar)
+{
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+        ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Decodes a response: true, with the x index of the cancelled cluster's first
+// CTA, when a launch was cancelled.
+__device__ __forceinline__ bool clc_query(uint32_t resp, int* first_x)
+{
+    uint32_t ok, x = 0u;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 rr;\n\t"
+        "ld.shared.b128 rr, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, rr;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, rr;\n\t}"
+        : "=r"(ok), "+r"(x)
+        : "r"(resp)
+        : "memory");
+    *first_x = static_cast<int>(x);
+    return ok != 0;
+}
+
 // 2-D tiled load of the box at coordinates (x, y) (x = innermost) into shared
 // memory at `dst`; completion is signalled on mbarrier `bar` as transaction bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y)

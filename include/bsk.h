@@ -291,6 +291,11 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *                            TMEM allocation, L2 prefetch of the first weight tiles)
  *                            overlaps that kernel's last CTAs.  Either way no input is read
  *                            and no output written before the earlier kernel has completed.
+ *   BSK_OPT_TILE_SCHED       tile order of the CTA-pair GEMM kernel (whole tiles): 0 or 1
+ *                            fixed (pair p takes tiles p, p + P, ...), 2 dynamic (one cluster
+ *                            per tile launched; a pair that is done takes the tile of a
+ *                            cluster whose launch it cancels, so tiles go to the pairs that
+ *                            are free first; BSK_OPT_NUM_SMS does not cap this grid)
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
@@ -305,7 +310,8 @@ enum {
     BSK_OPT_GEMV_KERNEL = 9,
     BSK_OPT_GEMM_KERNEL = 10,
     BSK_OPT_STREAM_K = 11,
-    BSK_OPT_PDL = 12
+    BSK_OPT_PDL = 12,
+    BSK_OPT_TILE_SCHED = 13
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);

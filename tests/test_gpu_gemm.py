@@ -285,3 +285,31 @@ def test_stream_k_on_cta_pairs(M, N, K, sms):
     cols = sorted({0, 1, 255, 256, N // 2, N - 1})
     rows = sorted({0, 127, 128, M // 2, M - 1})
     sampled_check(got, A, B, M, N, K, cols, rows, True)
+
+
+@pytest.mark.parametrize("M,N,K", [(1000, 777, 1030), (256, 256, 64), (300, 517, 200), (2304, 2560, 1024),
+                                   (4095, 4097, 4100)])
+def test_dynamic_tile_order_on_cta_pairs(M, N, K):
+    """CTA pairs with the dynamic tile order forced (one cluster per tile launched,
+    free pairs taking the tiles of clusters whose launch they cancel), from a
+    single tile up to 17 x 16 tiles: integer inputs give the oracle's bits, and
+    on random inputs the result equals the fixed order's bit for bit (a tile's
+    sum does not depend on which pair computes it)."""
+    A, B = operands(M, N, K, "int2")
+    bsk.set_option("tile_sched", 2)
+    try:
+        got = run(A, B, M, N, K)
+    finally:
+        bsk.set_option("tile_sched", 0)
+    cols = sorted(c for c in {0, 1, 255, 256, N // 2, N - 1} if c < N)
+    rows = sorted(r for r in {0, 127, 128, M // 2, M - 1} if r < M)
+    sampled_check(got, A, B, M, N, K, cols, rows, True)
+    Ar, Br = operands(M, N, K, "normal0.5")
+    outs = {}
+    for sched in (1, 2):
+        bsk.set_option("tile_sched", sched)
+        try:
+            outs[sched] = run(Ar, Br, M, N, K)
+        finally:
+            bsk.set_option("tile_sched", 0)
+    assert np.array_equal(outs[1], outs[2])

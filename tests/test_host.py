@@ -187,7 +187,14 @@ def test_options_round_trip_and_range_checks(lib):
         bsk.set_option("block_n", 96)
     with pytest.raises(bsk.BskError):
         bsk.set_option("gemv_rows", 3)
+    for name, good, bad in (("pdl", 1, 2), ("tile_sched", 2, 3), ("stream_k", 2, 3)):
+        bsk.set_option(name, good)
+        assert bsk.get_option(name) == good
+        bsk.set_option(name, 0)
+        with pytest.raises(bsk.BskError):
+            bsk.set_option(name, bad)
     assert lib.bsk_set_option(99, 1) == 1
+    assert lib.bsk_set_option(len(bsk.OPTIONS) + 1, 1) == 1
 
 
 def test_watchdog_probe_validates_limit(lib):
