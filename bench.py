@@ -27,7 +27,8 @@ Reported (one JSON line, rank 0):
              FP16 GEMMs, the 4096-token BF16 prefill projection, gemm_f16 in
              other storage forms with a fused bias, and the FP8 GEMM), measured
              after the step.
-  decode_attention  split-KV decode attention at 8K/16K/32K tokens (KV-cache GB/s).
+  decode_attention  split-KV decode attention at 8K/16K/32K tokens (KV-cache GB/s),
+             back-to-back calls (and, separately, each call between events).
   cpu_baseline  the oracle timed on a bounded sample on the host cores.
 
 ``--impl reference`` times the oracle (the plain CPU triple loop) on the same
@@ -336,6 +337,25 @@ def time_launches(fn, iters: int, warmup: int = 3) -> float:
     return statistics.fmean(evs[i].elapsed_time(evs[i + 1]) for i in range(iters))
 
 
+def time_chain(fn, iters: int, warmup: int = 3) -> float:
+    """Mean device time (ms) per call of `iters` back-to-back calls of `fn` on the
+    current stream, CUDA events at the chain's ends only (an event between two
+    launches would stop the programmatic-dependent overlap of consecutive calls)."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(iters):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
 def other_configs(W_prefill, dev, peaks):
     """Device time of the other workloads (256^3, the ragged 4095x4097x4100 GEMM
     and the 4096-token prefill projection), each on its own seeded inputs."""
@@ -407,7 +427,9 @@ def other_configs(W_prefill, dev, peaks):
 def attention_configs(dev, hbm_peak):
     """Split-KV decode attention at the page's head shape (16 query heads over 4 KV
     heads, head_dim 256, 784-token pages) for 8K / 16K / 32K tokens, with the
-    automatic segment count and with the page's 16 / 32 rule."""
+    automatic segment count and with the page's 16 / 32 rule.  `us` is the mean
+    per call over 20 back-to-back calls (each on a cache copy not in L2);
+    `per_call_events_us` brackets every call with events."""
     import numpy as np
     import torch
 
@@ -440,10 +462,11 @@ def attention_configs(dev, hbm_peak):
                 bsk.decode_attention_bf16_enqueue(q, kc, vc, bt, sl, o, 1, nqh, nkv, hd, bs, nb, nb, L, 1.0 / 16.0,
                                                   segs)
 
-            ms = time_launches(call, 20)
+            ms = time_chain(call, 20)
+            ms_single = time_launches(call, 20)
             gbs = kv_bytes / (ms * 1e-3) / 1e9
             row[name] = {"segments": segs, "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-                         "frac_of_hbm": round(gbs / hbm_peak, 4)}
+                         "frac_of_hbm": round(gbs / hbm_peak, 4), "per_call_events_us": round(ms_single * 1e3, 2)}
         row["kv_copies"] = copies
         out[f"L{L}"] = row
         del k, v, kvs

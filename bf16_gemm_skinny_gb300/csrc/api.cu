@@ -614,6 +614,7 @@ int enqueue_decode_attention(const uint16_t* q, const uint16_t* k_cache, const u
     a.num_segments = segs;
     a.scale = softmax_scale;
     a.status = g_status_dev;
+    a.pdl = opt_or(BSK_OPT_PDL, 0) != 1;
     char msg[512] = "";
     if (bsk::launch_decode_attention(a, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
     return BSK_OK;

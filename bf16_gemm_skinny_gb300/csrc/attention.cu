@@ -211,9 +211,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
     __shared__ __align__(16) float2 s_p[kAttnWarps][T][G];
     __shared__ __align__(16) float2 s_c[kAttnWarps][G];
     extern __shared__ __align__(16) uint8_t smem[];
-    // The merge kernel launched after this one may be scheduled from now on; it
-    // waits on the device for this grid to complete before reading anything.
-    asm volatile("griddepcontrol.launch_dependents;");
+    // This kernel is a programmatic dependent of the kernel before it in the
+    // stream: nothing is read before that kernel has completed.  The merge
+    // kernel launched after this one may be scheduled from now on; it waits on
+    // the device for this grid to complete before reading anything.
+    griddep_wait();
+    griddep_launch_dependents();
 
     int L = p.seq_lens[seq];
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
@@ -481,12 +484,11 @@ constexpr int kMergeLoads = 16;   // o_s loads in flight per lane
 // One CTA per (query head x sequence, 32 output elements).  It is launched as
 // a programmatic dependent of the split kernel, so it may be scheduled while
 // the split kernel's last CTAs still run; griddepcontrol.wait holds it until
-// that grid has completed and its partials are visible.  Then: each thread
-// loads (m_s, l_s) of its segments in one round, M = max_s m_s, weights
-// w_s = 2^(m_s - M) (in shared memory), L = sum_s w_s l_s; each warp sums
-// w_s o_s[e] over every 8th segment for the CTA's 32 elements (one per lane),
-// all of its loads issued before the sums, and the eight partial sums are
-// added: out[e] = sum / L.
+// that grid has completed and its partials are visible.  Then, in one round of
+// loads, each thread fetches (m_s, l_s) of its segments and the o_s[e] its warp
+// sums (every 8th segment, the CTA's 32 elements, one per lane).  M = max_s
+// m_s, weights w_s = 2^(m_s - M) (in shared memory), L = sum_s w_s l_s; each
+// warp sums w_s o_s[e] and the eight partial sums are added: out[e] = sum / L.
 template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     attn_merge_kernel(const float* __restrict__ partial, __nv_bfloat16* __restrict__ out, int num_segments)
@@ -501,6 +503,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     constexpr int kThreads = kMergeWarps * 32;
     constexpr int kPerThread = 1024 / kThreads;   // num_segments <= 1024
     const float* base = partial + static_cast<long long>(head) * num_segments * (HD + 2);
+    const int e = blockIdx.y * 32 + lane;
+    const float* po = base + 2 + e;
+    // the first kMergeLoads of this warp's o_s[e], loaded together with (m_s, l_s)
+    float v0[kMergeLoads];
+#pragma unroll
+    for (int u = 0; u < kMergeLoads; ++u) {
+        const int s = warp + u * kMergeWarps;
+        v0[u] = s < num_segments ? po[static_cast<long long>(s) * (HD + 2)] : 0.f;
+    }
     float ms[kPerThread], ls[kPerThread];
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
@@ -527,10 +538,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         }
     }
     const float Lsum = block_sum(lsum, s_red);   // its barriers also publish s_w
-    const int e = blockIdx.y * 32 + lane;
-    const float* po = base + 2 + e;
     float O = 0.f;
-    for (int s0 = warp; s0 < num_segments; s0 += kMergeWarps * kMergeLoads) {
+#pragma unroll
+    for (int u = 0; u < kMergeLoads; ++u) {
+        const int s = warp + u * kMergeWarps;
+        if (s < num_segments) O = fmaf(s_w[s], v0[u], O);
+    }
+    for (int s0 = warp + kMergeWarps * kMergeLoads; s0 < num_segments; s0 += kMergeWarps * kMergeLoads) {
         float v[kMergeLoads];
 #pragma unroll
         for (int u = 0; u < kMergeLoads; ++u) {
@@ -565,8 +579,8 @@ int launch_split(const AttnLaunch& a, const AttnParams& p, cudaStream_t stream, 
         return 1;
     }
     dim3 grid(a.num_segments, a.num_kv_heads, a.num_seqs);
-    kern<<<grid, kAttnWarps * 32, smem, stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_kernel(kern, grid, dim3(kAttnWarps * 32), static_cast<size_t>(smem), stream, a.pdl, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "attention launch failed: %s", cudaGetErrorString(e));
         return 1;

@@ -169,6 +169,7 @@ struct AttnLaunch {
     int block_size, max_blocks, num_blocks, max_seq_len, num_segments;
     float scale;
     int* status;
+    bool pdl = true;              // split kernel: programmatic dependent of the previous kernel
 };
 int launch_decode_attention(const AttnLaunch& a, cudaStream_t stream, char* msg, size_t msg_len);
 // CTAs of the attention's split kernel resident per SM for this head shape (>= 1).

@@ -285,12 +285,13 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *                            one-CTA-per-tile kernel when whole tiles would fill under three
  *                            quarters of the SMs and a tile has at least 32 k-blocks; whole
  *                            tiles on CTA pairs
- *   BSK_OPT_PDL              1: launch the GEMM and GEMV kernels in plain stream order;
- *                            0 (default): as programmatic dependents of the kernel before
- *                            them in the stream, so that their prologue (barrier set-up,
- *                            TMEM allocation, L2 prefetch of the first weight tiles)
- *                            overlaps that kernel's last CTAs.  Either way no input is read
- *                            and no output written before the earlier kernel has completed.
+ *   BSK_OPT_PDL              1: launch the GEMM, GEMV and attention kernels in plain stream
+ *                            order; 0 (default): as programmatic dependents of the kernel
+ *                            before them in the stream, so that their launch and prologue
+ *                            (barrier set-up, TMEM allocation, L2 prefetch of the first
+ *                            weight tiles) overlap that kernel's last CTAs.  Either way no
+ *                            input is read and no output written before the earlier kernel
+ *                            has completed.
  *   BSK_OPT_TILE_SCHED       tile order of the CTA-pair GEMM kernel (whole tiles): 0 or 1
  *                            fixed (pair p takes tiles p, p + P, ...), 2 dynamic (one cluster
  *                            per tile launched; a pair that is done takes the tile of a
