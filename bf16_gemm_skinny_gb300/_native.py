@@ -49,7 +49,7 @@ EXPORTS = (
     "bsk_stream_check", "bsk_last_error", "bsk_status_string", "bsk_version", "bsk_tile_coord",
     "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout", "gemm_f16_colmajor_noalloc",
     "decode_attention_bf16", "bsk_decode_attention_bf16_enqueue", "gemm_f16", "bsk_gemm_f16_enqueue",
-    "gemm_fp8", "bsk_gemm_fp8_enqueue",
+    "gemm_fp8", "bsk_gemm_fp8_enqueue", "gemm_f16_colmajor_host", "gemv_bf16_host",
 )
 
 COL_MAJOR, ROW_MAJOR = 0, 1
@@ -82,7 +82,8 @@ def load():
         lib = ctypes.CDLL(path)
         p = ctypes.c_void_p
         i = ctypes.c_int
-        for name in ("gemm_f16_colmajor", "bsk_gemm_f16_colmajor_enqueue", "gemm_f16_colmajor_noalloc"):
+        for name in ("gemm_f16_colmajor", "bsk_gemm_f16_colmajor_enqueue", "gemm_f16_colmajor_noalloc",
+                     "gemm_f16_colmajor_host"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
             getattr(lib, name).restype = i
         for name in ("gemm_f16", "bsk_gemm_f16_enqueue"):
@@ -91,7 +92,7 @@ def load():
         for name in ("gemm_fp8", "bsk_gemm_fp8_enqueue"):
             getattr(lib, name).argtypes = [i, p, i, p, i, p, i, i, i, i, i, ctypes.c_float, p]
             getattr(lib, name).restype = i
-        for name in ("gemv_bf16", "bsk_gemv_bf16_enqueue"):
+        for name in ("gemv_bf16", "bsk_gemv_bf16_enqueue", "gemv_bf16_host"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
             getattr(lib, name).restype = i
         for name in ("decode_attention_bf16", "bsk_decode_attention_bf16_enqueue"):
@@ -122,7 +123,9 @@ def _addr(t) -> int | None:
         return None
     if isinstance(t, int):
         return t
-    return int(t.data_ptr())
+    if hasattr(t, "data_ptr"):
+        return int(t.data_ptr())
+    return int(t.ctypes.data)   # a NumPy array (host memory)
 
 
 _torch = None
@@ -212,6 +215,18 @@ def gemm_f16_colmajor_noalloc(A, B, C, M: int, N: int, K: int, stream=None) -> N
 def gemv_bf16(W, x, y, M: int, K: int, n: int, stream=None) -> None:
     """y[t, j] = sum_k x[t, k] W[j, k], BF16; blocks until done."""
     _check(load().gemv_bf16(_addr(W), _addr(x), _addr(y), M, K, n, _stream(stream)))
+
+
+def gemm_f16_colmajor_host(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """gemm_f16_colmajor on host buffers (CPU tensors or NumPy arrays; pinned ones
+    overlap the copies with the computation); blocks until C holds the result."""
+    _check(load().gemm_f16_colmajor_host(_addr(A), _addr(B), _addr(C), M, N, K, _stream(stream)))
+
+
+def gemv_bf16_host(W, x, y, M: int, K: int, n: int, stream=None) -> None:
+    """gemv_bf16 on host buffers (CPU tensors or NumPy arrays); blocks until y holds
+    the result."""
+    _check(load().gemv_bf16_host(_addr(W), _addr(x), _addr(y), M, K, n, _stream(stream)))
 
 
 def gemv_bf16_enqueue(W, x, y, M: int, K: int, n: int, stream=None) -> None:

@@ -17,6 +17,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "bsk.h"
 #include "bsk_internal.h"
@@ -148,9 +149,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Workspace {
     void* ptr = nullptr;
     cudaStream_t s = nullptr;
-    ~Workspace()
+    ~Workspace() { release(); }
+    // stream-ordered free on the stream it was taken on
+    void release()
     {
         if (ptr != nullptr) cudaFreeAsync(ptr, s);
+        ptr = nullptr;
     }
 };
 
@@ -161,7 +165,7 @@ int alloc_workspace(Workspace& ws, size_t bytes, cudaStream_t s)
     if (e != cudaSuccess) {
         cudaGetLastError();
         ws.ptr = nullptr;
-        return fail(BSK_ERR_NO_MEMORY, "cudaMallocAsync(%zu bytes) for the pack workspace failed: %s", bytes,
+        return fail(BSK_ERR_NO_MEMORY, "cudaMallocAsync(%zu bytes) for a workspace failed: %s", bytes,
                     cudaGetErrorString(e));
     }
     return BSK_OK;
@@ -620,6 +624,230 @@ int enqueue_decode_attention(const uint16_t* q, const uint16_t* k_cache, const u
     return BSK_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Entry points on host buffers.  The library copies the operands to the
+// device, computes and copies the result back in blocks, so that the copy of
+// one block in, the computation of the block before it and the copy of the
+// block before that out run at the same time, on three streams: host ->
+// device, the caller's stream, device -> host.  The link between host and
+// device is the bound of such a call; the blocks hide the computation and the
+// copy back behind the copy in.
+// ---------------------------------------------------------------------------
+class HostPipe {
+  public:
+    HostPipe() = default;
+    HostPipe(const HostPipe&) = delete;
+    HostPipe& operator=(const HostPipe&) = delete;
+    ~HostPipe()
+    {
+        for (cudaEvent_t e : events_) cudaEventDestroy(e);
+        if (in_ != nullptr) cudaStreamDestroy(in_);
+        if (out_ != nullptr) cudaStreamDestroy(out_);
+    }
+    int init()
+    {
+        cudaError_t e = cudaStreamCreateWithFlags(&in_, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&out_, cudaStreamNonBlocking);
+        return e == cudaSuccess ? BSK_OK : fail_cuda(e, "cudaStreamCreateWithFlags");
+    }
+    cudaStream_t in() const { return in_; }
+    cudaStream_t out() const { return out_; }
+    // Makes `waiter` wait for the work enqueued on `from` so far.
+    int order(cudaStream_t from, cudaStream_t waiter)
+    {
+        cudaEvent_t ev = nullptr;
+        cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaEventCreateWithFlags");
+        events_.push_back(ev);
+        if ((e = cudaEventRecord(ev, from)) != cudaSuccess) return fail_cuda(e, "cudaEventRecord");
+        if ((e = cudaStreamWaitEvent(waiter, ev, 0)) != cudaSuccess) return fail_cuda(e, "cudaStreamWaitEvent");
+        return BSK_OK;
+    }
+
+  private:
+    cudaStream_t in_ = nullptr, out_ = nullptr;
+    std::vector<cudaEvent_t> events_;
+};
+
+// Device memory of the host-buffer calls: a memory pool of the library's per
+// device (not the caller's default pool) that keeps up to kHostPoolKeep bytes
+// mapped between calls, so that a call does not map fresh memory each time.
+constexpr unsigned long long kHostPoolKeep = 2ull << 30;
+
+int host_pool(cudaMemPool_t* out)
+{
+    static std::mutex mu;
+    static cudaMemPool_t pools[bsk::SmemOptIn::kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= bsk::SmemOptIn::kMaxDevices) return fail(BSK_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (pools[dev] == nullptr) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return fail_cuda(e, "cudaMemPoolCreate");
+        unsigned long long keep = kHostPoolKeep;
+        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return fail_cuda(e, "cudaMemPoolSetAttribute");
+        }
+        pools[dev] = pool;
+    }
+    *out = pools[dev];
+    return BSK_OK;
+}
+
+int alloc_host_call_workspace(Workspace& ws, size_t bytes, cudaStream_t s)
+{
+    cudaMemPool_t pool = nullptr;
+    int st = host_pool(&pool);
+    if (st != BSK_OK) return st;
+    ws.s = s;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws.ptr, bytes, pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        ws.ptr = nullptr;
+        return fail(BSK_ERR_NO_MEMORY, "cudaMallocFromPoolAsync(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+    }
+    return BSK_OK;
+}
+
+// Blocks of a streamed operand of `bytes`: about 64 MB each, 1 to 8.
+int pipe_blocks(size_t bytes)
+{
+    const size_t per = 64ull << 20;
+    const size_t b = (bytes + per - 1) / per;
+    return static_cast<int>(b < 1 ? 1 : (b > 8 ? 8 : b));
+}
+
+// C = A B (column-major FP16, as gemm_f16_colmajor) on host buffers: A goes
+// to the device first, then B and C in column blocks (a column block of a
+// column-major matrix is one contiguous range).
+int run_gemm_f16_host(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, cudaStream_t s)
+{
+    if (M < 0 || N < 0 || K < 0) return fail(BSK_ERR_INVALID_ARG, "negative size (M=%d N=%d K=%d)", M, N, K);
+    if (M == 0 || N == 0) return BSK_OK;
+    const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(K) * N * 2;
+    const size_t c_bytes = static_cast<size_t>(M) * N * 2;
+    if (C == nullptr) return fail(BSK_ERR_INVALID_ARG, "C is NULL");
+    if (K > 0 && (A == nullptr || B == nullptr)) return fail(BSK_ERR_INVALID_ARG, "A or B is NULL");
+    if (K > 0 && (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes)))
+        return fail(BSK_ERR_INVALID_ARG, "C overlaps an input");
+    if (K == 0) {   // the empty sum
+        std::memset(C, 0, c_bytes);
+        return BSK_OK;
+    }
+    int sms = 0;
+    int st = prepare_device(&sms);
+    if (st != BSK_OK) return st;
+    const size_t a_pad = (a_bytes + 255) / 256 * 256, b_pad = (b_bytes + 255) / 256 * 256;
+    Workspace ws;
+    if ((st = alloc_host_call_workspace(ws, a_pad + b_pad + c_bytes, s)) != BSK_OK) return st;
+    uint8_t* base = static_cast<uint8_t*>(ws.ptr);
+    uint16_t* dA = reinterpret_cast<uint16_t*>(base);
+    uint16_t* dB = reinterpret_cast<uint16_t*>(base + a_pad);
+    uint16_t* dC = reinterpret_cast<uint16_t*>(base + a_pad + b_pad);
+    HostPipe hp;
+    if ((st = hp.init()) != BSK_OK) return st;
+    // the copies start after the caller's earlier work on `s` (which may be
+    // writing the host buffers) and after the workspace allocation
+    if ((st = hp.order(s, hp.in())) != BSK_OK || (st = hp.order(s, hp.out())) != BSK_OK) return st;
+    cudaError_t e = cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, hp.in());
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyAsync(A)");
+    const int blocks = pipe_blocks(b_bytes);
+    const long long nb = ((static_cast<long long>(N) + blocks - 1) / blocks + 255) / 256 * 256;
+    for (long long n0 = 0; n0 < N && st == BSK_OK; n0 += nb) {
+        const long long n1 = n0 + nb < N ? n0 + nb : N;
+        e = cudaMemcpyAsync(dB + n0 * K, B + n0 * K, static_cast<size_t>(n1 - n0) * K * 2, cudaMemcpyHostToDevice,
+                            hp.in());
+        if (e != cudaSuccess) {
+            st = fail_cuda(e, "cudaMemcpyAsync(B block)");
+            break;
+        }
+        if ((st = hp.order(hp.in(), s)) != BSK_OK) break;
+        st = enqueue_gemm_general(0, 0, dA, M, dB + n0 * K, K, dC + n0 * M, M, M, static_cast<int>(n1 - n0), K,
+                                  nullptr, 0, s);
+        if (st != BSK_OK) break;
+        if ((st = hp.order(s, hp.out())) != BSK_OK) break;
+        e = cudaMemcpyAsync(C + n0 * M, dC + n0 * M, static_cast<size_t>(n1 - n0) * M * 2, cudaMemcpyDeviceToHost,
+                            hp.out());
+        if (e != cudaSuccess) st = fail_cuda(e, "cudaMemcpyAsync(C block)");
+    }
+    // join both copy streams before the workspace is released and the call returns
+    const int j1 = hp.order(hp.in(), s), j2 = hp.order(hp.out(), s);
+    ws.release();
+    const int sync = sync_and_check(s);
+    if (st != BSK_OK) return st;
+    if (j1 != BSK_OK) return j1;
+    if (j2 != BSK_OK) return j2;
+    return sync;
+}
+
+// y = x W^T (BF16, as gemv_bf16) on host buffers: x goes to the device first,
+// then W in row blocks; each block's outputs (n rows of its width) come back
+// with one strided copy into y.
+int run_gemv_bf16_host(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, cudaStream_t s)
+{
+    if (M < 0 || K < 0 || n < 0) return fail(BSK_ERR_INVALID_ARG, "negative size (M=%d K=%d n=%d)", M, K, n);
+    if (M == 0 || n == 0) return BSK_OK;
+    const size_t w_bytes = static_cast<size_t>(M) * K * 2, x_bytes = static_cast<size_t>(n) * K * 2;
+    const size_t y_bytes = static_cast<size_t>(n) * M * 2;
+    if (y == nullptr) return fail(BSK_ERR_INVALID_ARG, "y is NULL");
+    if (K > 0 && (W == nullptr || x == nullptr)) return fail(BSK_ERR_INVALID_ARG, "W or x is NULL");
+    if (K > 0 && (overlaps(y, y_bytes, W, w_bytes) || overlaps(y, y_bytes, x, x_bytes)))
+        return fail(BSK_ERR_INVALID_ARG, "y overlaps an input");
+    if (K == 0) {   // the empty sum
+        std::memset(y, 0, y_bytes);
+        return BSK_OK;
+    }
+    int sms = 0;
+    int st = prepare_device(&sms);
+    if (st != BSK_OK) return st;
+    const size_t w_pad = (w_bytes + 255) / 256 * 256, x_pad = (x_bytes + 255) / 256 * 256;
+    Workspace ws;
+    if ((st = alloc_host_call_workspace(ws, w_pad + x_pad + y_bytes, s)) != BSK_OK) return st;
+    uint8_t* base = static_cast<uint8_t*>(ws.ptr);
+    uint16_t* dW = reinterpret_cast<uint16_t*>(base);
+    uint16_t* dx = reinterpret_cast<uint16_t*>(base + w_pad);
+    uint16_t* dy = reinterpret_cast<uint16_t*>(base + w_pad + x_pad);
+    HostPipe hp;
+    if ((st = hp.init()) != BSK_OK) return st;
+    if ((st = hp.order(s, hp.in())) != BSK_OK || (st = hp.order(s, hp.out())) != BSK_OK) return st;
+    cudaError_t e = cudaMemcpyAsync(dx, x, x_bytes, cudaMemcpyHostToDevice, hp.in());
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyAsync(x)");
+    const int blocks = pipe_blocks(w_bytes);
+    const long long mb = ((static_cast<long long>(M) + blocks - 1) / blocks + 127) / 128 * 128;
+    for (long long m0 = 0; m0 < M && st == BSK_OK; m0 += mb) {
+        const long long m1 = m0 + mb < M ? m0 + mb : M;
+        const long long rows = m1 - m0;
+        e = cudaMemcpyAsync(dW + m0 * K, W + m0 * K, static_cast<size_t>(rows) * K * 2, cudaMemcpyHostToDevice,
+                            hp.in());
+        if (e != cudaSuccess) {
+            st = fail_cuda(e, "cudaMemcpyAsync(W block)");
+            break;
+        }
+        if ((st = hp.order(hp.in(), s)) != BSK_OK) break;
+        // this block's outputs, n x rows, contiguous at dy + n * m0
+        uint16_t* dyb = dy + static_cast<long long>(n) * m0;
+        if ((st = enqueue_gemv_bf16(dW + m0 * K, dx, dyb, static_cast<int>(rows), K, n, s)) != BSK_OK) break;
+        if ((st = hp.order(s, hp.out())) != BSK_OK) break;
+        e = cudaMemcpy2DAsync(y + m0, static_cast<size_t>(M) * 2, dyb, static_cast<size_t>(rows) * 2,
+                              static_cast<size_t>(rows) * 2, static_cast<size_t>(n), cudaMemcpyDeviceToHost, hp.out());
+        if (e != cudaSuccess) st = fail_cuda(e, "cudaMemcpy2DAsync(y block)");
+    }
+    const int j1 = hp.order(hp.in(), s), j2 = hp.order(hp.out(), s);
+    ws.release();
+    const int sync = sync_and_check(s);
+    if (st != BSK_OK) return st;
+    if (j1 != BSK_OK) return j1;
+    if (j2 != BSK_OK) return j2;
+    return sync;
+}
+
 }  // namespace
 
 namespace bsk {
@@ -703,6 +931,16 @@ int bsk_gemm_f16_colmajor_enqueue(const uint16_t* A, const uint16_t* B, uint16_t
 int bsk_gemv_bf16_enqueue(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream)
 {
     return enqueue_gemv_bf16(W, x, y, M, K, n, stream);
+}
+
+int gemm_f16_colmajor_host(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream)
+{
+    return run_gemm_f16_host(A, B, C, M, N, K, static_cast<cudaStream_t>(stream));
+}
+
+int gemv_bf16_host(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream)
+{
+    return run_gemv_bf16_host(W, x, y, M, K, n, static_cast<cudaStream_t>(stream));
 }
 
 int decode_attention_bf16(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,

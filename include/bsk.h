@@ -215,6 +215,29 @@ int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, uint16_t* C,
                               void* stream);
 
 /*
+ * gemm_f16_colmajor and gemv_bf16 on HOST buffers: A, B, C (W, x, y) are host
+ * pointers with the same layouts, sizes and results as the device calls (the
+ * same kernels compute them).  The call takes device memory for the operands
+ * and the result in stream order (M*K + K*N + M*N, or M*K + n*K + n*M,
+ * 16-bit elements), copies in, computes, copies back and returns when the
+ * result is in C (y), with `stream` synchronised.  The copies run on two
+ * streams of the call's own beside `stream` and overlap the work in blocks:
+ * the GEMM copies A first, then B and C in column blocks (the GEMM of one
+ * block runs while the next block of B comes in and the previous block of C
+ * goes out); gemv_bf16_host copies x first, then W in row blocks.  The
+ * copies start after the work enqueued on `stream` before the call.
+ * Page-locked (pinned) host buffers let the copies overlap the computation;
+ * pageable buffers give the same result, with less overlap.  The device
+ * memory comes from a memory pool of the library's (one per device, created
+ * on the first such call), which keeps up to 2 GiB mapped between calls so
+ * that repeated calls do not map fresh memory.  K = 0 fills C
+ * (y) with +0.0 on the host; M = 0, N = 0 (n = 0) do nothing.  Errors as for
+ * the device calls; C (y) must not overlap an input.
+ */
+int gemm_f16_colmajor_host(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, void* stream);
+int gemv_bf16_host(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, int K, int n, void* stream);
+
+/*
  * Same work as gemm_f16_colmajor / gemv_bf16 / decode_attention_bf16, but asynchronous: validates the
  * arguments, launches on `stream` and returns without waiting.  A device-side
  * watchdog timeout raised by this work is reported by the next

@@ -178,6 +178,25 @@ def test_empty_outputs_are_no_ops_without_a_device(lib):
     assert lib.gemv_bf16(None, None, None, 9, 7, 0, None) == 0
 
 
+def test_host_buffer_calls_validate_without_a_gpu(lib):
+    """Argument checks come before any CUDA call; K = 0 is the empty sum, filled on the host."""
+    import numpy as np
+
+    assert lib.gemm_f16_colmajor_host(None, None, None, -1, 4, 4, None) == 1
+    assert lib.gemv_bf16_host(None, None, None, 4, 4, -2, None) == 1
+    assert lib.gemm_f16_colmajor_host(None, None, None, 0, 4, 4, None) == 0
+    assert lib.gemv_bf16_host(None, None, None, 4, 4, 0, None) == 0
+    c = np.full(12, 0x5A5A, np.uint16)
+    assert lib.gemm_f16_colmajor_host(None, None, c.ctypes.data, 3, 4, 4, None) == 1   # A, B NULL with K > 0
+    a = np.ones(12, np.uint16)
+    assert lib.gemm_f16_colmajor_host(a.ctypes.data, a.ctypes.data, a.ctypes.data, 3, 4, 4, None) == 1   # overlap
+    assert lib.gemm_f16_colmajor_host(None, None, c.ctypes.data, 3, 4, 0, None) == 0
+    assert np.all(c == 0)
+    y = np.full(6, 0x5A5A, np.uint16)
+    assert lib.gemv_bf16_host(None, None, y.ctypes.data, 3, 0, 2, None) == 0
+    assert np.all(y == 0)
+
+
 def test_options_round_trip_and_range_checks(lib):
     assert bsk.get_option("group_m") == 0
     bsk.set_option("group_m", 12)
