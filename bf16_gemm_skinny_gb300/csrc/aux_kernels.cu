@@ -7,13 +7,33 @@
 namespace bsk {
 namespace {
 
+// The 16 bytes that start `m` bytes into `lo` (lo followed by hi, little-endian).
+__device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, unsigned m)
+{
+    const unsigned r = (m & 3u) * 8u;   // bit shift inside a word
+    uint32_t v0, v1, v2, v3, v4;        // words m/4 .. m/4 + 4 of the 32 bytes
+    switch (m >> 2) {
+    case 0: v0 = lo.x; v1 = lo.y; v2 = lo.z; v3 = lo.w; v4 = hi.x; break;
+    case 1: v0 = lo.y; v1 = lo.z; v2 = lo.w; v3 = hi.x; v4 = hi.y; break;
+    case 2: v0 = lo.z; v1 = lo.w; v2 = hi.x; v3 = hi.y; v4 = hi.z; break;
+    default: v0 = lo.w; v1 = hi.x; v2 = hi.y; v3 = hi.z; v4 = hi.w; break;
+    }
+    return make_uint4(__funnelshift_r(v0, v1, r), __funnelshift_r(v1, v2, r), __funnelshift_r(v2, v3, r),
+                      __funnelshift_r(v3, v4, r));
+}
+
 // dst[i + j*ld_dst] = src[i + j*ld_src] for i < inner, j < outer.  The TMA
 // needs 16-byte aligned bases and leading dimensions; the pack gives unaligned
 // operands that shape in a workspace without touching the caller's buffers
 // ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 1: inputs may not be modified).
 // Grid: x over 16-byte groups of a line, y over lines (grid-stride).  The
-// source may have any alignment (element loads); the destination lines are
-// 16-byte aligned (base and ld_dst), so each full group is one 16-byte store.
+// destination lines are 16-byte aligned (base and ld_dst), so each full group
+// is one 16-byte store.  A source group at any byte offset is read as the
+// aligned 16-byte chunk holding its first byte and, unless the offset is 0,
+// the next chunk, then shifted into place (two aligned loads, the second the
+// neighbouring thread's first, instead of one load per element).  Both chunks
+// hold bytes of the group, so neither reaches a page the line does not touch.
+// The last, partial group of a line is copied element by element.
 template <typename T>
 __global__ void __launch_bounds__(256)
     pack_kernel(const T* __restrict__ src, long long ld_src, T* __restrict__ dst, long long ld_dst, int inner,
@@ -27,13 +47,11 @@ __global__ void __launch_bounds__(256)
         const T* s = src + j * ld_src + i0;
         T* d = dst + j * ld_dst + i0;
         if (full) {
-            union {
-                uint4 u;
-                T e[V];
-            } pk;
-#pragma unroll
-            for (int t = 0; t < V; ++t) pk.e[t] = s[t];
-            *reinterpret_cast<uint4*>(d) = pk.u;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(s);
+            const uint4* chunk = reinterpret_cast<const uint4*>(a & ~static_cast<uintptr_t>(15));
+            const unsigned m = static_cast<unsigned>(a & 15u);
+            const uint4 lo = chunk[0];
+            *reinterpret_cast<uint4*>(d) = m == 0u ? lo : realign16(lo, chunk[1], m);
         } else {
             for (long long t = 0; i0 + t < inner; ++t) d[t] = s[t];
         }

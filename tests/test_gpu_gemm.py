@@ -313,3 +313,14 @@ def test_dynamic_tile_order_on_cta_pairs(M, N, K):
         finally:
             bsk.set_option("tile_sched", 0)
     assert np.array_equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("offset", range(8))
+def test_pack_every_base_offset(offset):
+    """Bases at every 2-byte offset inside a 16-byte chunk and odd leading
+    dimensions: the pack's aligned loads and shifts, bit for bit."""
+    M, N, K = 257, 130, 67
+    A, B = operands(M, N, K, "int2")
+    got = run(A, B, M, N, K, offset=offset)
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    assert np.array_equal(got, want)

@@ -281,3 +281,15 @@ def test_stream_k_on_cta_pairs():
         bsk.set_option("stream_k", 0)
     _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", "bf16")
     assert np.array_equal(got, bits)
+
+
+@pytest.mark.parametrize("offset", range(16))
+def test_pack_every_byte_offset(offset):
+    """FP8 operands at every byte offset inside a 16-byte chunk, with odd leading
+    dimensions (every line starts at another offset): the pack's aligned loads
+    and byte shifts, bit for bit."""
+    M, N, K = 200, 72, 131
+    A2, B2 = operands(M, N, K, "int2", "e4m3")
+    got, Af, lda, Bf, ldb = run(A2, B2, "e4m3", "f32", pad_a=3, pad_b=5, offset=offset)
+    _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", "f32")
+    assert np.array_equal(got, bits)
