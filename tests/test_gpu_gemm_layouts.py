@@ -267,3 +267,29 @@ def test_ragged_m_with_aligned_ldc_leaves_padding_alone(M, pad_c):
     got, Af, lda, Bf, ldb = run(0, 0, 0, A2, B2, pad_c=pad_c)   # run() checks the padding
     _, out = want(0, 0, 0, Af, lda, Bf, ldb, M, N, K)
     assert np.array_equal(got, out)
+
+
+@pytest.mark.parametrize("sched", [{"stream_k": 2}, {"stream_k": 2, "gemm_kernel": 1}, {"tile_sched": 2}])
+@pytest.mark.parametrize("order,transa,transb,mode", [
+    (0, 0, 0, 1), (0, 1, 1, 2), (1, 0, 1, 2), (1, 1, 0, 1), (0, 0, 1, 0)])
+def test_schedules_with_layouts_and_bias(sched, order, transa, transb, mode):
+    """Stream-K (on CTA pairs and on single CTAs) and the dynamic tile order with
+    every storage form and a per-row or per-column bias: the owner of a split
+    tile adds the partials before the bias and the single rounding, and a
+    dynamically ordered tile keeps its own bias slice.  Integer inputs and bias:
+    the oracle's bits."""
+    M, N, K = 700, 600, 2100
+    A2, B2 = operands(M, N, K, "int2")
+    bias = None
+    if mode:
+        vals = np.random.default_rng(9).integers(-40, 41, max(M, N))
+        bias = enc(vals)[:M if mode == 1 else N]
+    for k, v in sched.items():
+        bsk.set_option(k, v)
+    try:
+        got, Af, lda, Bf, ldb = run(order, transa, transb, A2, B2, pad_a=2, pad_b=1, pad_c=3, bias=bias, mode=mode)
+    finally:
+        for k in sched:
+            bsk.set_option(k, 0)
+    _, out = want(order, transa, transb, Af, lda, Bf, ldb, M, N, K, bias=bias, mode=mode)
+    assert np.array_equal(got, out), f"{int((got != out).sum())} of {got.size} entries differ"
