@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
     using SM = SplitSmem<HD, G>;
     static_assert(G <= 8, "at most 8 query heads per KV head (rows of the score MMA)");
     static_assert(KS % 2 == 0, "k-steps are loaded two at a time");
+    static_assert(kAttnStages * kAttnTokens <= 32, "the stages' token-validity bits share one 32-bit word");
     const int seg = blockIdx.x;
     const int kvh = blockIdx.y;
     const int seq = blockIdx.z;
