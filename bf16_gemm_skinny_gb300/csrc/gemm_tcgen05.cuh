@@ -28,6 +28,20 @@
 // of tile i overlaps the mainloop of tile i+1.  Tiles are visited in the
 // grouped (GROUP_M) order of "Hygon 优化", section 分组调度.
 //
+// Schedules (the same roles walk the same sequence of (tile, k-blocks)):
+//   * whole tiles, fixed: unit u of U (a CTA, or a CTA pair) takes tiles
+//     u, u + U, ... in the grouped order;
+//   * stream-K: whole waves as above, then the last wave's (tile, k-block)
+//     iterations shared evenly; the unit holding a split tile's first k-block
+//     adds the others' FP32 partials (workspace slots released by GPU-scope
+//     flags) in unit order; the launch is cooperative;
+//   * dynamic order (CTA pairs): one cluster per tile launched; a pair that is
+//     done takes the tile of a cluster whose launch it cancels (cluster launch
+//     control), the answers passed to every role through a small ring.
+// Whole-tile launches are programmatic dependents of the kernel before them:
+// the prologue (barriers, TMEM, tensor-map and L2 prefetches) runs first and
+// griddepcontrol.wait comes before any global read or write.
+//
 // Tails: TMA zero-fills the parts of a box outside the tensor (M, N and K
 // tails contribute zero products; a zero byte is +0 in both FP8 formats) and
 // the TMA store / masked store drop rows and columns outside C ("Hygon 优化",
