@@ -192,17 +192,6 @@ struct GemmOp {
     int bias_mode = 0;
 };
 
-// Copies an operand into the workspace with a 16-byte-multiple leading dimension.
-int pack_operand(const void* src, long long ld_src, void* dst, long long ld_dst, int inner, int outer, int eb,
-                 cudaStream_t s, char* msg, size_t msg_len)
-{
-    if (eb == 1)
-        return bsk::launch_pack_8bit(static_cast<const uint8_t*>(src), ld_src, static_cast<uint8_t*>(dst), ld_dst,
-                                     inner, outer, s, msg, msg_len);
-    return bsk::launch_pack(static_cast<const uint16_t*>(src), ld_src, static_cast<uint16_t*>(dst), ld_dst, inner,
-                            outer, s, msg, msg_len);
-}
-
 // Runs the tcgen05 GEMM on operands in any layout TMA may not take directly:
 // an operand whose base is not 16-byte aligned or whose leading dimension is
 // not a multiple of 16 bytes is packed into a stream-ordered workspace.
@@ -287,16 +276,22 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
         int st = alloc_workspace(ws, a_bytes + b_bytes + sk_part_bytes + sk_flag_bytes, s);
         if (st != BSK_OK) return st;
         uint8_t* base = static_cast<uint8_t*>(ws.ptr);
+        // the operands that need it are copied to a 16-byte-multiple leading
+        // dimension in the workspace, both in one launch
+        bsk::PackCopy copies[2];
+        int n_copies = 0;
         if (!a_ok) {
-            if (pack_operand(op.A, op.lda, base, lda_p, a_inner, a_outer, eb, s, msg, sizeof(msg)))
-                return fail(BSK_ERR_CUDA, "%s", msg);
+            copies[n_copies++] = {op.A, op.lda * eb, base, lda_p * eb, static_cast<long long>(a_inner) * eb, a_outer};
             Ause = base;
         }
         if (!b_ok) {
-            if (pack_operand(op.B, op.ldb, base + a_bytes, ldb_p, b_inner, b_outer, eb, s, msg, sizeof(msg)))
-                return fail(BSK_ERR_CUDA, "%s", msg);
+            copies[n_copies++] = {op.B, op.ldb * eb, base + a_bytes, ldb_p * eb, static_cast<long long>(b_inner) * eb,
+                                  b_outer};
             Buse = base + a_bytes;
         }
+        if (n_copies > 0 &&
+            bsk::launch_pack(copies, n_copies, sms, opt_or(BSK_OPT_PDL, 0) != 1, s, msg, sizeof(msg)))
+            return fail(BSK_ERR_CUDA, "%s", msg);
         if (stream_k) {
             sk_part = reinterpret_cast<float*>(base + a_bytes + b_bytes);
             sk_flag = reinterpret_cast<int*>(base + a_bytes + b_bytes + sk_part_bytes);

@@ -1,4 +1,5 @@
 // aux_kernels.cu -- the operand pack kernel and the bounded-wait test probe.
+#include <algorithm>
 #include <cstdio>
 
 #include "bsk_internal.h"
@@ -22,58 +23,124 @@ __device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uns
                       __funnelshift_r(v3, v4, r));
 }
 
-// dst[i + j*ld_dst] = src[i + j*ld_src] for i < inner, j < outer.  The TMA
-// needs 16-byte aligned bases and leading dimensions; the pack gives unaligned
-// operands that shape in a workspace without touching the caller's buffers
-// ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 1: inputs may not be modified).
-// Grid: x over 16-byte groups of a line, y over lines (grid-stride).  The
-// destination lines are 16-byte aligned (base and ld_dst), so each full group
-// is one 16-byte store.  A source group at any byte offset is read as the
-// aligned 16-byte chunk holding its first byte and, unless the offset is 0,
-// the next chunk, then shifted into place (two aligned loads, the second the
-// neighbouring thread's first, instead of one load per element).  Both chunks
-// hold bytes of the group, so neither reaches a page the line does not touch.
-// The last, partial group of a line is copied element by element.
-template <typename T>
-__global__ void __launch_bounds__(256)
-    pack_kernel(const T* __restrict__ src, long long ld_src, T* __restrict__ dst, long long ld_dst, int inner,
-                int outer)
+// One operand's copy as the kernel sees it: `lines` lines of line_bytes bytes.
+// A step is 32 consecutive 16-byte groups of one line (512 bytes, one per
+// lane; the last group of a line may be partial, and lanes past the line's
+// end idle), numbered line by line.
+struct PackJob {
+    const uint8_t* src;
+    long long ld_src;          // bytes from one source line to the next
+    uint8_t* dst;              // 16-byte aligned
+    long long ld_dst;          // bytes, a multiple of 16
+    unsigned line_bytes;
+    unsigned steps_per_line;
+    unsigned steps;            // steps_per_line x lines, below 2^31
+    unsigned blocks;           // CTAs working on this job
+};
+
+constexpr int kPackThreads = 256;
+constexpr int kPackWarps = kPackThreads / 32;
+constexpr int kPackStages = 6;        // cp.async ring depth per lane
+constexpr int kPackCtasPerSm = 4;     // 4 x 48 KB of ring per SM
+
+__device__ __forceinline__ void pack_cp_async16(uint32_t dst, const void* src)
 {
-    constexpr int V = 16 / static_cast<int>(sizeof(T));
-    const long long i0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * V;
-    if (i0 >= inner) return;
-    const bool full = i0 + V <= inner;
-    for (long long j = blockIdx.y; j < outer; j += gridDim.y) {
-        const T* s = src + j * ld_src + i0;
-        T* d = dst + j * ld_dst + i0;
-        if (full) {
-            const uintptr_t a = reinterpret_cast<uintptr_t>(s);
-            const uint4* chunk = reinterpret_cast<const uint4*>(a & ~static_cast<uintptr_t>(15));
-            const unsigned m = static_cast<unsigned>(a & 15u);
-            const uint4 lo = chunk[0];
-            *reinterpret_cast<uint4*>(d) = m == 0u ? lo : realign16(lo, chunk[1], m);
-        } else {
-            for (long long t = 0; i0 + t < inner; ++t) d[t] = s[t];
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void pack_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void pack_cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// A cursor over a warp's steps: line index and step within the line.
+struct PackCursor {
+    unsigned line, k;
+    __device__ __forceinline__ void next(unsigned steps_per_line)
+    {
+        if (++k == steps_per_line) {
+            k = 0;
+            ++line;
         }
     }
-}
+};
 
-template <typename T>
-int launch_pack_t(const T* src, long long ld_src, T* dst, long long ld_dst, int inner, int outer, cudaStream_t stream,
-                  char* msg, size_t msg_len)
+// dst line l = src line l, byte for byte, for up to two operands in one launch
+// (the first job.blocks CTAs take job 0, the rest job 1).  The TMA needs
+// 16-byte aligned bases and leading dimensions; the pack gives unaligned
+// operands that shape in a workspace without touching the caller's buffers
+// ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 1: inputs may not be modified).
+//
+// Each warp takes a contiguous range of steps.  A lane's group at any byte
+// offset is read as the aligned 16-byte chunk holding its first byte and,
+// unless the offset is 0, the next chunk: both hold bytes of the group, so
+// neither reaches a page the line does not touch.  The chunks go through a
+// per-lane ring of kPackStages slots in shared memory with cp.async, so each
+// SM keeps its warps' next five steps of reads in flight while it shifts
+// the current step into place and stores it (one aligned 16-byte store per
+// group).  Every lane reads back only what it copied itself: the commit /
+// wait_group counting is the only synchronisation, and it always completes.
+// The partial last group of a line is copied byte by byte.
+__global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_kernel(PackJob j0, PackJob j1)
 {
-    if (inner <= 0 || outer <= 0) return 0;
-    constexpr int V = 16 / static_cast<int>(sizeof(T));
-    const long long groups = (static_cast<long long>(inner) + V - 1) / V;
-    const unsigned gx = static_cast<unsigned>((groups + 255) / 256);
-    const unsigned gy = static_cast<unsigned>(outer < 65535 ? outer : 65535);
-    pack_kernel<T><<<dim3(gx, gy, 1), 256, 0, stream>>>(src, ld_src, dst, ld_dst, inner, outer);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
-        return 1;
+    __shared__ __align__(16) uint4 ring[kPackWarps][kPackStages][2][32];
+    griddep_wait();               // the source may be the previous kernel's output
+    griddep_launch_dependents();  // the GEMM's prologue may start; it waits for this grid's completion
+    const bool second = blockIdx.x >= j0.blocks;
+    const uint8_t* const src = second ? j1.src : j0.src;
+    uint8_t* const dst = second ? j1.dst : j0.dst;
+    const long long ld_src = second ? j1.ld_src : j0.ld_src;
+    const long long ld_dst = second ? j1.ld_dst : j0.ld_dst;
+    const unsigned line_bytes = second ? j1.line_bytes : j0.line_bytes;
+    const unsigned spl = second ? j1.steps_per_line : j0.steps_per_line;
+    const unsigned steps = second ? j1.steps : j0.steps;
+    const unsigned blocks = second ? j1.blocks : j0.blocks;
+    const unsigned b = second ? blockIdx.x - j0.blocks : blockIdx.x;
+    const unsigned warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const unsigned long long nw = static_cast<unsigned long long>(blocks) * kPackWarps;
+    const unsigned long long w = static_cast<unsigned long long>(b) * kPackWarps + warp;
+    const unsigned s0 = static_cast<unsigned>(steps * w / nw);
+    const unsigned n = static_cast<unsigned>(steps * (w + 1) / nw) - s0;
+    const unsigned off = lane * 16u;   // the lane's group within a step, in bytes
+    PackCursor in{s0 / spl, s0 % spl};
+    PackCursor out = in;
+
+    auto issue = [&](int slot) {
+        const unsigned g = in.k * 512u + off;
+        if (g + 16u <= line_bytes) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(src + in.line * ld_src + g);
+            const uint8_t* chunk = reinterpret_cast<const uint8_t*>(a & ~static_cast<uintptr_t>(15));
+            pack_cp_async16(smem_u32(&ring[warp][slot][0][lane]), chunk);
+            if ((a & 15u) != 0u) pack_cp_async16(smem_u32(&ring[warp][slot][1][lane]), chunk + 16);
+        }
+        pack_cp_commit();
+        in.next(spl);
+    };
+
+#pragma unroll
+    for (int t = 0; t < kPackStages - 1; ++t) {
+        if (static_cast<unsigned>(t) < n) issue(t);
+        else pack_cp_commit();
     }
-    return 0;
+    int slot = 0;
+    for (unsigned i = 0; i < n; ++i) {
+        // the slot consumed last iteration takes the step kPackStages - 1 ahead
+        const int ahead = slot == 0 ? kPackStages - 1 : slot - 1;
+        if (i + (kPackStages - 1) < n) issue(ahead);
+        else pack_cp_commit();
+        pack_cp_wait<kPackStages - 1>();   // this lane's copies of step i have landed
+        const unsigned g = out.k * 512u + off;
+        const uint8_t* sp = src + out.line * ld_src + g;
+        uint8_t* dp = dst + out.line * ld_dst + g;
+        if (g + 16u <= line_bytes) {
+            const unsigned m = static_cast<unsigned>(reinterpret_cast<uintptr_t>(sp) & 15u);
+            const uint4 lo = ring[warp][slot][0][lane];
+            *reinterpret_cast<uint4*>(dp) = m == 0u ? lo : realign16(lo, ring[warp][slot][1][lane], m);
+        } else if (g < line_bytes) {
+            for (unsigned t = 0; t < line_bytes - g; ++t) dp[t] = sp[t];
+        }
+        out.next(spl);
+        slot = slot == kPackStages - 1 ? 0 : slot + 1;
+    }
+    pack_cp_wait<0>();   // the trailing (empty) groups
 }
 
 // C(m,n) = bias value (or +0.0) for m < M, n < N, C(m,n) at C[m + n*ldc]: the
@@ -116,16 +183,59 @@ __global__ void wait_timeout_probe_kernel(int* status, unsigned long long limit_
 
 }  // namespace
 
-int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long ld_dst, int inner, int outer,
-                cudaStream_t stream, char* msg, size_t msg_len)
+int launch_pack(const PackCopy* copies, int n, int sms, bool pdl, cudaStream_t stream, char* msg, size_t msg_len)
 {
-    return launch_pack_t<uint16_t>(src, ld_src, dst, ld_dst, inner, outer, stream, msg, msg_len);
-}
-
-int launch_pack_8bit(const uint8_t* src, long long ld_src, uint8_t* dst, long long ld_dst, int inner, int outer,
-                     cudaStream_t stream, char* msg, size_t msg_len)
-{
-    return launch_pack_t<uint8_t>(src, ld_src, dst, ld_dst, inner, outer, stream, msg, msg_len);
+    PackJob jobs[2] = {};
+    int nj = 0;
+    auto flush = [&]() -> int {
+        // persistent grid, split between the jobs by their steps (at least one
+        // CTA each, no more than one warp per step)
+        const unsigned long long per_cta = kPackWarps;
+        const unsigned long long u0 = jobs[0].steps, u1 = nj > 1 ? jobs[1].steps : 0ull;
+        const unsigned long long total = static_cast<unsigned long long>(sms > 0 ? sms : 1) * kPackCtasPerSm;
+        unsigned long long b0 = nj > 1 ? (total * u0 + (u0 + u1) / 2) / (u0 + u1) : total;
+        if (b0 < 1) b0 = 1;
+        unsigned long long b1 = nj > 1 ? (total > b0 ? total - b0 : 1ull) : 0ull;
+        b0 = std::min(b0, (u0 + per_cta - 1) / per_cta);
+        b1 = std::min(b1, (u1 + per_cta - 1) / per_cta);
+        jobs[0].blocks = static_cast<unsigned>(b0);
+        jobs[1].blocks = static_cast<unsigned>(b1);
+        cudaError_t e = launch_kernel(pack_kernel, dim3(static_cast<unsigned>(b0 + b1)), dim3(kPackThreads), 0,
+                                      stream, pdl, jobs[0], jobs[1]);
+        nj = 0;
+        jobs[0] = PackJob{};
+        jobs[1] = PackJob{};
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
+            return 1;
+        }
+        return 0;
+    };
+    for (int i = 0; i < n; ++i) {
+        const PackCopy& c = copies[i];
+        if (c.line_bytes <= 0 || c.lines <= 0) continue;
+        if (c.line_bytes > (1LL << 31)) {
+            snprintf(msg, msg_len, "pack: line of %lld bytes is too long", c.line_bytes);
+            return 1;
+        }
+        const unsigned long long spl = (static_cast<unsigned long long>(c.line_bytes) + 511) / 512;
+        // keep each job's step count below 2^31 (32-bit step arithmetic in the kernel)
+        const long long lines_per_job = static_cast<long long>(std::max(1ull, (1ull << 31) / spl - 1));
+        for (long long l0 = 0; l0 < c.lines; l0 += lines_per_job) {
+            const long long nl = std::min(lines_per_job, c.lines - l0);
+            PackJob& j = jobs[nj++];
+            j.src = static_cast<const uint8_t*>(c.src) + l0 * c.ld_src;
+            j.ld_src = c.ld_src;
+            j.dst = static_cast<uint8_t*>(c.dst) + l0 * c.ld_dst;
+            j.ld_dst = c.ld_dst;
+            j.line_bytes = static_cast<unsigned>(c.line_bytes);
+            j.steps_per_line = static_cast<unsigned>(spl);
+            j.steps = static_cast<unsigned>(spl * static_cast<unsigned long long>(nl));
+            if (nj == 2 && flush()) return 1;
+        }
+    }
+    if (nj > 0 && flush()) return 1;
+    return 0;
 }
 
 int launch_fill_bias(uint16_t* C, long long ldc, int M, int N, const uint16_t* bias, int bias_mode,

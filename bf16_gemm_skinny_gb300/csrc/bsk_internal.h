@@ -175,14 +175,21 @@ int launch_decode_attention(const AttnLaunch& a, cudaStream_t stream, char* msg,
 // CTAs of the attention's split kernel resident per SM for this head shape (>= 1).
 int attention_ctas_per_sm(int head_dim, int q_per_kv);
 
-// Copy an `outer` x `inner` matrix of 16-bit elements (inner contiguous) from
-// leading dimension ld_src to ld_dst.  The source is only read.
-int launch_pack(const uint16_t* src, long long ld_src, uint16_t* dst, long long ld_dst, int inner, int outer,
-                cudaStream_t stream, char* msg, size_t msg_len);
+// One operand copy for launch_pack: `lines` lines of line_bytes bytes, line l
+// read from src + l * ld_src and written to dst + l * ld_dst (bytes; dst and
+// ld_dst 16-byte aligned).  The source is only read.
+struct PackCopy {
+    const void* src;
+    long long ld_src;
+    void* dst;
+    long long ld_dst;
+    long long line_bytes;
+    long long lines;
+};
 
-// The same for 8-bit elements.
-int launch_pack_8bit(const uint8_t* src, long long ld_src, uint8_t* dst, long long ld_dst, int inner, int outer,
-                     cudaStream_t stream, char* msg, size_t msg_len);
+// Enqueues the n copies (two to a launch) on `stream`, as programmatic
+// dependents of the kernel before them when pdl is set.
+int launch_pack(const PackCopy* copies, int n, int sms, bool pdl, cudaStream_t stream, char* msg, size_t msg_len);
 
 // C(m,n) = bias[m] (mode 1), bias[n] (mode 2) or +0.0 (mode 0) for the M x N
 // column-major C with leading dimension ldc: the GEMM with K == 0.

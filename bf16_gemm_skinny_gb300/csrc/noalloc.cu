@@ -170,16 +170,21 @@ extern "C" int gemm_f16_colmajor_noalloc(const uint16_t* A, const uint16_t* B, u
     char msg[512] = "";
     const uint16_t* Ause = A;
     const uint16_t* Buse = B;
+    bsk::PackCopy copies[2];
+    int n_copies = 0;
     if (!a_ok) {
         uint16_t* Ap = reinterpret_cast<uint16_t*>(d->scratch);
-        if (bsk::launch_pack(A, M, Ap, lda_p, M, K, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
+        copies[n_copies++] = {A, M * 2LL, Ap, lda_p * 2LL, M * 2LL, K};
         Ause = Ap;
     }
     if (!b_ok) {
         uint16_t* Bp = reinterpret_cast<uint16_t*>(d->scratch + a_pack);
-        if (bsk::launch_pack(B, K, Bp, ldb_p, K, N, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
+        copies[n_copies++] = {B, K * 2LL, Bp, ldb_p * 2LL, K * 2LL, N};
         Buse = Bp;
     }
+    if (n_copies > 0 && bsk::launch_pack(copies, n_copies, d->sms, option_or(BSK_OPT_PDL, 0) != 1, s, msg,
+                                         sizeof(msg)))
+        return fail(BSK_ERR_CUDA, "%s", msg);
     bsk::GemmLaunch g;
     g.A = Ause;
     g.lda = lda_p;

@@ -315,6 +315,23 @@ def test_dynamic_tile_order_on_cta_pairs(M, N, K):
     assert np.array_equal(outs[1], outs[2])
 
 
+@pytest.mark.parametrize("sms,offset", [(1, 3), (2, 0), (5, 7)])
+def test_pack_on_few_sms(sms, offset):
+    """The pack on a grid capped to a few SMs: each warp streams hundreds of
+    512-byte steps through its ring (many wrap-arounds, line changes inside a
+    warp's range, the partial last group of every line), both operands in one
+    launch; the result must equal the oracle's bit for bit."""
+    M, N, K = 1001, 515, 1037
+    A, B = operands(M, N, K, "int2")
+    bsk.set_option("num_sms", sms)
+    try:
+        got = run(A, B, M, N, K, offset=offset)
+    finally:
+        bsk.set_option("num_sms", 0)
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    assert np.array_equal(got, want)
+
+
 @pytest.mark.parametrize("offset", range(8))
 def test_pack_every_base_offset(offset):
     """Bases at every 2-byte offset inside a 16-byte chunk and odd leading
