@@ -492,12 +492,14 @@ int enqueue_gemv_bf16(const uint16_t* W, const uint16_t* x, uint16_t* y, int M, 
         cudaError_t e = cudaMemsetAsync(y, 0, y_bytes, s);
         return e == cudaSuccess ? BSK_OK : fail_cuda(e, "cudaMemsetAsync");
     }
-    // n <= 2: the CUDA-core GEMV.  From n = 3 on the tensor-core skinny GEMM
-    // (128 x 32 tiles, deep TMA ring) streams W at least as fast: the CUDA-core
-    // kernels become FMA- and issue-bound as the token count grows (measured on
-    // GB300 at 34816 x 5120: equal at n = 3, 72 vs 114 us at n = 8).
+    // n <= 3: the CUDA-core GEMV.  From n = 4 on the tensor-core skinny GEMM
+    // (128 x 32 tiles, deep TMA ring) streams W faster: the CUDA-core kernels
+    // become FMA- and issue-bound as the token count grows.  Measured on GB300 at
+    // 34816 x 5120 in chains of back-to-back launches: n = 3 56.0 vs 57.9 us,
+    // n = 4 59.5 vs 57.7 us (best CUDA-core configuration vs tensor cores),
+    // n = 8 75.0 vs 57.4 us.
     const long long gemv_kernel = opt_or(BSK_OPT_GEMV_KERNEL, 0);
-    const bool cuda_core = n <= 8 && (gemv_kernel == 0 ? n <= 2 : gemv_kernel != 5);
+    const bool cuda_core = n <= 8 && (gemv_kernel == 0 ? n <= 3 : gemv_kernel != 5);
     if (cuda_core) {
         bsk::GemvLaunch g;
         g.W = W;

@@ -1,5 +1,5 @@
 // gemv.cu -- decode GEMV / skinny GEMM on the CUDA cores: y = x W^T, n <= 8 tokens
-// (by default gemv_bf16 runs n <= 2 here and larger n on the tensor cores).
+// (by default gemv_bf16 runs n <= 3 here and larger n on the tensor cores).
 //
 // DCU decode-GEMV article (forum.sourcefind.cn): section 6.1 fixes the shapes
 // (X:[n,k], W:[m,k], Y:[n,m], all row-major) and section 6.2 the work split:
@@ -847,15 +847,17 @@ int try_launch_tokpair(const GemvLaunch& g, cudaStream_t stream, char* msg, size
 }
 
 // Kernel choice for the aligned path.  Measured on the 34816 x 5120 decode
-// shape: n <= 2 streams fastest from registers (the arithmetic is light and
-// the loads of U chunks per lane keep HBM busy); for n = 3..4 the cp.async
-// ring keeps loads in flight while the arithmetic runs (x in FP32); for
-// n >= 5 the FMAs dominate and the token-paired kernel does the fewest
-// instructions per weight.
+// shape: n <= 3 streams fastest from registers (the arithmetic is light and
+// the loads of U chunks per lane keep HBM busy; 4 rows per warp for n <= 2,
+// 2 rows for n = 3, whose 3 x 4 accumulators per row leave fewer registers
+// for loads in flight); at n = 4 the cp.async ring keeps loads in flight
+// while the arithmetic runs (x in FP32); for n >= 5 the FMAs dominate and
+// the token-paired kernel does the fewest instructions per weight.  (By
+// default gemv_bf16 sends n >= 4 to the tensor cores.)
 template <int NT>
 int launch_vec_any(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
-    const int kernel = g.kernel != 0 ? g.kernel : (NT <= 2 ? 1 : (NT <= 4 ? 2 : 4));
+    const int kernel = g.kernel != 0 ? g.kernel : (NT <= 3 ? 1 : (NT <= 4 ? 2 : 4));
     if (kernel == 4) {
         const int rows = g.rows_per_warp > 0 ? g.rows_per_warp : 8;
         int status = 0;
@@ -873,7 +875,7 @@ int launch_vec_any(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t m
             return 1;
         }
     }
-    const int rows = g.rows_per_warp > 0 ? g.rows_per_warp : 4;
+    const int rows = g.rows_per_warp > 0 ? g.rows_per_warp : (kernel == 1 && NT == 3 ? 2 : 4);
     if (kernel == 2 || kernel == 3 || (kernel == 4)) {
         GemvLaunch gk = g;
         gk.kernel = kernel == 4 ? 3 : kernel;

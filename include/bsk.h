@@ -7,7 +7,7 @@
  *                      any leading dimensions and an optional fused bias;
  *   gemm_fp8           FP8 (E4M3 / E5M2) GEMM with FP32 accumulation;
  *   gemv_bf16          BF16 linear layer y = x W^T: the HBM-bound decode GEMV for
- *                      n <= 2 tokens (CUDA cores), the tensor-core GEMM for
+ *                      n <= 3 tokens (CUDA cores), the tensor-core GEMM for
  *                      larger n (skinny decode batches, prefill projections);
  *   decode_attention_bf16  split-KV decode attention over a paged BF16 KV cache.
  *
@@ -149,8 +149,8 @@ int gemm_fp8(int format, const uint8_t* A, int lda, const uint8_t* B, int ldb, v
  *     y : [n, M] row-major   y(t,j) = y[t*M + j] = sum_k x(t,k) W(j,k)
  * Section 2: n = 1 is the decode GEMV, large n the prefill GEMM.
  *
- * n <= 2 runs the CUDA-core GEMV (128-bit weight stream, warp-shuffle
- * reduction); n >= 3 runs the tcgen05 GEMM with both operands K-major (tiles
+ * n <= 3 runs the CUDA-core GEMV (128-bit weight stream, warp-shuffle
+ * reduction); n >= 4 runs the tcgen05 GEMM with both operands K-major (tiles
  * as narrow as 128 x 32 for small n).
  * Any M, K, n >= 0 are accepted (unaligned W/x or K % 8 != 0 take a scalar
  * CUDA-core variant, or the pack workspace on the tensor-core path).  y must
@@ -298,8 +298,8 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_GEMV_KERNEL      kernel of gemv_bf16 for n <= 8: 1 register streaming,
  *                            2 cp.async-pipelined, 3 pipelined with x kept in BF16,
  *                            4 token-paired (n >= 5) -- the CUDA-core GEMVs -- or 5 the
- *                            tensor-core skinny GEMM (default: 1 for n <= 2, 5 for
- *                            n >= 3; a CUDA-core kernel whose buffers do not fit in
+ *                            tensor-core skinny GEMM (default: 1 for n <= 3, 5 for
+ *                            n >= 4; a CUDA-core kernel whose buffers do not fit in
  *                            shared memory falls back to another)
  *   BSK_OPT_STREAM_K         GEMM schedule: 1 whole tiles, 2 stream-K (every SM -- or CTA
  *                            pair -- an equal share of the tile x k-block iterations of the

@@ -119,12 +119,12 @@ def test_all_kernels_full_decode_shape(kernel, n):
     check_tolerance(got, ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"gemv kernel={kernel} n={n}")
 
 
-@pytest.mark.parametrize("M,K,n,offset", [(517, 1001, 3, 0), (300, 4096, 8, 1), (64, 7, 1, 0)])
+@pytest.mark.parametrize("M,K,n,offset", [(517, 1001, 3, 0), (517, 1001, 4, 0), (300, 4096, 8, 1), (64, 7, 1, 0)])
 @pytest.mark.parametrize("kernel", [0, 1])
 def test_scalar_variant(M, K, n, offset, kernel):
     """K not a multiple of 8, or unaligned pointers: the scalar CUDA-core kernel
-    (kernel 1 requested), or by default for n >= 3 the tensor-core path on
-    packed operands."""
+    (kernel 1 requested, or by default for n <= 3), or by default for n >= 4
+    the tensor-core path on packed operands."""
     W, x = operands(M, K, n, False)
     ref, _ = oracle.linear_bf16(W, x, M, K, n)
     bsk.set_option("gemv_kernel", kernel)

@@ -111,7 +111,7 @@ def test_fp16_inf_and_nan_propagate():
 
 @pytest.mark.parametrize("n", [1, 4, 8, 24])
 def test_bf16_linear_subnormals_and_specials(n):
-    """The linear layer (CUDA-core GEMV for n <= 2, tensor cores beyond): BF16
+    """The linear layer (CUDA-core GEMV for n <= 3, tensor cores beyond): BF16
     subnormal weights with subnormal and normal results, an Inf and a NaN."""
     import torch
 
