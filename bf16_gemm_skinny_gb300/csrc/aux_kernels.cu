@@ -40,8 +40,8 @@ struct PackJob {
 
 constexpr int kPackThreads = 256;
 constexpr int kPackWarps = kPackThreads / 32;
-constexpr int kPackStages = 6;        // cp.async ring depth per lane
-constexpr int kPackCtasPerSm = 4;     // 4 x 48 KB of ring per SM
+constexpr int kPackStages = 8;        // cp.async ring depth per warp
+constexpr int kPackCtasPerSm = 4;
 
 __device__ __forceinline__ void pack_cp_async16(uint32_t dst, const void* src)
 {
@@ -51,14 +51,18 @@ __device__ __forceinline__ void pack_cp_commit() { asm volatile("cp.async.commit
 template <int N>
 __device__ __forceinline__ void pack_cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// A cursor over a warp's steps: line index and step within the line.
+// A cursor over a warp's steps: the current line's source and destination
+// starts and the step within the line.
 struct PackCursor {
-    unsigned line, k;
-    __device__ __forceinline__ void next(unsigned steps_per_line)
+    const uint8_t* s;
+    uint8_t* d;
+    unsigned k;
+    __device__ __forceinline__ void next(unsigned steps_per_line, long long ld_src, long long ld_dst)
     {
         if (++k == steps_per_line) {
             k = 0;
-            ++line;
+            s += ld_src;
+            d += ld_dst;
         }
     }
 };
@@ -69,19 +73,21 @@ struct PackCursor {
 // operands that shape in a workspace without touching the caller's buffers
 // ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 1: inputs may not be modified).
 //
-// Each warp takes a contiguous range of steps.  A lane's group at any byte
-// offset is read as the aligned 16-byte chunk holding its first byte and,
-// unless the offset is 0, the next chunk: both hold bytes of the group, so
-// neither reaches a page the line does not touch.  The chunks go through a
-// per-lane ring of kPackStages slots in shared memory with cp.async, so each
-// SM keeps its warps' next five steps of reads in flight while it shifts
-// the current step into place and stores it (one aligned 16-byte store per
-// group).  Every lane reads back only what it copied itself: the commit /
-// wait_group counting is the only synchronisation, and it always completes.
-// The partial last group of a line is copied byte by byte.
+// Each warp takes a contiguous range of steps.  A step's 32 groups start m
+// bytes past a 16-byte boundary (m is the line's, the same for the whole
+// warp), so they span 33 aligned source chunks: lane l copies chunk l with
+// cp.async and lane 31 also chunk 32, each only if it holds bytes of a full
+// group (so no copy reaches a page the line does not touch).  The chunks go
+// through a per-warp ring of kPackStages steps in shared memory, so each SM
+// keeps its warps' next seven steps of reads in flight.  After its own
+// copies land (wait_group), a __syncwarp lets lane l read chunk l + 1 of its
+// neighbour; the two chunks are shifted into place and stored with one
+// aligned 16-byte store.  A second __syncwarp keeps the slot from being
+// refilled before every lane has read it.  The partial last group of a line
+// is copied byte by byte.
 __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_kernel(PackJob j0, PackJob j1)
 {
-    __shared__ __align__(16) uint4 ring[kPackWarps][kPackStages][2][32];
+    __shared__ __align__(16) uint4 ring[kPackWarps][kPackStages][33];
     griddep_wait();               // the source may be the previous kernel's output
     griddep_launch_dependents();  // the GEMM's prologue may start; it waits for this grid's completion
     const bool second = blockIdx.x >= j0.blocks;
@@ -100,19 +106,23 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_kernel(Pack
     const unsigned s0 = static_cast<unsigned>(steps * w / nw);
     const unsigned n = static_cast<unsigned>(steps * (w + 1) / nw) - s0;
     const unsigned off = lane * 16u;   // the lane's group within a step, in bytes
-    PackCursor in{s0 / spl, s0 % spl};
+    const unsigned line0 = s0 / spl;
+    PackCursor in{src + line0 * ld_src, dst + line0 * ld_dst, s0 % spl};
     PackCursor out = in;
 
     auto issue = [&](int slot) {
         const unsigned g = in.k * 512u + off;
-        if (g + 16u <= line_bytes) {
-            const uintptr_t a = reinterpret_cast<uintptr_t>(src + in.line * ld_src + g);
-            const uint8_t* chunk = reinterpret_cast<const uint8_t*>(a & ~static_cast<uintptr_t>(15));
-            pack_cp_async16(smem_u32(&ring[warp][slot][0][lane]), chunk);
-            if ((a & 15u) != 0u) pack_cp_async16(smem_u32(&ring[warp][slot][1][lane]), chunk + 16);
-        }
+        const uintptr_t a = reinterpret_cast<uintptr_t>(in.s) + g;
+        const unsigned m = static_cast<unsigned>(a & 15u);
+        const uint8_t* chunk = reinterpret_cast<const uint8_t*>(a & ~static_cast<uintptr_t>(15));
+        // chunk `lane` holds the start of this lane's group and, when m > 0, the
+        // end of the previous lane's group
+        const bool full = g + 16u <= line_bytes;
+        if (full || (m != 0u && lane != 0u && g <= line_bytes))
+            pack_cp_async16(smem_u32(&ring[warp][slot][lane]), chunk);
+        if (lane == 31u && m != 0u && full) pack_cp_async16(smem_u32(&ring[warp][slot][32]), chunk + 16);
         pack_cp_commit();
-        in.next(spl);
+        in.next(spl, ld_src, ld_dst);
     };
 
 #pragma unroll
@@ -127,17 +137,18 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_kernel(Pack
         if (i + (kPackStages - 1) < n) issue(ahead);
         else pack_cp_commit();
         pack_cp_wait<kPackStages - 1>();   // this lane's copies of step i have landed
+        __syncwarp();                      // ... and so have its neighbours'
         const unsigned g = out.k * 512u + off;
-        const uint8_t* sp = src + out.line * ld_src + g;
-        uint8_t* dp = dst + out.line * ld_dst + g;
+        const uint8_t* sp = out.s + g;
         if (g + 16u <= line_bytes) {
             const unsigned m = static_cast<unsigned>(reinterpret_cast<uintptr_t>(sp) & 15u);
-            const uint4 lo = ring[warp][slot][0][lane];
-            *reinterpret_cast<uint4*>(dp) = m == 0u ? lo : realign16(lo, ring[warp][slot][1][lane], m);
+            const uint4 lo = ring[warp][slot][lane];
+            *reinterpret_cast<uint4*>(out.d + g) = m == 0u ? lo : realign16(lo, ring[warp][slot][lane + 1], m);
         } else if (g < line_bytes) {
-            for (unsigned t = 0; t < line_bytes - g; ++t) dp[t] = sp[t];
+            for (unsigned t = 0; t < line_bytes - g; ++t) out.d[g + t] = sp[t];
         }
-        out.next(spl);
+        __syncwarp();                      // every lane has read the slot before it is refilled
+        out.next(spl, ld_src, ld_dst);
         slot = slot == kPackStages - 1 ? 0 : slot + 1;
     }
     pack_cp_wait<0>();   // the trailing (empty) groups
