@@ -41,16 +41,19 @@ OPTIONS = {
     "stream_k": 11,
     "pdl": 12,
     "tile_sched": 13,
+    "block_m": 14,
 }
 
-# Every symbol include/bsk.h declares.
+# Every symbol include/bsk.h (the C ABI) declares.
 EXPORTS = (
     "gemm_f16_colmajor", "gemv_bf16", "bsk_gemm_f16_colmajor_enqueue", "bsk_gemv_bf16_enqueue",
-    "bsk_stream_check", "bsk_last_error", "bsk_status_string", "bsk_version", "bsk_tile_coord",
-    "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout", "gemm_f16_colmajor_noalloc",
+    "bsk_stream_check", "bsk_last_error", "bsk_status_string", "bsk_version", "gemm_f16_colmajor_noalloc",
     "decode_attention_bf16", "bsk_decode_attention_bf16_enqueue", "gemm_f16", "bsk_gemm_f16_enqueue",
     "gemm_fp8", "bsk_gemm_fp8_enqueue", "gemm_f16_colmajor_host", "gemv_bf16_host",
 )
+# Tuning options and test hooks (csrc/bsk_tuning.h): exported for the tests and
+# the benchmark, not part of the C ABI.
+TUNING_EXPORTS = ("bsk_tile_coord", "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout")
 
 COL_MAJOR, ROW_MAJOR = 0, 1
 BIAS_NONE, BIAS_ROW, BIAS_COLUMN = 0, 1, 2

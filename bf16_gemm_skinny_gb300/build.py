@@ -35,7 +35,7 @@ def _sources():
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        [os.path.join(INCLUDE, "bsk.h"), os.path.abspath(__file__)]
+        glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
 def is_stale() -> bool:

@@ -21,6 +21,7 @@
 
 #include "bsk.h"
 #include "bsk_internal.h"
+#include "bsk_tuning.h"
 
 namespace {
 
@@ -45,7 +46,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 14;
+constexpr int kNumOpts = 15;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -76,7 +77,12 @@ DeviceInfo g_dev[kMaxDevices];
 volatile int* g_status_host = nullptr;
 int* g_status_dev = nullptr;
 
-int prepare_device(int* sms_out)
+// Checks the current device (compute capability 10.3) and returns the SM
+// count the GEMMs may use.  With `status_word` set it also creates, once per
+// process, the pinned host-mapped status word the regular calls report
+// device-side timeouts through (the fixed-scratch path passes false: it
+// allocates nothing and brings its own status word).
+int prepare_device(int* sms_out, bool status_word = true)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -95,7 +101,7 @@ int prepare_device(int* sms_out)
     if (!d.supported)
         return fail(BSK_ERR_UNSUPPORTED_DEVICE, "device %d has compute capability %d.%d; this library is built for 10.3 (sm_103a)",
                     dev, d.major, d.minor);
-    if (g_status_host == nullptr) {
+    if (status_word && g_status_host == nullptr) {
         void* h = nullptr;
         e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable);
         if (e != cudaSuccess) return fail_cuda(e, "cudaHostAlloc(status word)");
@@ -192,26 +198,72 @@ struct GemmOp {
     int bias_mode = 0;
 };
 
-// Runs the tcgen05 GEMM on operands in any layout TMA may not take directly:
-// an operand whose base is not 16-byte aligned or whose leading dimension is
-// not a multiple of 16 bytes is packed into a stream-ordered workspace.
-int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
+// Which operands must be packed before the TMA can read them (base not
+// 16-byte aligned, or leading dimension not a multiple of 16 bytes), their
+// padded leading dimensions and their workspace bytes (each rounded to 256).
+struct PackPlan {
+    int eb = 2;                   // element bytes of A and B
+    int a_inner = 0, a_outer = 0;  // stored extents: `inner` contiguous elements in each of `outer` lines
+    int b_inner = 0, b_outer = 0;
+    bool a_ok = true, b_ok = true;
+    long long lda_p = 0, ldb_p = 0;
+    size_t a_bytes = 0, b_bytes = 0;
+};
+
+PackPlan plan_pack(const GemmOp& op)
 {
+    PackPlan pp;
     const bool force_pack = opt_or(BSK_OPT_FORCE_PACK, 0) != 0;
     const bool fp8 = op.in_type == bsk::kInE4M3 || op.in_type == bsk::kInE5M2;
-    const int eb = fp8 ? 1 : 2;              // element bytes of A and B
-    const long long ld_unit = 16 / eb;       // elements per 16 bytes
-    // stored extents: `inner` contiguous elements in each of `outer` lines
-    const int a_inner = op.a_mn_major ? op.M : op.K, a_outer = op.a_mn_major ? op.K : op.M;
-    const int b_inner = op.b_mn_major ? op.N : op.K, b_outer = op.b_mn_major ? op.K : op.N;
-    const bool a_ok = !force_pack && aligned16(op.A) && (op.lda % ld_unit == 0);
-    const bool b_ok = !force_pack && aligned16(op.B) && (op.ldb % ld_unit == 0);
-    const long long lda_p = a_ok ? op.lda : (a_inner + ld_unit - 1) / ld_unit * ld_unit;
-    const long long ldb_p = b_ok ? op.ldb : (b_inner + ld_unit - 1) / ld_unit * ld_unit;
-    size_t a_bytes = a_ok ? 0 : static_cast<size_t>(lda_p) * a_outer * eb;
-    size_t b_bytes = b_ok ? 0 : static_cast<size_t>(ldb_p) * b_outer * eb;
-    a_bytes = (a_bytes + 255) / 256 * 256;
-    b_bytes = (b_bytes + 255) / 256 * 256;
+    pp.eb = fp8 ? 1 : 2;
+    const long long ld_unit = 16 / pp.eb;   // elements per 16 bytes
+    pp.a_inner = op.a_mn_major ? op.M : op.K;
+    pp.a_outer = op.a_mn_major ? op.K : op.M;
+    pp.b_inner = op.b_mn_major ? op.N : op.K;
+    pp.b_outer = op.b_mn_major ? op.K : op.N;
+    pp.a_ok = !force_pack && aligned16(op.A) && (op.lda % ld_unit == 0);
+    pp.b_ok = !force_pack && aligned16(op.B) && (op.ldb % ld_unit == 0);
+    // a packed line starts on a 128-byte boundary (one TMA box row never
+    // straddles two 128-byte L2 lines more than it must)
+    const long long pad_unit = 128 / pp.eb;
+    pp.lda_p = pp.a_ok ? op.lda : (pp.a_inner + pad_unit - 1) / pad_unit * pad_unit;
+    pp.ldb_p = pp.b_ok ? op.ldb : (pp.b_inner + pad_unit - 1) / pad_unit * pad_unit;
+    const size_t a_bytes = pp.a_ok ? 0 : static_cast<size_t>(pp.lda_p) * pp.a_outer * pp.eb;
+    const size_t b_bytes = pp.b_ok ? 0 : static_cast<size_t>(pp.ldb_p) * pp.b_outer * pp.eb;
+    pp.a_bytes = (a_bytes + 255) / 256 * 256;
+    pp.b_bytes = (b_bytes + 255) / 256 * 256;
+    return pp;
+}
+
+// The GemmOp of gemm_f16_colmajor(A, B, C, M, N, K).
+GemmOp colmajor_op(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K)
+{
+    GemmOp op;
+    op.A = A;
+    op.lda = M > 1 ? M : 1;
+    op.B = B;
+    op.ldb = K > 1 ? K : 1;
+    op.C = C;
+    op.ldc = M > 1 ? M : 1;
+    op.M = M;
+    op.N = N;
+    op.K = K;
+    return op;
+}
+
+// Runs the tcgen05 GEMM on operands in any layout TMA may not take directly:
+// an operand whose base is not 16-byte aligned or whose leading dimension is
+// not a multiple of 16 bytes is packed into a stream-ordered workspace (or
+// into `fixed`, when given).
+int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch* fixed = nullptr)
+{
+    const PackPlan pp = plan_pack(op);
+    const bool fp8 = op.in_type == bsk::kInE4M3 || op.in_type == bsk::kInE5M2;
+    const int eb = pp.eb;
+    const int a_inner = pp.a_inner, a_outer = pp.a_outer, b_inner = pp.b_inner, b_outer = pp.b_outer;
+    const bool a_ok = pp.a_ok, b_ok = pp.b_ok;
+    const long long lda_p = pp.lda_p, ldb_p = pp.ldb_p;
+    const size_t a_bytes = pp.a_bytes, b_bytes = pp.b_bytes;
 
     // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
     // tile, deep ring: the weight stream sets the pace), else 256 on CTA pairs.
@@ -238,6 +290,18 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
         return static_cast<double>(tiles) / static_cast<double>(waves * slots);
     };
     const long long m_tiles = (op.M + 127LL) / 128;
+    // Few tiles and a short k loop (too short to share out as stream-K): the
+    // call's time is latency -- launch, first loads, one tile's MMAs, the
+    // epilogue -- so narrower tiles on single CTAs spread it over more SMs.
+    // 256^3 on GB300, calls back to back: 7.9 us per call on one CTA pair,
+    // 5.2 us on 128 x 128 tiles, 4.6 us on 128 x 64 tiles (8 CTAs).
+    if (pair && gemm_kernel == 0 && bn_opt == 0 && kbs < 32) {
+        const long long pair_tiles = ((op.M + 255LL) / 256) * ((op.N + 255LL) / 256);
+        if (pair_tiles * 4 <= (sms / 2 > 0 ? sms / 2 : 1)) {
+            pair = false;
+            block_n = op.N <= 32 && !op.b_mn_major ? 32 : 64;
+        }
+    }
     if (pair && gemm_kernel == 0 && sk_opt != 1 && kbs >= 32) {
         const long long pair_tiles = ((op.M + 255LL) / 256) * ((op.N + 255LL) / 256);
         if (fill(pair_tiles, sms / 2 > 0 ? sms / 2 : 1) < 0.75) pair = false;
@@ -262,6 +326,29 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     // (dynamic time over fixed): 8192^2 x 16384 1.00, 8192^3 0.98, the prefill
     // shape 1.00, 4095 x 4097 x 4100 and 8192^2 x 4096 1.03.
     const bool dyn = pair && !stream_k && opt_or(BSK_OPT_TILE_SCHED, 0) == 2;
+    // Tile height of the one-CTA kernel on a K-major A with one tile column (the
+    // skinny decode shapes): the rows per tile -- a multiple of 8 from 32 to 128
+    // -- that leave each CTA the fewest rows, so that the CTAs fill the SMs
+    // evenly and finish together.  The 34816-row decode weight on 152 SMs: 291
+    // tiles of 120 rows on 146 CTAs (240 rows each) instead of 272 tiles of 128
+    // rows on 136 CTAs (256 each).
+    int block_m = 128;
+    const long long bm_opt = opt_or(BSK_OPT_BLOCK_M, 0);
+    if (!pair && !stream_k && !op.a_mn_major && (op.N + block_n - 1LL) / block_n == 1) {
+        if (bm_opt > 0) {
+            block_m = static_cast<int>(bm_opt);
+        } else {
+            long long best = LLONG_MAX;
+            for (int h = 128; h >= 32; h -= 8) {
+                const long long tiles = (op.M + h - 1LL) / h;
+                const long long rows = (tiles + sms - 1) / sms * h;
+                if (rows < best) {
+                    best = rows;
+                    block_m = h;
+                }
+            }
+        }
+    }
     // one slot per CTA: block_n x 128 FP32 (CTA pairs: each CTA's 128 rows of a 256-wide tile)
     const size_t sk_part_bytes = stream_k ? static_cast<size_t>(sms) * block_n * 128 * sizeof(float) : 0;
     const size_t sk_flag_bytes = stream_k ? static_cast<size_t>(sms) * sizeof(int) : 0;
@@ -272,10 +359,22 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     float* sk_part = nullptr;
     int* sk_flag = nullptr;
     char msg[512] = "";
-    if (a_bytes + b_bytes + sk_part_bytes + sk_flag_bytes > 0) {
-        int st = alloc_workspace(ws, a_bytes + b_bytes + sk_part_bytes + sk_flag_bytes, s);
-        if (st != BSK_OK) return st;
-        uint8_t* base = static_cast<uint8_t*>(ws.ptr);
+    const size_t ws_bytes = a_bytes + b_bytes + sk_part_bytes + sk_flag_bytes;
+    if (ws_bytes > 0) {
+        uint8_t* base = nullptr;
+        if (fixed != nullptr) {
+            if (ws_bytes > fixed->bytes)
+                return fail(BSK_ERR_INVALID_ARG,
+                            "this problem needs %zu bytes of workspace (packed operands%s), more than the fixed "
+                            "%zu-byte (%zu MiB) scratch array; pass 16-byte-aligned operands with 16-byte-multiple "
+                            "leading dimensions (no pack) or use the allocating entry point",
+                            ws_bytes, stream_k ? " and stream-K partials" : "", fixed->bytes, fixed->bytes >> 20);
+            base = static_cast<uint8_t*>(fixed->ptr);
+        } else {
+            int st = alloc_workspace(ws, ws_bytes, s);
+            if (st != BSK_OK) return st;
+            base = static_cast<uint8_t*>(ws.ptr);
+        }
         // the operands that need it are copied to a 16-byte-multiple leading
         // dimension in the workspace, both in one launch
         bsk::PackCopy copies[2];
@@ -290,7 +389,10 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
             Buse = base + a_bytes;
         }
         if (n_copies > 0 &&
-            bsk::launch_pack(copies, n_copies, sms, opt_or(BSK_OPT_PDL, 0) != 1, s, msg, sizeof(msg)))
+            bsk::launch_pack(copies, n_copies, sms, opt_or(BSK_OPT_PDL, 0) != 1,
+                             fixed != nullptr ? fixed->status : g_status_dev,
+                             static_cast<unsigned long long>(opt_or(BSK_OPT_WAIT_LIMIT_US, kDefaultWaitLimitUs)) * 1000ull,
+                             s, msg, sizeof(msg)))
             return fail(BSK_ERR_CUDA, "%s", msg);
         if (stream_k) {
             sk_part = reinterpret_cast<float*>(base + a_bytes + b_bytes);
@@ -318,6 +420,7 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     g.bias = op.bias_mode != 0 ? op.bias : nullptr;
     g.bias_mode = op.bias_mode;
     g.block_n = block_n;
+    g.block_m = block_m;
     g.pair = pair;
     g.stream_k = stream_k;
     g.sk_part = sk_part;
@@ -331,7 +434,7 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s)
     g.tma_store = op.out_type != bsk::kOutF32 && aligned16(op.C) && (op.ldc % 8 == 0) && (op.M % 8 == 0) &&
                   opt_or(BSK_OPT_FORCE_DIRECT_STORE, 0) == 0;
     g.num_sms = sms;
-    g.status = g_status_dev;
+    g.status = fixed != nullptr ? fixed->status : g_status_dev;
     g.wait_limit_ns = static_cast<unsigned long long>(opt_or(BSK_OPT_WAIT_LIMIT_US, kDefaultWaitLimitUs)) * 1000ull;
     g.pdl = opt_or(BSK_OPT_PDL, 0) != 1;
     g.dyn = dyn;
@@ -350,7 +453,7 @@ long long span_elems(long long inner, long long outer, long long ld)
 // onto it by the caller): C = op(A) op(B) [+ bias].
 int enqueue_gemm_general(int transa, int transb, const uint16_t* A, long long lda, const uint16_t* B,
                          long long ldb, uint16_t* C, long long ldc, int M, int N, int K, const uint16_t* bias,
-                         int bias_mode, void* stream)
+                         int bias_mode, void* stream, const bsk::FixedScratch* fixed = nullptr)
 {
     if (M < 0 || N < 0 || K < 0) return fail(BSK_ERR_INVALID_ARG, "negative size (M=%d N=%d K=%d)", M, N, K);
     if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1))
@@ -376,7 +479,7 @@ int enqueue_gemm_general(int transa, int transb, const uint16_t* A, long long ld
     const long long tiles = ((M + 127LL) / 128) * ((N + 127LL) / 128);
     if (tiles > INT_MAX) return fail(BSK_ERR_INVALID_ARG, "problem too large (%lld tiles)", tiles);
     int sms = 0;
-    int st = prepare_device(&sms);
+    int st = prepare_device(&sms, fixed == nullptr);
     if (st != BSK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) {
@@ -399,7 +502,7 @@ int enqueue_gemm_general(int transa, int transb, const uint16_t* A, long long ld
     op.K = K;
     op.bias = bias;
     op.bias_mode = bias_mode;
-    return run_gemm(op, sms, s);
+    return run_gemm(op, sms, s, fixed);
 }
 
 int enqueue_gemm_f16_cblas(int order, int transa, int transb, const uint16_t* A, int lda, const uint16_t* B,
@@ -851,6 +954,20 @@ int run_gemv_bf16_host(const uint16_t* W, const uint16_t* x, uint16_t* y, int M,
 
 namespace bsk {
 
+size_t gemm_f16_colmajor_pack_bytes(const uint16_t* A, const uint16_t* B, int M, int N, int K)
+{
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    const PackPlan pp = plan_pack(colmajor_op(A, B, nullptr, M, N, K));
+    return pp.a_bytes + pp.b_bytes;
+}
+
+int enqueue_gemm_f16_colmajor_fixed(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
+                                    const FixedScratch& scratch, cudaStream_t stream)
+{
+    return enqueue_gemm_general(0, 0, A, M > 1 ? M : 1, B, K > 1 ? K : 1, C, M > 1 ? M : 1, M, N, K, nullptr, 0,
+                                stream, &scratch);
+}
+
 void record_error(const char* msg)
 {
     snprintf(t_err, sizeof(t_err), "%s", msg);
@@ -1012,6 +1129,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_STREAM_K: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_PDL: ok = value == 0 || value == 1; break;
     case BSK_OPT_TILE_SCHED: ok = value >= 0 && value <= 2; break;
+    case BSK_OPT_BLOCK_M: ok = value >= 0 && value <= 128 && value % 8 == 0; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

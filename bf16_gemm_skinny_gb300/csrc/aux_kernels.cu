@@ -23,135 +23,122 @@ __device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uns
                       __funnelshift_r(v3, v4, r));
 }
 
-// One operand's copy as the kernel sees it: `lines` lines of line_bytes bytes.
-// A step is 32 consecutive 16-byte groups of one line (512 bytes, one per
-// lane; the last group of a line may be partial, and lanes past the line's
-// end idle), numbered line by line.
+// One operand's copy as the kernel sees it: `lines` lines of line_bytes bytes,
+// each cut into `pieces` pieces of piece_bytes (a multiple of 16; the last
+// piece of a line may be shorter), numbered line by line: unit u is piece
+// u % pieces of line u / pieces.
 struct PackJob {
     const uint8_t* src;
     long long ld_src;          // bytes from one source line to the next
     uint8_t* dst;              // 16-byte aligned
-    long long ld_dst;          // bytes, a multiple of 16
-    unsigned line_bytes;
-    unsigned steps_per_line;
-    unsigned steps;            // steps_per_line x lines, below 2^31
+    long long ld_dst;          // bytes, a multiple of 16, at least line_bytes rounded up to 16
+    long long line_bytes;
+    long long piece_bytes;
+    long long pieces;          // per line
+    long long units;           // pieces x lines
     unsigned blocks;           // CTAs working on this job
 };
 
 constexpr int kPackThreads = 256;
-constexpr int kPackWarps = kPackThreads / 32;
-constexpr int kPackStages = 8;        // cp.async ring depth per warp
+constexpr int kPackBufs = 4;                     // pieces in flight per CTA
+constexpr int kPackPiece = 8192;                 // longest piece, bytes
+constexpr int kPackBufBytes = kPackPiece + 32;   // a piece's aligned cover plus the chunk read past it
 constexpr int kPackCtasPerSm = 4;
-
-__device__ __forceinline__ void pack_cp_async16(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void pack_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void pack_cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// A cursor over a warp's steps: the current line's source and destination
-// starts and the step within the line.
-struct PackCursor {
-    const uint8_t* s;
-    uint8_t* d;
-    unsigned k;
-    __device__ __forceinline__ void next(unsigned steps_per_line, long long ld_src, long long ld_dst)
-    {
-        if (++k == steps_per_line) {
-            k = 0;
-            s += ld_src;
-            d += ld_dst;
-        }
-    }
-};
+constexpr int kSitePack = 0x20;                  // wait site reported on a timeout
 
 // dst line l = src line l, byte for byte, for up to two operands in one launch
-// (the first job.blocks CTAs take job 0, the rest job 1).  The TMA needs
+// (the first j0.blocks CTAs take job 0, the rest job 1).  The TMA needs
 // 16-byte aligned bases and leading dimensions; the pack gives unaligned
 // operands that shape in a workspace without touching the caller's buffers
 // ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 1: inputs may not be modified).
 //
-// Each warp takes a contiguous range of steps.  A step's 32 groups start m
-// bytes past a 16-byte boundary (m is the line's, the same for the whole
-// warp), so they span 33 aligned source chunks: lane l copies chunk l with
-// cp.async and lane 31 also chunk 32, each only if it holds bytes of a full
-// group (so no copy reaches a page the line does not touch).  The chunks go
-// through a per-warp ring of kPackStages steps in shared memory, so each SM
-// keeps its warps' next seven steps of reads in flight.  After its own
-// copies land (wait_group), a __syncwarp lets lane l read chunk l + 1 of its
-// neighbour; the two chunks are shifted into place and stored with one
-// aligned 16-byte store.  A second __syncwarp keeps the slot from being
-// refilled before every lane has read it.  The partial last group of a line
-// is copied byte by byte.
-__global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_kernel(PackJob j0, PackJob j1)
+// Each CTA takes a contiguous range of units (line pieces).  For each, one
+// thread issues a bulk copy of the piece's 16-byte-aligned cover -- from the
+// aligned chunk holding its first byte to the end of the chunk holding its
+// last, so no byte outside the pages the piece touches is read -- into one of
+// kPackBufs shared-memory buffers, completing on that buffer's mbarrier, so
+// kPackBufs pieces per CTA are in flight.  Once a piece has landed, thread t
+// writes output chunks t, t + 256, ...: chunk c is the 16 bytes that start m
+// bytes into buffer chunk c (m = the piece's offset from a 16-byte boundary),
+// shifted out of buffer chunks c and c + 1, with one aligned 16-byte store.  A
+// line's last chunk may carry up to 15 bytes past the line's end into the
+// destination's padding (its leading dimension is rounded up to 16 bytes; the
+// GEMM's tensor maps never read the padding).  Every wait is bounded.
+__global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm)
+    pack_kernel(PackJob j0, PackJob j1, int* status, unsigned long long limit_ns)
 {
-    __shared__ __align__(16) uint4 ring[kPackWarps][kPackStages][33];
+    __shared__ __align__(128) uint8_t buf[kPackBufs][kPackBufBytes];
+    __shared__ __align__(8) uint64_t bars[kPackBufs];
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPackBufs; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        abort_flag = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
     griddep_wait();               // the source may be the previous kernel's output
     griddep_launch_dependents();  // the GEMM's prologue may start; it waits for this grid's completion
     const bool second = blockIdx.x >= j0.blocks;
-    const uint8_t* const src = second ? j1.src : j0.src;
-    uint8_t* const dst = second ? j1.dst : j0.dst;
-    const long long ld_src = second ? j1.ld_src : j0.ld_src;
-    const long long ld_dst = second ? j1.ld_dst : j0.ld_dst;
-    const unsigned line_bytes = second ? j1.line_bytes : j0.line_bytes;
-    const unsigned spl = second ? j1.steps_per_line : j0.steps_per_line;
-    const unsigned steps = second ? j1.steps : j0.steps;
-    const unsigned blocks = second ? j1.blocks : j0.blocks;
-    const unsigned b = second ? blockIdx.x - j0.blocks : blockIdx.x;
-    const unsigned warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-    const unsigned long long nw = static_cast<unsigned long long>(blocks) * kPackWarps;
-    const unsigned long long w = static_cast<unsigned long long>(b) * kPackWarps + warp;
-    const unsigned s0 = static_cast<unsigned>(steps * w / nw);
-    const unsigned n = static_cast<unsigned>(steps * (w + 1) / nw) - s0;
-    const unsigned off = lane * 16u;   // the lane's group within a step, in bytes
-    const unsigned line0 = s0 / spl;
-    PackCursor in{src + line0 * ld_src, dst + line0 * ld_dst, s0 % spl};
-    PackCursor out = in;
+    const PackJob& j = second ? j1 : j0;
+    const long long b = second ? blockIdx.x - j0.blocks : blockIdx.x;
+    const long long u0 = j.units * b / j.blocks;
+    const long long n = j.units * (b + 1) / j.blocks - u0;
 
-    auto issue = [&](int slot) {
-        const unsigned g = in.k * 512u + off;
-        const uintptr_t a = reinterpret_cast<uintptr_t>(in.s) + g;
-        const unsigned m = static_cast<unsigned>(a & 15u);
-        const uint8_t* chunk = reinterpret_cast<const uint8_t*>(a & ~static_cast<uintptr_t>(15));
-        // chunk `lane` holds the start of this lane's group and, when m > 0, the
-        // end of the previous lane's group
-        const bool full = g + 16u <= line_bytes;
-        if (full || (m != 0u && lane != 0u && g <= line_bytes))
-            pack_cp_async16(smem_u32(&ring[warp][slot][lane]), chunk);
-        if (lane == 31u && m != 0u && full) pack_cp_async16(smem_u32(&ring[warp][slot][32]), chunk + 16);
-        pack_cp_commit();
-        in.next(spl, ld_src, ld_dst);
+    // source start, destination start and length of unit u
+    auto piece = [&](long long u, const uint8_t*& s, uint8_t*& d, long long& len) {
+        const long long line = u / j.pieces;
+        const long long off = (u - line * j.pieces) * j.piece_bytes;
+        s = j.src + line * j.ld_src + off;
+        d = j.dst + line * j.ld_dst + off;
+        len = j.line_bytes - off < j.piece_bytes ? j.line_bytes - off : j.piece_bytes;
     };
+    // thread 0: unit u0 + i into buffer i % kPackBufs
+    auto issue = [&](long long i) {
+        const uint8_t* s;
+        uint8_t* d;
+        long long len;
+        piece(u0 + i, s, d, len);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(s);
+        const uintptr_t lo = a & ~static_cast<uintptr_t>(15);
+        const uintptr_t hi = (a + static_cast<uintptr_t>(len) + 15) & ~static_cast<uintptr_t>(15);
+        const uint32_t bar = smem_u32(&bars[i % kPackBufs]);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(hi - lo));
+        bulk_load(smem_u32(buf[i % kPackBufs]), reinterpret_cast<const void*>(lo), static_cast<uint32_t>(hi - lo), bar);
+    };
+    if (threadIdx.x == 0)
+        for (long long i = 0; i < n && i < kPackBufs; ++i) issue(i);
 
-#pragma unroll
-    for (int t = 0; t < kPackStages - 1; ++t) {
-        if (static_cast<unsigned>(t) < n) issue(t);
-        else pack_cp_commit();
-    }
-    int slot = 0;
-    for (unsigned i = 0; i < n; ++i) {
-        // the slot consumed last iteration takes the step kPackStages - 1 ahead
-        const int ahead = slot == 0 ? kPackStages - 1 : slot - 1;
-        if (i + (kPackStages - 1) < n) issue(ahead);
-        else pack_cp_commit();
-        pack_cp_wait<kPackStages - 1>();   // this lane's copies of step i have landed
-        __syncwarp();                      // ... and so have its neighbours'
-        const unsigned g = out.k * 512u + off;
-        const uint8_t* sp = out.s + g;
-        if (g + 16u <= line_bytes) {
-            const unsigned m = static_cast<unsigned>(reinterpret_cast<uintptr_t>(sp) & 15u);
-            const uint4 lo = ring[warp][slot][lane];
-            *reinterpret_cast<uint4*>(out.d + g) = m == 0u ? lo : realign16(lo, ring[warp][slot][lane + 1], m);
-        } else if (g < line_bytes) {
-            for (unsigned t = 0; t < line_bytes - g; ++t) out.d[g + t] = sp[t];
+    const WaitCtl wc{&abort_flag, status, limit_ns};
+    long long i = 0;
+    for (; i < n; ++i) {
+        const int bi = static_cast<int>(i % kPackBufs);
+        const bool ok = mbar_wait(smem_u32(&bars[bi]), static_cast<uint32_t>(i / kPackBufs) & 1u, wc, kSitePack);
+        if (!__syncthreads_and(ok)) break;
+        const uint8_t* s;
+        uint8_t* d;
+        long long len;
+        piece(u0 + i, s, d, len);
+        const unsigned m = static_cast<unsigned>(reinterpret_cast<uintptr_t>(s) & 15u);
+        const uint4* sb = reinterpret_cast<const uint4*>(buf[bi]);
+        const unsigned chunks = static_cast<unsigned>((len + 15) / 16);
+        for (unsigned c = threadIdx.x; c < chunks; c += kPackThreads) {
+            const uint4 lo = sb[c];
+            *reinterpret_cast<uint4*>(d + 16ull * c) = m == 0u ? lo : realign16(lo, sb[c + 1], m);
         }
-        __syncwarp();                      // every lane has read the slot before it is refilled
-        out.next(spl, ld_src, ld_dst);
-        slot = slot == kPackStages - 1 ? 0 : slot + 1;
+        __syncthreads();   // every thread has read the buffer before it is refilled
+        if (threadIdx.x == 0 && i + kPackBufs < n) {
+            fence_proxy_async_smem();
+            issue(i + kPackBufs);
+        }
     }
-    pack_cp_wait<0>();   // the trailing (empty) groups
+    if (i < n && threadIdx.x == 0) {
+        // abort: the copies issued and not consumed must land before the CTA exits
+        uint32_t never = 0u;
+        const WaitCtl wc_drain{&never, status, limit_ns};
+        const long long issued = n < i + kPackBufs ? n : i + kPackBufs;
+        for (long long k = i; k < issued; ++k)
+            mbar_wait(smem_u32(&bars[k % kPackBufs]), static_cast<uint32_t>(k / kPackBufs) & 1u, wc_drain, kSitePack);
+    }
 }
 
 // C(m,n) = bias value (or +0.0) for m < M, n < N, C(m,n) at C[m + n*ldc]: the
@@ -194,58 +181,72 @@ __global__ void wait_timeout_probe_kernel(int* status, unsigned long long limit_
 
 }  // namespace
 
-int launch_pack(const PackCopy* copies, int n, int sms, bool pdl, cudaStream_t stream, char* msg, size_t msg_len)
+int preload_aux_kernels(char* msg, size_t msg_len)
+{
+    const void* kernels[] = {reinterpret_cast<const void*>(pack_kernel), reinterpret_cast<const void*>(fill_bias_kernel)};
+    for (const void* k : kernels) {
+        cudaFuncAttributes attr;
+        const cudaError_t e = cudaFuncGetAttributes(&attr, k);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncGetAttributes (pack/fill kernel): %s", cudaGetErrorString(e));
+            return 1;
+        }
+    }
+    return 0;
+}
+
+int launch_pack(const PackCopy* copies, int n, int sms, bool pdl, int* status, unsigned long long limit_ns,
+                cudaStream_t stream, char* msg, size_t msg_len)
 {
     PackJob jobs[2] = {};
     int nj = 0;
-    auto flush = [&]() -> int {
-        // persistent grid, split between the jobs by their steps (at least one
-        // CTA each, no more than one warp per step)
-        const unsigned long long per_cta = kPackWarps;
-        const unsigned long long u0 = jobs[0].steps, u1 = nj > 1 ? jobs[1].steps : 0ull;
-        const unsigned long long total = static_cast<unsigned long long>(sms > 0 ? sms : 1) * kPackCtasPerSm;
-        unsigned long long b0 = nj > 1 ? (total * u0 + (u0 + u1) / 2) / (u0 + u1) : total;
-        if (b0 < 1) b0 = 1;
-        unsigned long long b1 = nj > 1 ? (total > b0 ? total - b0 : 1ull) : 0ull;
-        b0 = std::min(b0, (u0 + per_cta - 1) / per_cta);
-        b1 = std::min(b1, (u1 + per_cta - 1) / per_cta);
-        jobs[0].blocks = static_cast<unsigned>(b0);
-        jobs[1].blocks = static_cast<unsigned>(b1);
-        cudaError_t e = launch_kernel(pack_kernel, dim3(static_cast<unsigned>(b0 + b1)), dim3(kPackThreads), 0,
-                                      stream, pdl, jobs[0], jobs[1]);
-        nj = 0;
-        jobs[0] = PackJob{};
-        jobs[1] = PackJob{};
-        if (e != cudaSuccess) {
-            snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
-            return 1;
-        }
-        return 0;
-    };
     for (int i = 0; i < n; ++i) {
         const PackCopy& c = copies[i];
         if (c.line_bytes <= 0 || c.lines <= 0) continue;
-        if (c.line_bytes > (1LL << 31)) {
-            snprintf(msg, msg_len, "pack: line of %lld bytes is too long", c.line_bytes);
+        if (nj == 2) {
+            snprintf(msg, msg_len, "pack: at most two copies per launch");
             return 1;
         }
-        const unsigned long long spl = (static_cast<unsigned long long>(c.line_bytes) + 511) / 512;
-        // keep each job's step count below 2^31 (32-bit step arithmetic in the kernel)
-        const long long lines_per_job = static_cast<long long>(std::max(1ull, (1ull << 31) / spl - 1));
-        for (long long l0 = 0; l0 < c.lines; l0 += lines_per_job) {
-            const long long nl = std::min(lines_per_job, c.lines - l0);
-            PackJob& j = jobs[nj++];
-            j.src = static_cast<const uint8_t*>(c.src) + l0 * c.ld_src;
-            j.ld_src = c.ld_src;
-            j.dst = static_cast<uint8_t*>(c.dst) + l0 * c.ld_dst;
-            j.ld_dst = c.ld_dst;
-            j.line_bytes = static_cast<unsigned>(c.line_bytes);
-            j.steps_per_line = static_cast<unsigned>(spl);
-            j.steps = static_cast<unsigned>(spl * static_cast<unsigned long long>(nl));
-            if (nj == 2 && flush()) return 1;
+        if ((reinterpret_cast<uintptr_t>(c.dst) & 15u) != 0 || (c.ld_dst & 15) != 0 ||
+            c.ld_dst < (c.line_bytes + 15) / 16 * 16) {
+            snprintf(msg, msg_len, "pack: destination not 16-byte aligned or its leading dimension too small");
+            return 1;
         }
+        PackJob& j = jobs[nj++];
+        j.src = static_cast<const uint8_t*>(c.src);
+        j.ld_src = c.ld_src;
+        j.dst = static_cast<uint8_t*>(c.dst);
+        j.ld_dst = c.ld_dst;
+        j.line_bytes = c.line_bytes;
+        // pieces of equal length (multiples of 16), at most kPackPiece bytes each
+        j.pieces = (c.line_bytes + kPackPiece - 1) / kPackPiece;
+        j.piece_bytes = ((c.line_bytes + j.pieces - 1) / j.pieces + 15) / 16 * 16;
+        j.units = j.pieces * c.lines;
     }
-    if (nj > 0 && flush()) return 1;
+    if (nj == 0) return 0;
+    // persistent grid, split between the jobs by their bytes (at least one CTA
+    // each, no more CTAs than units)
+    const unsigned long long total = static_cast<unsigned long long>(sms > 0 ? sms : 1) * kPackCtasPerSm;
+    const double w0 = static_cast<double>(jobs[0].line_bytes) * static_cast<double>(jobs[0].units / jobs[0].pieces);
+    const double w1 = nj > 1 ? static_cast<double>(jobs[1].line_bytes) * static_cast<double>(jobs[1].units / jobs[1].pieces)
+                             : 0.0;
+    unsigned long long b0 = nj > 1 ? static_cast<unsigned long long>(static_cast<double>(total) * w0 / (w0 + w1) + 0.5)
+                                   : total;
+    if (b0 < 1) b0 = 1;
+    unsigned long long b1 = nj > 1 ? (total > b0 ? total - b0 : 1ull) : 0ull;
+    b0 = std::min<unsigned long long>(b0, static_cast<unsigned long long>(jobs[0].units));
+    b1 = std::min<unsigned long long>(b1, nj > 1 ? static_cast<unsigned long long>(jobs[1].units) : 0ull);
+    jobs[0].blocks = static_cast<unsigned>(b0);
+    jobs[1].blocks = static_cast<unsigned>(b1);
+    static SmemOptIn attrs;
+    cudaError_t e = attrs.ensure(reinterpret_cast<const void*>(pack_kernel), 0);
+    if (e == cudaSuccess)
+        e = launch_kernel(pack_kernel, dim3(static_cast<unsigned>(b0 + b1)), dim3(kPackThreads), 0, stream, pdl,
+                          jobs[0], jobs[1], status, limit_ns);
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
+        return 1;
+    }
     return 0;
 }
 
@@ -256,8 +257,12 @@ int launch_fill_bias(uint16_t* C, long long ldc, int M, int N, const uint16_t* b
     if (total <= 0) return 0;
     long long grid = (total + 255) / 256;
     if (grid > 4096) grid = 4096;
-    fill_bias_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(C, ldc, M, N, bias, bias_mode);
-    cudaError_t e = cudaGetLastError();
+    static SmemOptIn attrs;
+    cudaError_t e = attrs.ensure(reinterpret_cast<const void*>(fill_bias_kernel), 0);
+    if (e == cudaSuccess) {
+        fill_bias_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(C, ldc, M, N, bias, bias_mode);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "fill launch failed: %s", cudaGetErrorString(e));
         return 1;

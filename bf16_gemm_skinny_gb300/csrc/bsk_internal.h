@@ -74,13 +74,20 @@ void record_error(const char* msg);
 // cuTensorMapEncodeTiled from the driver (resolved once through the runtime).
 TmapEncodeFn tmap_encoder();
 
-// Raises one kernel's dynamic shared-memory limit, once per device: a launcher
-// keeps one of these in a function-local static next to the kernel it launches,
-// so the attribute call is not repeated on every launch (it costs host time
-// that short kernels would otherwise wait for).
+// Sets one kernel's launch attributes once per device: a launcher keeps one of
+// these in a function-local static next to the kernel it launches, so the
+// attribute calls are not repeated on every launch (they cost host time that
+// short kernels would otherwise wait for).
+//  * the dynamic shared-memory limit, raised to `bytes`;
+//  * the preferred carveout: every kernel of the library asks for the largest
+//    shared-memory share of the SM's L1/shared storage.  The GEMM kernels need
+//    it (about 200 KB per CTA), and when consecutive kernels in a stream ask
+//    for different carveouts the SMs are reconfigured between them, which
+//    delays the second kernel's start (its loads use no L1 allocation, so the
+//    smaller L1 costs nothing).
 struct SmemOptIn {
     static constexpr int kMaxDevices = 128;
-    std::atomic<int> done[kMaxDevices];   // bytes already allowed on each device (static storage: zero)
+    std::atomic<int> done[kMaxDevices];   // 1 + bytes already allowed on each device (static storage: 0 = none yet)
 
     cudaError_t ensure(const void* kernel, int bytes)
     {
@@ -88,9 +95,15 @@ struct SmemOptIn {
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         const bool slot = dev >= 0 && dev < kMaxDevices;
-        if (slot && done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e == cudaSuccess && slot) done[dev].store(bytes, std::memory_order_release);
+        const int have = slot ? done[dev].load(std::memory_order_acquire) : 0;
+        if (have > bytes) return cudaSuccess;
+        if (have == 0) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
+        }
+        if (bytes > 0) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess && slot) done[dev].store(bytes + 1, std::memory_order_release);
         return e;
     }
 };
@@ -120,6 +133,7 @@ struct GemmLaunch {
     int out_type = kOutF16;  // GemmOutType of C
     float alpha = 1.0f;      // FP8 inputs: C = alpha * A * B (the 16-bit kernels ignore it)
     int block_n = 256;       // 32, 64, 128 or 256
+    int block_m = 128;       // one-CTA kernel, K-major A, whole tiles: rows per tile (8..128, a multiple of 8)
     bool pair = true;        // block_n == 256 only: CTA-pair kernel (256 x 256 tiles over two SMs)
     int group_m = 2;         // >= 1
     bool tma_store = false;  // C 16-byte aligned with 16-byte-multiple ldc
@@ -187,14 +201,46 @@ struct PackCopy {
     long long lines;
 };
 
-// Enqueues the n copies (two to a launch) on `stream`, as programmatic
-// dependents of the kernel before them when pdl is set.
-int launch_pack(const PackCopy* copies, int n, int sms, bool pdl, cudaStream_t stream, char* msg, size_t msg_len);
+// Enqueues the n (at most two) copies in one launch on `stream`, as a
+// programmatic dependent of the kernel before it when pdl is set.  A wait that
+// gives up after limit_ns records a timeout in `status`.  The destination's
+// leading dimension must be a multiple of 16 bytes and at least line_bytes
+// rounded up to 16: a line's last 16-byte chunk is stored whole.
+int launch_pack(const PackCopy* copies, int n, int sms, bool pdl, int* status, unsigned long long limit_ns,
+                cudaStream_t stream, char* msg, size_t msg_len);
 
 // C(m,n) = bias[m] (mode 1), bias[n] (mode 2) or +0.0 (mode 0) for the M x N
 // column-major C with leading dimension ldc: the GEMM with K == 0.
 int launch_fill_bias(uint16_t* C, long long ldc, int M, int N, const uint16_t* bias, int bias_mode,
                      cudaStream_t stream, char* msg, size_t msg_len);
+
+// A caller-provided region that replaces the GEMM's stream-ordered workspace
+// (packed operands, stream-K partials and flags), and the device status word
+// its kernels report a timeout in.  `ptr` is 256-byte aligned.
+struct FixedScratch {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    int* status = nullptr;
+};
+
+// The work of gemm_f16_colmajor on `stream` with its workspace taken from
+// `scratch` instead of allocated: the same argument checks, the same plan
+// (pack, tile width, kernel, schedule, options) and the same kernels.  A plan
+// that needs more than scratch.bytes is refused with BSK_ERR_INVALID_ARG
+// before anything is launched.  Allocates nothing (no pinned status word
+// either: the kernels write scratch.status).  Returns a bsk_status.
+int enqueue_gemm_f16_colmajor_fixed(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
+                                    const FixedScratch& scratch, cudaStream_t stream);
+
+// Workspace bytes gemm_f16_colmajor(A, B, C, M, N, K) spends on packed
+// operands (host arithmetic only; stream-K partials come on top).
+size_t gemm_f16_colmajor_pack_bytes(const uint16_t* A, const uint16_t* B, int M, int N, int K);
+
+// Loads the device code of every kernel the column-major FP16 GEMM may launch
+// (its GEMM instances; the pack and fill kernels), so that no later launch of
+// them maps device memory for code under lazy module loading.  0 on success.
+int preload_gemm_f16_colmajor_kernels(char* msg, size_t msg_len);
+int preload_aux_kernels(char* msg, size_t msg_len);
 
 // Test hook: one CTA waits on an mbarrier that nothing completes, with the same
 // bounded wait the GEMM uses; it must give up after `limit_ns` and record a

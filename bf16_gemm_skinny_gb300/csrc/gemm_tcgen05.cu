@@ -51,6 +51,28 @@ int dispatch_pair(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t ms
 
 }  // namespace
 
+int preload_gemm_f16_colmajor_kernels(char* msg, size_t msg_len)
+{
+    // the instances gemm_f16_colmajor may pick: MN-major A, K-major B, FP16 in
+    // and out, on CTA pairs or one CTA per 128 x BN tile
+    const void* kernels[] = {
+        reinterpret_cast<const void*>(gemm_tcgen05_pair_kernel<true, false, kInF16, kOutF16>),
+        reinterpret_cast<const void*>(gemm_tcgen05_kernel<256, true, false, kInF16, kOutF16>),
+        reinterpret_cast<const void*>(gemm_tcgen05_kernel<128, true, false, kInF16, kOutF16>),
+        reinterpret_cast<const void*>(gemm_tcgen05_kernel<64, true, false, kInF16, kOutF16>),
+        reinterpret_cast<const void*>(gemm_tcgen05_kernel<32, true, false, kInF16, kOutF16>),
+    };
+    for (const void* k : kernels) {
+        cudaFuncAttributes attr;
+        const cudaError_t e = cudaFuncGetAttributes(&attr, k);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncGetAttributes (GEMM kernel): %s", cudaGetErrorString(e));
+            return 1;
+        }
+    }
+    return 0;
+}
+
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
     if (g.in_type == kInE4M3 || g.in_type == kInE5M2) return launch_gemm_fp8(g, stream, msg, msg_len);

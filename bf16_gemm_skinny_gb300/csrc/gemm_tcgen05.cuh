@@ -100,6 +100,11 @@ struct Cfg {
 
 struct Params {
     int M, N, K;
+    // Rows of C per tile: 128 (the MMA's M), or fewer -- a multiple of 8 -- in
+    // the balanced schedule of the one-CTA kernel with a K-major A, where every
+    // CTA gets the same number of rows (the rows past `bm` that the MMA still
+    // computes come from stale shared memory and are not stored).
+    int bm;
     int num_m, num_n, num_tiles, num_kb;
     int group_m;
     void* C;
@@ -231,11 +236,12 @@ __device__ __forceinline__ uint16_t round_out(uint32_t acc_bits)
     }
 }
 
-// Masked column-major stores of one lane's row m, columns n0..n0+31.
+// Masked column-major stores of one lane's row m, columns n0..n0+31 (rows at
+// or past m_end -- the end of C or of the tile -- store nothing).
 template <int OUT>
-__device__ __forceinline__ void store_row(const uint32_t (&r)[32], const Params& p, int m, int n0)
+__device__ __forceinline__ void store_row(const uint32_t (&r)[32], const Params& p, int m, int n0, int m_end)
 {
-    if (m >= p.M) return;
+    if (m >= m_end) return;
     if constexpr (OUT == kOutF32) {
         uint32_t* Cg = reinterpret_cast<uint32_t*>(p.C);
 #pragma unroll
@@ -379,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_prefetch_l2_2d(&tmA, pm * kBM, k0);
                     tma_prefetch_l2_2d(&tmA, pm * kBM + 64, k0);
                 } else {
-                    tma_prefetch_l2_2d(&tmA, k0, pm * kBM);
+                    tma_prefetch_l2_2d(&tmA, k0, pm * p.bm);
                 }
                 if constexpr (B_MN) {
 #pragma unroll
@@ -407,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Waits on the abort path ignore the abort flag but keep the time limit.
     uint32_t never = 0u;
     const WaitCtl wc_drain{&never, p.status, p.wait_limit_ns};
+    // bytes a stage's loads deliver: a K-major A box is p.bm rows of 128 bytes
+    const uint32_t stage_tx = (A_MN ? Cf::kABytes : p.bm * kRowBytes) + Cf::kBBytes;
 
     if (warp == 0) {
         // ------------------------------------------------------------------
@@ -422,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ok && seg_next(p, cur, tile, kb0, kb1)) {
                 int pm, pn;
                 tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
-                const int m0 = pm * kBM;
+                const int m0 = pm * p.bm;
                 const int n0 = pn * BN;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
@@ -430,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t fb = full0 + 8 * stage;
-                    mbar_arrive_expect_tx(fb, Cf::kStageBytes);
+                    mbar_arrive_expect_tx(fb, stage_tx);
                     const uint32_t a_dst = smem_u32(sA + stage * Cf::kABytes);
                     const uint32_t b_dst = smem_u32(sB + stage * Cf::kBBytes);
                     const int k0 = kb * Ty::kBK;
@@ -539,8 +547,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             int pm, pn;
             tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
-            const int m0 = pm * kBM + quarter * 32;
+            const int m0 = pm * p.bm + quarter * 32;
             const int n0 = pn * BN;
+            // rows of C this warp stores: its 32 TMEM lanes, clipped to the tile and to C
+            const int tile_end = pm * p.bm + p.bm;
+            const int m_end = tile_end < p.M ? tile_end : p.M;
+            // the TMA store writes all 32 rows of a box (clipped at M only)
+            const bool whole_quarter = m0 + 32 <= tile_end;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
             // Stream-K roles: a segment that does not start the tile leaves its
@@ -579,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + pq[j * kBM]);
                 }
                 finish_acc<IN, OUT>(r, p, m0 + lane, n0 + c * 32);
-                if (Ty::kOutBytes == 2 && p.tma_store) {
+                if (Ty::kOutBytes == 2 && p.tma_store && whole_quarter) {
                     uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
                     if (lane == 0) bulk_wait_group_read<1>();   // the store that used `buf` has read it
                     __syncwarp();
@@ -593,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_commit_group();
                     }
                 } else {
-                    store_row<OUT>(r, p, m0 + lane, n0 + c * 32);
+                    store_row<OUT>(r, p, m0 + lane, n0 + c * 32, m_end);
                 }
             }
             if (to_slot) {
@@ -974,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_commit_group();
                     }
                 } else {
-                    store_row<OUT>(r, p, m0 + lane, n0 + c * 32);
+                    store_row<OUT>(r, p, m0 + lane, n0 + c * 32, p.M);
                 }
             }
             if (to_slot) {
@@ -1030,18 +1043,19 @@ inline bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* b
 }
 
 // Tensor maps of A, B (128-byte swizzled k rows or 64 x 64 MN-major boxes) and
-// C (16-bit outputs stored by TMA only).  `rows_b` is the B box height.
+// C (16-bit outputs stored by TMA only).  `rows_a` is the height of a K-major
+// A box (the tile's rows), `rows_b` the B box height.
 template <int IN, int OUT, bool A_MN, bool B_MN>
-bool encode_operands(const GemmLaunch& g, int rows_b, CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmC,
-                     char* msg, size_t msg_len)
+bool encode_operands(const GemmLaunch& g, int rows_a, int rows_b, CUtensorMap* tmA, CUtensorMap* tmB,
+                     CUtensorMap* tmC, char* msg, size_t msg_len)
 {
     using Ty = Types<IN, OUT>;
     const CUtensorMapDataType dt = tmap_type(IN);
     const unsigned long long eb = Ty::kElemBytes;
     const bool ok_a = A_MN ? encode_2d(tmA, dt, g.A, g.M, g.K, g.lda * eb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg,
                                        msg_len)
-                           : encode_2d(tmA, dt, g.A, g.K, g.M, g.lda * eb, Ty::kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
-                                       msg, msg_len);
+                           : encode_2d(tmA, dt, g.A, g.K, g.M, g.lda * eb, Ty::kBK, rows_a,
+                                       CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len);
     if (!ok_a) return false;
     const bool ok_b = B_MN ? encode_2d(tmB, dt, g.B, g.N, g.K, g.ldb * eb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, msg,
                                        msg_len)
@@ -1065,14 +1079,19 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
 {
     using Cf = Cfg<BN>;
     using Ty = Types<IN, OUT>;
+    // Tile rows: 128, or the balanced height the planner chose (K-major A,
+    // whole tiles only).
+    const int bm = (!A_MN && !g.stream_k && g.block_m >= 8 && g.block_m <= kBM && g.block_m % 8 == 0) ? g.block_m
+                                                                                                       : kBM;
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_operands<IN, OUT, A_MN, B_MN>(g, BN, &tmA, &tmB, &tmC, msg, msg_len)) return 1;
+    if (!encode_operands<IN, OUT, A_MN, B_MN>(g, bm, BN, &tmA, &tmB, &tmC, msg, msg_len)) return 1;
 
     Params p;
     p.M = g.M;
     p.N = g.N;
     p.K = g.K;
-    p.num_m = (g.M + kBM - 1) / kBM;
+    p.bm = bm;
+    p.num_m = (g.M + bm - 1) / bm;
     p.num_n = (g.N + BN - 1) / BN;
     p.num_tiles = p.num_m * p.num_n;
     p.num_kb = (g.K + Ty::kBK - 1) / Ty::kBK;
@@ -1148,9 +1167,10 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     using Cf = PairCfg;
     using Ty = Types<IN, OUT>;
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_operands<IN, OUT, A_MN, B_MN>(g, kBM, &tmA, &tmB, &tmC, msg, msg_len)) return 1;
+    if (!encode_operands<IN, OUT, A_MN, B_MN>(g, kBM, kBM, &tmA, &tmB, &tmC, msg, msg_len)) return 1;
     Params p;
     p.M = g.M;
+    p.bm = kBM;
     p.N = g.N;
     p.K = g.K;
     p.num_m = (g.M + Cf::kTile - 1) / Cf::kTile;

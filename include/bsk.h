@@ -195,18 +195,28 @@ int decode_attention_bf16(const uint16_t* q, const uint16_t* k_cache, const uint
  * gemm_f16_colmajor for callers that cannot allocate device memory during a
  * call (for example a serving process whose own allocator reserved all free
  * HBM at start-up, or a program held to a device-memory budget fixed when it
- * started).  Same arguments, result and blocking behaviour as
- * gemm_f16_colmajor, and the same kernels.  The pages have no counterpart:
+ * started).  Same arguments, result bits and blocking behaviour as
+ * gemm_f16_colmajor: the same argument checks, the same choice of tiles,
+ * kernel and schedule, the same kernels.  The pages have no counterpart:
  * this entry point exists for the way the library is deployed.
  *
- * Instead of allocating a workspace when an operand must be packed (base not
- * 16-byte aligned, or M or K not a multiple of 8), it packs into a fixed
- * 96 MiB device array that is part of the library (held on every GPU that
- * loads it, until the process exits), and it calls no cudaMalloc, cudaFree or
- * other allocating routine.  Calls needing more scratch than 96 MiB return
- * BSK_ERR_INVALID_ARG; aligned operands need none at any size.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress): make it before any stream capture on that device.
+ * Where gemm_f16_colmajor allocates a stream-ordered workspace (to pack an
+ * operand whose base is not 16-byte aligned or whose M or K is not a multiple
+ * of 8, or for the FP32 partials of the stream-K schedule), this call uses a
+ * fixed 96 MiB device array that is part of the library (held on every GPU
+ * that loads it, until the process exits) and calls no cudaMalloc, cudaFree
+ * or other allocating routine.  Calls needing more workspace than 96 MiB
+ * return BSK_ERR_INVALID_ARG before any device work; aligned operands need no
+ * pack at any size.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and loads the device code of the kernels it may
+ * launch.  Under CUDA's default lazy module loading that is when the 96 MiB
+ * array and the kernels' code are mapped, so the first call on a device does
+ * take device memory: make it before the caller reserves the device's free
+ * memory (or run with CUDA_MODULE_LOADING=EAGER), and before anything else on
+ * its stream is being captured.  Later calls allocate nothing.
+ * The call blocks (it reads the device status word back and synchronises
+ * `stream`), so it cannot be captured into a CUDA graph.
  * All calls share the array and keep the previous call's contents in it, so
  * calls that overlap on the GPU (several streams or host threads) race:
  * serialise them.
@@ -270,83 +280,6 @@ const char* bsk_status_string(int status);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int bsk_version(void);
-
-/*
- * Tile order of the GEMM ("Hygon 优化", section 分组调度：提高 L2 数据复用):
- * maps the flattened tile index t of a num_m x num_n tile grid to its tile
- * coordinates, visiting group_m tile rows per tile column, the last group
- * holding the remaining rows.  Host-side copy of the function the kernel
- * uses; needs no GPU.  Invalid arguments give (-1, -1).
- */
-void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* pid_n);
-
-/*
- * Tuning and test options (process-wide; not thread-safe; 0 restores the
- * default).  Keys:
- *   BSK_OPT_GROUP_M          GEMM tile-row group size (default 2 for CTA pairs, 16 otherwise)
- *   BSK_OPT_BLOCK_N          GEMM tile width 32, 64, 128 or 256 (default: the smallest of
- *                            32/64/128 that covers N, else 256)
- *   BSK_OPT_FORCE_PACK       1: pack A and B even when aligned
- *   BSK_OPT_FORCE_DIRECT_STORE 1: masked register stores instead of the TMA store
- *   BSK_OPT_GEMV_ROWS        GEMV rows of W per warp: 1, 2, 4 or 8 (default by n)
- *   BSK_OPT_GEMV_WARPS       GEMV warps per CTA, 1..16 (default 16 pipelined, 8 streaming)
- *   BSK_OPT_WAIT_LIMIT_US    device-side wait limit in microseconds (default 2 s)
- *   BSK_OPT_NUM_SMS          cap on the persistent GEMM grid (default: all SMs)
- *   BSK_OPT_GEMM_KERNEL      GEMM kernel for 256-wide tiles: 1 one CTA per 128 x 256 tile,
- *                            2 CTA pairs on 256 x 256 tiles (default 2; narrower tiles
- *                            always run one CTA per 128 x BN tile)
- *   BSK_OPT_GEMV_KERNEL      kernel of gemv_bf16 for n <= 8: 1 register streaming,
- *                            2 cp.async-pipelined, 3 pipelined with x kept in BF16,
- *                            4 token-paired (n >= 5) -- the CUDA-core GEMVs -- or 5 the
- *                            tensor-core skinny GEMM (default: 1 for n <= 3, 5 for
- *                            n >= 4; a CUDA-core kernel whose buffers do not fit in
- *                            shared memory falls back to another)
- *   BSK_OPT_STREAM_K         GEMM schedule: 1 whole tiles, 2 stream-K (every SM -- or CTA
- *                            pair -- an equal share of the tile x k-block iterations of the
- *                            last wave; split tiles are summed in FP32 by the unit that
- *                            holds their first k-block), 0 automatic: stream-K on the
- *                            one-CTA-per-tile kernel when whole tiles would fill under three
- *                            quarters of the SMs and a tile has at least 32 k-blocks; whole
- *                            tiles on CTA pairs
- *   BSK_OPT_PDL              1: launch the GEMM, GEMV and attention kernels in plain stream
- *                            order; 0 (default): as programmatic dependents of the kernel
- *                            before them in the stream, so that their launch and prologue
- *                            (barrier set-up, TMEM allocation, L2 prefetch of the first
- *                            weight tiles) overlap that kernel's last CTAs.  Either way no
- *                            input is read and no output written before the earlier kernel
- *                            has completed.
- *   BSK_OPT_TILE_SCHED       tile order of the CTA-pair GEMM kernel (whole tiles): 0 or 1
- *                            fixed (pair p takes tiles p, p + P, ...), 2 dynamic (one cluster
- *                            per tile launched; a pair that is done takes the tile of a
- *                            cluster whose launch it cancels, so tiles go to the pairs that
- *                            are free first; BSK_OPT_NUM_SMS does not cap this grid)
- * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
- */
-enum {
-    BSK_OPT_GROUP_M = 1,
-    BSK_OPT_BLOCK_N = 2,
-    BSK_OPT_FORCE_PACK = 3,
-    BSK_OPT_FORCE_DIRECT_STORE = 4,
-    BSK_OPT_GEMV_ROWS = 5,
-    BSK_OPT_GEMV_WARPS = 6,
-    BSK_OPT_WAIT_LIMIT_US = 7,
-    BSK_OPT_NUM_SMS = 8,
-    BSK_OPT_GEMV_KERNEL = 9,
-    BSK_OPT_GEMM_KERNEL = 10,
-    BSK_OPT_STREAM_K = 11,
-    BSK_OPT_PDL = 12,
-    BSK_OPT_TILE_SCHED = 13
-};
-int bsk_set_option(int key, long long value);
-long long bsk_get_option(int key);
-
-/*
- * Test hook for the watchdog: launches one CTA that waits on a barrier that
- * nothing completes, using the GEMM's bounded wait with a limit of
- * `limit_us` microseconds (1 .. 10,000,000).  Returns BSK_ERR_TIMEOUT when the
- * wait gave up as designed, BSK_OK never.  Blocks until the probe finished.
- */
-int bsk_test_wait_timeout(unsigned int limit_us, void* stream);
 
 #ifdef __cplusplus
 }

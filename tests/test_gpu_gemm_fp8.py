@@ -186,6 +186,22 @@ def test_skinny_n(N):
     assert np.array_equal(got, bits)
 
 
+@pytest.mark.parametrize("block_m", [8, 56, 120])
+@pytest.mark.parametrize("N", [8, 100])
+def test_skinny_tile_heights(block_m, N):
+    """Narrow tiles of block_m weight rows (the balanced schedule's heights,
+    forced): bit-exact on integer inputs, and C's padding rows stay untouched."""
+    M, K = 1000, 640
+    A2, B2 = operands(M, N, K, "int2", "e4m3")
+    bsk.set_option("block_m", block_m)
+    try:
+        got, Af, lda, Bf, ldb = run(A2, B2, "e4m3", "bf16", pad_a=16, pad_c=5)
+    finally:
+        bsk.set_option("block_m", 0)
+    _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", "bf16")
+    assert np.array_equal(got, bits)
+
+
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_unaligned_pointers_and_strides(out):
     """Bases one byte off and leading dimensions not multiples of 16: both operands are packed."""

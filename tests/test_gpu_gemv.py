@@ -194,6 +194,28 @@ def test_skinny_34816x5120_full(n):
     check_tolerance(run(W, x, M, K, n), ref, "bf16", K, absmax_bf16(x), absmax_bf16(W), f"skinny n={n}")
 
 
+@pytest.mark.parametrize("block_m", [8, 40, 64, 120, 128])
+@pytest.mark.parametrize("M,K,n", [(34816, 1032, 4), (4095, 1032, 8), (1003, 640, 32), (777, 2048, 100)])
+def test_skinny_tile_heights(block_m, M, K, n):
+    """The tensor-core skinny path with tiles of block_m rows of W (the heights
+    of the balanced schedule, forced; the MMA still computes 128 rows, of which
+    only the tile's are stored): integer inputs match the oracle bit for bit,
+    random ones stay within tolerance."""
+    bsk.set_option("block_m", block_m)
+    bsk.set_option("gemv_kernel", 5)
+    try:
+        W, x = operands(M, K, n, True)
+        _, want = oracle.linear_bf16(W, x, M, K, n)
+        assert np.array_equal(run(W, x, M, K, n), want)
+        W, x = operands(M, K, n, False)
+        ref, _ = oracle.linear_bf16(W, x, M, K, n)
+        check_tolerance(run(W, x, M, K, n), ref, "bf16", K, absmax_bf16(x), absmax_bf16(W),
+                        f"{M}x{K} n={n} block_m={block_m}")
+    finally:
+        bsk.set_option("block_m", 0)
+        bsk.set_option("gemv_kernel", 0)
+
+
 def test_k_zero_and_empty():
     got = run(np.zeros(0, np.uint16), np.zeros(0, np.uint16), 50, 0, 3)
     assert np.all(got == 0)

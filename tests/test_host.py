@@ -20,23 +20,38 @@ def lib():
     return bsk.load()
 
 
-def header_functions():
-    text = open(os.path.join(ROOT, "include", "bsk.h")).read()
+def header_functions(path=("include", "bsk.h")):
+    text = open(os.path.join(ROOT, *path)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?(?:int|void|long long|char)\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
+TUNING_HEADER = ("bf16_gemm_skinny_gb300", "csrc", "bsk_tuning.h")
+
+
 def test_header_declares_the_bound_symbols():
     assert header_functions() == sorted(bsk.EXPORTS)
+    assert header_functions(TUNING_HEADER) == sorted(bsk.TUNING_EXPORTS)
+
+
+def test_public_header_holds_no_tuning_state_or_test_hook():
+    """The C ABI holds the product calls only: the process-wide options and the
+    test hooks live in the internal tuning header."""
+    public = header_functions()
+    for name in bsk.TUNING_EXPORTS:
+        assert name not in public, name
+    text = open(os.path.join(ROOT, "include", "bsk.h")).read()
+    assert "BSK_OPT_" not in text
 
 
 def test_library_exports_every_header_symbol(lib):
-    for name in header_functions():
+    names = header_functions() + header_functions(TUNING_HEADER)
+    for name in names:
         assert hasattr(lib, name), name
     out = os.popen(f"nm -D --defined-only {bsk.library_path()}").read()
     exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
-    missing = set(header_functions()) - exported
+    missing = set(names) - exported
     assert not missing, missing
 
 
