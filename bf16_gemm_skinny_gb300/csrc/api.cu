@@ -327,28 +327,16 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     // shape 1.00, 4095 x 4097 x 4100 and 8192^2 x 4096 1.03.
     const bool dyn = pair && !stream_k && opt_or(BSK_OPT_TILE_SCHED, 0) == 2;
     // Tile height of the one-CTA kernel on a K-major A with one tile column (the
-    // skinny decode shapes): the rows per tile -- a multiple of 8 from 32 to 128
-    // -- that leave each CTA the fewest rows, so that the CTAs fill the SMs
-    // evenly and finish together.  The 34816-row decode weight on 152 SMs: 291
-    // tiles of 120 rows on 146 CTAs (240 rows each) instead of 272 tiles of 128
-    // rows on 136 CTAs (256 each).
+    // skinny decode shapes): 128 rows, or fewer on request.  Heights that leave
+    // every CTA the fewest rows -- the 34816-row decode weight as 291 tiles of
+    // 120 rows on 146 CTAs, 240 rows each, instead of 272 tiles of 128 on 136
+    // CTAs -- measured 1.2 us slower per launch on GB300 (n = 4 and 8, chains of
+    // 24 launches: 59.2 / 58.6 us against 57.8 / 57.4), so they are not the
+    // default.
     int block_m = 128;
     const long long bm_opt = opt_or(BSK_OPT_BLOCK_M, 0);
-    if (!pair && !stream_k && !op.a_mn_major && (op.N + block_n - 1LL) / block_n == 1) {
-        if (bm_opt > 0) {
-            block_m = static_cast<int>(bm_opt);
-        } else {
-            long long best = LLONG_MAX;
-            for (int h = 128; h >= 32; h -= 8) {
-                const long long tiles = (op.M + h - 1LL) / h;
-                const long long rows = (tiles + sms - 1) / sms * h;
-                if (rows < best) {
-                    best = rows;
-                    block_m = h;
-                }
-            }
-        }
-    }
+    if (!pair && !stream_k && !op.a_mn_major && (op.N + block_n - 1LL) / block_n == 1 && bm_opt > 0)
+        block_m = static_cast<int>(bm_opt);
     // one slot per CTA: block_n x 128 FP32 (CTA pairs: each CTA's 128 rows of a 256-wide tile)
     const size_t sk_part_bytes = stream_k ? static_cast<size_t>(sms) * block_n * 128 * sizeof(float) : 0;
     const size_t sk_flag_bytes = stream_k ? static_cast<size_t>(sms) * sizeof(int) : 0;
@@ -425,8 +413,13 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     g.stream_k = stream_k;
     g.sk_part = sk_part;
     g.sk_flag = sk_flag;
-    // Tile-row group: measured best on GB300 for 8192^3-class and prefill shapes.
-    g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, g.pair && g.block_n == 256 ? 2 : 16));
+    // Tile-row group ("Hygon 优化", section 分组调度).  CTA pairs: 8.  Measured on
+    // GB300 on 8192^2 x 16384, one launch (cold L2): DRAM reads 4.54 / 4.35 /
+    // 2.34 / 3.46 GB for GROUP_M 2 / 4 / 8 / 16, 1.235 / 1.238 / 1.169 / 1.204
+    // ms; back to back for seconds under the 1.4 kW cap every setting does the
+    // same work per SM cycle and 8 runs at the highest clock: 1580 / 1631 /
+    // 1644 / 1622 TFLOP/s.  One CTA per tile: 16.
+    g.group_m = static_cast<int>(opt_or(BSK_OPT_GROUP_M, g.pair && g.block_n == 256 ? 8 : 16));
     // TMA store of C: 16-byte aligned base and ldc, and M a multiple of 8.  With
     // a ragged M the store's clipping was seen to write up to the end of the
     // last 16-byte unit, i.e. into C's padding rows when ldc > M.

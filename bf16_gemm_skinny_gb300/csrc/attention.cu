@@ -598,11 +598,8 @@ int launch_split(const AttnLaunch& a, const AttnParams& p, cudaStream_t stream, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    static SmemOptIn merge_attrs;
-    e = merge_attrs.ensure(reinterpret_cast<const void*>(attn_merge_kernel<HD>), 0);
-    if (e == cudaSuccess)
-        e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, static_cast<const float*>(p.partial),
-                               reinterpret_cast<__nv_bfloat16*>(a.out), a.num_segments);
+    e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, static_cast<const float*>(p.partial),
+                           reinterpret_cast<__nv_bfloat16*>(a.out), a.num_segments);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "attention merge launch failed: %s", cudaGetErrorString(e));

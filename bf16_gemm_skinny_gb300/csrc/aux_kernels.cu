@@ -39,10 +39,12 @@ struct PackJob {
     unsigned blocks;           // CTAs working on this job
 };
 
-constexpr int kPackThreads = 256;
-constexpr int kPackBufs = 4;                     // pieces in flight per CTA
-constexpr int kPackPiece = 8192;                 // longest piece, bytes
+constexpr int kPackThreads = 256;                // warp 0: producer (one lane); warps 1..7: consumers
+constexpr int kPackConsumers = kPackThreads - 32;
+constexpr int kPackBufs = 6;                     // pieces in flight per CTA
+constexpr int kPackPiece = 8704;                 // longest piece, bytes (an 8200-byte line is one piece)
 constexpr int kPackBufBytes = kPackPiece + 32;   // a piece's aligned cover plus the chunk read past it
+constexpr int kPackSmem = kPackBufs * kPackBufBytes + 2 * kPackBufs * 8 + 16;
 constexpr int kPackCtasPerSm = 4;
 constexpr int kSitePack = 0x20;                  // wait site reported on a timeout
 
@@ -52,27 +54,39 @@ constexpr int kSitePack = 0x20;                  // wait site reported on a time
 // operands that shape in a workspace without touching the caller's buffers
 // ("MTT S4000 GEMM 优化中的分块、尾处理与并发实战复盘", section 1: inputs may not be modified).
 //
-// Each CTA takes a contiguous range of units (line pieces).  For each, one
-// thread issues a bulk copy of the piece's 16-byte-aligned cover -- from the
-// aligned chunk holding its first byte to the end of the chunk holding its
-// last, so no byte outside the pages the piece touches is read -- into one of
-// kPackBufs shared-memory buffers, completing on that buffer's mbarrier, so
-// kPackBufs pieces per CTA are in flight.  Once a piece has landed, thread t
-// writes output chunks t, t + 256, ...: chunk c is the 16 bytes that start m
-// bytes into buffer chunk c (m = the piece's offset from a 16-byte boundary),
-// shifted out of buffer chunks c and c + 1, with one aligned 16-byte store.  A
-// line's last chunk may carry up to 15 bytes past the line's end into the
-// destination's padding (its leading dimension is rounded up to 16 bytes; the
-// GEMM's tensor maps never read the padding).  Every wait is bounded.
+// Each CTA takes a contiguous range of units (line pieces) through a ring of
+// kPackBufs shared-memory buffers, each with a "full" and an "empty" mbarrier.
+// One lane of warp 0 (the producer) issues, for each unit, a bulk copy of the
+// piece's 16-byte-aligned cover -- from the aligned chunk holding its first
+// byte to the end of the chunk holding its last, so no byte outside the pages
+// the piece touches is read -- completing on the buffer's full barrier, as
+// soon as the consumers have released the buffer.  The source is read with an
+// evict-first L2 policy: it is read once, and the packed copy, which the GEMM
+// reads next, should stay in L2.  Warps 1..7 (the consumers) wait for a
+// buffer, and consumer thread t writes output chunks t, t + 224, ...: chunk c
+// is the 16 bytes that start m bytes into buffer chunk c (m = the piece's
+// offset from a 16-byte boundary), shifted out of buffer chunks c and c + 1,
+// with one aligned 16-byte store; each warp then arrives on the buffer's empty
+// barrier.  A line's last chunk may carry up to 15 bytes past the line's end
+// into the destination's padding (its leading dimension is rounded up to 16
+// bytes; the GEMM's tensor maps never read the padding).  Every wait is
+// bounded; on a timeout the producer waits for its copies in flight before the
+// CTA exits.
 __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm)
     pack_kernel(PackJob j0, PackJob j1, int* status, unsigned long long limit_ns)
 {
-    __shared__ __align__(128) uint8_t buf[kPackBufs][kPackBufBytes];
-    __shared__ __align__(8) uint64_t bars[kPackBufs];
-    __shared__ uint32_t abort_flag;
+    extern __shared__ __align__(128) uint8_t pack_smem[];
+    uint8_t* const bufs = pack_smem;
+    const uint32_t full0 = smem_u32(pack_smem + kPackBufs * kPackBufBytes);
+    const uint32_t empty0 = full0 + 8 * kPackBufs;
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(pack_smem + kPackBufs * kPackBufBytes +
+                                                                          16 * kPackBufs);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kPackBufs; ++i) mbar_init(smem_u32(&bars[i]), 1);
-        abort_flag = 0u;
+        for (int i = 0; i < kPackBufs; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, kPackConsumers / 32);
+        }
+        *abort_flag = 0u;
         fence_mbar_init();
     }
     __syncthreads();
@@ -84,61 +98,95 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm)
     const long long u0 = j.units * b / j.blocks;
     const long long n = j.units * (b + 1) / j.blocks - u0;
 
-    // source start, destination start and length of unit u
-    auto piece = [&](long long u, const uint8_t*& s, uint8_t*& d, long long& len) {
-        const long long line = u / j.pieces;
-        const long long off = (u - line * j.pieces) * j.piece_bytes;
-        s = j.src + line * j.ld_src + off;
-        d = j.dst + line * j.ld_dst + off;
-        len = j.line_bytes - off < j.piece_bytes ? j.line_bytes - off : j.piece_bytes;
-    };
-    // thread 0: unit u0 + i into buffer i % kPackBufs
-    auto issue = [&](long long i) {
+    // A cursor over this CTA's units: the unit's source and destination starts
+    // and length, advanced without division (one division per CTA, for the start).
+    struct Cursor {
         const uint8_t* s;
         uint8_t* d;
+        long long off;   // offset of the piece in its line
         long long len;
-        piece(u0 + i, s, d, len);
-        const uintptr_t a = reinterpret_cast<uintptr_t>(s);
-        const uintptr_t lo = a & ~static_cast<uintptr_t>(15);
-        const uintptr_t hi = (a + static_cast<uintptr_t>(len) + 15) & ~static_cast<uintptr_t>(15);
-        const uint32_t bar = smem_u32(&bars[i % kPackBufs]);
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(hi - lo));
-        bulk_load(smem_u32(buf[i % kPackBufs]), reinterpret_cast<const void*>(lo), static_cast<uint32_t>(hi - lo), bar);
     };
-    if (threadIdx.x == 0)
-        for (long long i = 0; i < n && i < kPackBufs; ++i) issue(i);
+    const long long line0 = u0 / j.pieces;
+    const long long off0 = (u0 - line0 * j.pieces) * j.piece_bytes;
+    const Cursor start{j.src + line0 * j.ld_src + off0, j.dst + line0 * j.ld_dst + off0, off0,
+                       j.line_bytes - off0 < j.piece_bytes ? j.line_bytes - off0 : j.piece_bytes};
+    auto advance = [&](Cursor& c) {
+        if (c.off + j.piece_bytes < j.line_bytes) {
+            c.off += j.piece_bytes;
+            c.s += j.piece_bytes;
+            c.d += j.piece_bytes;
+        } else {   // next line
+            c.s += j.ld_src - c.off;
+            c.d += j.ld_dst - c.off;
+            c.off = 0;
+        }
+        c.len = j.line_bytes - c.off < j.piece_bytes ? j.line_bytes - c.off : j.piece_bytes;
+    };
+    const WaitCtl wc{abort_flag, status, limit_ns};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const WaitCtl wc{&abort_flag, status, limit_ns};
-    long long i = 0;
-    for (; i < n; ++i) {
-        const int bi = static_cast<int>(i % kPackBufs);
-        const bool ok = mbar_wait(smem_u32(&bars[bi]), static_cast<uint32_t>(i / kPackBufs) & 1u, wc, kSitePack);
-        if (!__syncthreads_and(ok)) break;
-        const uint8_t* s;
-        uint8_t* d;
-        long long len;
-        piece(u0 + i, s, d, len);
-        const unsigned m = static_cast<unsigned>(reinterpret_cast<uintptr_t>(s) & 15u);
-        const uint4* sb = reinterpret_cast<const uint4*>(buf[bi]);
-        const unsigned chunks = static_cast<unsigned>((len + 15) / 16);
-        for (unsigned c = threadIdx.x; c < chunks; c += kPackThreads) {
-            const uint4 lo = sb[c];
-            *reinterpret_cast<uint4*>(d + 16ull * c) = m == 0u ? lo : realign16(lo, sb[c + 1], m);
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t read_once = l2_policy_evict_first();
+            long long issued = 0;
+            bool ok = true;
+            Cursor cur = start;
+            int bi = 0;
+            uint32_t ph = 0;   // parity of the empty-barrier phase to wait for, once the ring has wrapped
+            for (; issued < n; ++issued) {
+                if (issued >= kPackBufs && !mbar_wait(empty0 + 8 * bi, ph, wc, kSitePack)) {
+                    ok = false;
+                    break;
+                }
+                const uintptr_t a = reinterpret_cast<uintptr_t>(cur.s);
+                const uintptr_t lo = a & ~static_cast<uintptr_t>(15);
+                const uintptr_t hi = (a + static_cast<uintptr_t>(cur.len) + 15) & ~static_cast<uintptr_t>(15);
+                mbar_arrive_expect_tx(full0 + 8 * bi, static_cast<uint32_t>(hi - lo));
+                bulk_load_hint(smem_u32(bufs + bi * kPackBufBytes), reinterpret_cast<const void*>(lo),
+                               static_cast<uint32_t>(hi - lo), full0 + 8 * bi, read_once);
+                advance(cur);
+                if (++bi == kPackBufs) {
+                    bi = 0;
+                    if (issued + 1 > kPackBufs) ph ^= 1u;
+                }
+            }
+            if (!ok) {
+                // abort: the copies of the last issued units may still be landing in
+                // this CTA's shared memory; wait for them (bounded) before exiting
+                uint32_t never = 0u;
+                const WaitCtl wc_drain{&never, status, limit_ns};
+                for (long long k = issued > kPackBufs ? issued - kPackBufs : 0; k < issued; ++k)
+                    mbar_wait(full0 + 8 * (k % kPackBufs), static_cast<uint32_t>(k / kPackBufs) & 1u, wc_drain,
+                              kSitePack);
+            }
         }
-        __syncthreads();   // every thread has read the buffer before it is refilled
-        if (threadIdx.x == 0 && i + kPackBufs < n) {
-            fence_proxy_async_smem();
-            issue(i + kPackBufs);
+    } else {
+        const unsigned t = threadIdx.x - 32;
+        Cursor cur = start;
+        int bi = 0;
+        uint32_t ph = 0;
+        for (long long i = 0; i < n; ++i) {
+            const bool ok = mbar_wait(full0 + 8 * bi, ph, wc, kSitePack);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const unsigned m = static_cast<unsigned>(reinterpret_cast<uintptr_t>(cur.s) & 15u);
+            const uint4* sb = reinterpret_cast<const uint4*>(bufs + bi * kPackBufBytes);
+            const unsigned chunks = static_cast<unsigned>((cur.len + 15) / 16);
+            uint4* out = reinterpret_cast<uint4*>(cur.d);
+            if (m == 0u) {
+                for (unsigned c = t; c < chunks; c += kPackConsumers) out[c] = sb[c];
+            } else {
+                for (unsigned c = t; c < chunks; c += kPackConsumers) out[c] = realign16(sb[c], sb[c + 1], m);
+            }
+            __syncwarp();   // the warp has read the buffer
+            if (lane == 0) mbar_arrive(empty0 + 8 * bi);
+            advance(cur);
+            if (++bi == kPackBufs) {
+                bi = 0;
+                ph ^= 1u;
+            }
         }
     }
-    if (i < n && threadIdx.x == 0) {
-        // abort: the copies issued and not consumed must land before the CTA exits
-        uint32_t never = 0u;
-        const WaitCtl wc_drain{&never, status, limit_ns};
-        const long long issued = n < i + kPackBufs ? n : i + kPackBufs;
-        for (long long k = i; k < issued; ++k)
-            mbar_wait(smem_u32(&bars[k % kPackBufs]), static_cast<uint32_t>(k / kPackBufs) & 1u, wc_drain, kSitePack);
-    }
+    __syncthreads();
 }
 
 // C(m,n) = bias value (or +0.0) for m < M, n < N, C(m,n) at C[m + n*ldc]: the
@@ -238,11 +286,11 @@ int launch_pack(const PackCopy* copies, int n, int sms, bool pdl, int* status, u
     b1 = std::min<unsigned long long>(b1, nj > 1 ? static_cast<unsigned long long>(jobs[1].units) : 0ull);
     jobs[0].blocks = static_cast<unsigned>(b0);
     jobs[1].blocks = static_cast<unsigned>(b1);
-    static SmemOptIn attrs;
-    cudaError_t e = attrs.ensure(reinterpret_cast<const void*>(pack_kernel), 0);
+    static SmemOptIn smem_opt;
+    cudaError_t e = smem_opt.ensure(reinterpret_cast<const void*>(pack_kernel), kPackSmem);
     if (e == cudaSuccess)
-        e = launch_kernel(pack_kernel, dim3(static_cast<unsigned>(b0 + b1)), dim3(kPackThreads), 0, stream, pdl,
-                          jobs[0], jobs[1], status, limit_ns);
+        e = launch_kernel(pack_kernel, dim3(static_cast<unsigned>(b0 + b1)), dim3(kPackThreads),
+                          static_cast<size_t>(kPackSmem), stream, pdl, jobs[0], jobs[1], status, limit_ns);
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "pack launch failed: %s", cudaGetErrorString(e));
         return 1;
@@ -257,12 +305,8 @@ int launch_fill_bias(uint16_t* C, long long ldc, int M, int N, const uint16_t* b
     if (total <= 0) return 0;
     long long grid = (total + 255) / 256;
     if (grid > 4096) grid = 4096;
-    static SmemOptIn attrs;
-    cudaError_t e = attrs.ensure(reinterpret_cast<const void*>(fill_bias_kernel), 0);
-    if (e == cudaSuccess) {
-        fill_bias_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(C, ldc, M, N, bias, bias_mode);
-        e = cudaGetLastError();
-    }
+    fill_bias_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(C, ldc, M, N, bias, bias_mode);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "fill launch failed: %s", cudaGetErrorString(e));
         return 1;

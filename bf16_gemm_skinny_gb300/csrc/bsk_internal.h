@@ -74,20 +74,16 @@ void record_error(const char* msg);
 // cuTensorMapEncodeTiled from the driver (resolved once through the runtime).
 TmapEncodeFn tmap_encoder();
 
-// Sets one kernel's launch attributes once per device: a launcher keeps one of
-// these in a function-local static next to the kernel it launches, so the
-// attribute calls are not repeated on every launch (they cost host time that
-// short kernels would otherwise wait for).
-//  * the dynamic shared-memory limit, raised to `bytes`;
-//  * the preferred carveout: every kernel of the library asks for the largest
-//    shared-memory share of the SM's L1/shared storage.  The GEMM kernels need
-//    it (about 200 KB per CTA), and when consecutive kernels in a stream ask
-//    for different carveouts the SMs are reconfigured between them, which
-//    delays the second kernel's start (its loads use no L1 allocation, so the
-//    smaller L1 costs nothing).
+// Raises one kernel's dynamic shared-memory limit, once per device: a launcher
+// keeps one of these in a function-local static next to the kernel it launches,
+// so the attribute call is not repeated on every launch (it costs host time
+// that short kernels would otherwise wait for).  (Asking every kernel for the
+// largest shared-memory carveout, so that consecutive kernels need no SM
+// reconfiguration, was measured on GB300 and dropped: the CUDA-core GEMV then
+// ran 52.5 -> 62.3 us per launch.)
 struct SmemOptIn {
     static constexpr int kMaxDevices = 128;
-    std::atomic<int> done[kMaxDevices];   // 1 + bytes already allowed on each device (static storage: 0 = none yet)
+    std::atomic<int> done[kMaxDevices];   // bytes already allowed on each device (static storage: zero)
 
     cudaError_t ensure(const void* kernel, int bytes)
     {
@@ -95,15 +91,9 @@ struct SmemOptIn {
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         const bool slot = dev >= 0 && dev < kMaxDevices;
-        const int have = slot ? done[dev].load(std::memory_order_acquire) : 0;
-        if (have > bytes) return cudaSuccess;
-        if (have == 0) {
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-            if (e != cudaSuccess) return e;
-        }
-        if (bytes > 0) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e == cudaSuccess && slot) done[dev].store(bytes + 1, std::memory_order_release);
+        if (slot && done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess && slot) done[dev].store(bytes, std::memory_order_release);
         return e;
     }
 };

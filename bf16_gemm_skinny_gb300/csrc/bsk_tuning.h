@@ -27,7 +27,7 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
 /*
  * Tuning and test options (process-wide; not thread-safe; 0 restores the
  * default).  Keys:
- *   BSK_OPT_GROUP_M          GEMM tile-row group size (default 2 for CTA pairs, 16 otherwise)
+ *   BSK_OPT_GROUP_M          GEMM tile-row group size (default 8 for CTA pairs, 16 otherwise)
  *   BSK_OPT_BLOCK_N          GEMM tile width 32, 64, 128 or 256 (default: the smallest of
  *                            32/64/128 that covers N, else 256)
  *   BSK_OPT_FORCE_PACK       1: pack A and B even when aligned
@@ -66,8 +66,7 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *                            are free first; BSK_OPT_NUM_SMS does not cap this grid)
  *   BSK_OPT_BLOCK_M          rows per tile of the one-CTA GEMM kernel with a K-major A and a
  *                            single tile column (the skinny decode shapes): 8..128, a
- *                            multiple of 8 (default: the height that leaves each CTA the
- *                            fewest rows; other shapes always use 128)
+ *                            multiple of 8 (default 128; other shapes always use 128)
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {

@@ -696,11 +696,8 @@ int launch_scalar(const GemvLaunch& g, cudaStream_t stream, char* msg, size_t ms
     const long long cap = static_cast<long long>(g.num_sms) * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    static SmemOptIn attrs;
-    cudaError_t e = attrs.ensure(reinterpret_cast<const void*>(gemv_bf16_scalar_kernel<NT>), 0);
-    if (e == cudaSuccess)
-        e = launch_kernel(gemv_bf16_scalar_kernel<NT>, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, stream,
-                          g.pdl, g.W, g.x, reinterpret_cast<__nv_bfloat16*>(g.y), g.M, g.K);
+    cudaError_t e = launch_kernel(gemv_bf16_scalar_kernel<NT>, dim3(static_cast<unsigned>(grid)), dim3(threads), 0,
+                                  stream, g.pdl, g.W, g.x, reinterpret_cast<__nv_bfloat16*>(g.y), g.M, g.K);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "GEMV launch failed: %s", cudaGetErrorString(e));
