@@ -267,7 +267,7 @@ def oracle_gemm_sample(A, B, seconds: float, max_cols: int = 4096):
     while elapsed < seconds and done < max_cols:
         cols = [(col + i * 977) % GEMM_N for i in range(batch)]
         t0 = time.perf_counter()
-        oracle.gemm_f16_colmajor(A, B, GEMM_M, GEMM_N, GEMM_K, cols=cols)
+        oracle.gemm_f16_colmajor(A, B, GEMM_M, GEMM_N, GEMM_K, cols=cols, threads=threads)
         elapsed += time.perf_counter() - t0
         done += batch
         col += 1
@@ -328,42 +328,44 @@ def timed_batches(run_batch, seconds: float, first: int, cap: int):
     return done, elapsed
 
 
-def oracle_configs(seconds_each: float):
-    """The oracle on all host cores for every workload, each on a bounded sample
-    of its outputs (whole output columns of a GEMM, whole output features of a
-    linear layer): rate, sample and seconds per workload."""
+def oracle_configs(seconds_each: float, threads: int):
+    """The oracle on `threads` host threads for every workload, each on a bounded
+    sample of its outputs (whole output columns of a GEMM, whole output features
+    of a linear layer): rate, sample and seconds per workload.  The thread count
+    is passed to every call: the oracle's OpenMP setting persists between calls."""
     import oracle
     from bf16_gemm_skinny_gb300 import inputs
 
-    threads = oracle.max_threads()
     out = {}
     for name, (M, N, K, dist) in (("gemm_256x256x256", (256, 256, 256, "uniform")),
                                    ("gemm_4095x4097x4100", (4095, 4097, 4100, "normal0.5"))):
         A, B = inputs.gemm_operands(M, N, K, dist)
         if M == 256:
-            reps, el = timed_batches(lambda i0, c: [oracle.gemm_f16_colmajor(A, B, M, N, K) for _ in range(c)],
-                                     seconds_each, 1, 1 << 16)
+            reps, el = timed_batches(lambda i0, c: [oracle.gemm_f16_colmajor(A, B, M, N, K, threads=threads)
+                                                    for _ in range(c)], seconds_each, 1, 1 << 16)
             out[name] = {"tflops": 2.0 * M * N * K * reps / el / 1e12, "sample": f"the whole GEMM, {reps} times",
                          "s": round(el, 2)}
         else:
             cols, el = timed_batches(lambda i0, c: oracle.gemm_f16_colmajor(
-                A, B, M, N, K, cols=[(i0 + i) * 131 % N for i in range(c)]), seconds_each, threads, N)
+                A, B, M, N, K, cols=[(i0 + i) * 131 % N for i in range(c)], threads=threads), seconds_each, threads, N)
             out[name] = {"tflops": 2.0 * M * K * cols / el / 1e12,
                          "sample": f"{cols} of {N} output columns", "s": round(el, 2)}
     W, _ = inputs.linear_operands(GEMV_M, GEMV_K, 1, "normal0.02", "normal1")
     for n in GEMV_NS:
         _, x = inputs.linear_operands(1, GEMV_K, n, "normal0.02", "normal1")
         rows, el = timed_batches(lambda i0, c: oracle.linear_bf16(
-            W, x, GEMV_M, GEMV_K, n, js=[(i0 + i) * 977 % GEMV_M for i in range(c)]), seconds_each, 4 * threads, GEMV_M)
+            W, x, GEMV_M, GEMV_K, n, js=[(i0 + i) * 977 % GEMV_M for i in range(c)], threads=threads), seconds_each,
+            4 * threads, GEMV_M)
         out[f"gemv_34816x5120_n{n}"] = {"gbs": rows * GEMV_K * 2 / el / 1e9, "sample": f"{rows} of {GEMV_M} output "
                                         "features (GB/s of weights read)", "s": round(el, 2)}
     _, X = inputs.linear_operands(1, GEMV_K, S_PREFILL, "normal0.02", "normal1")
     feats, el = timed_batches(lambda i0, c: oracle.linear_bf16(
-        W, X, GEMV_M, GEMV_K, S_PREFILL, js=[(i0 + i) * 977 % GEMV_M for i in range(c)]), seconds_each, threads,
-        GEMV_M)
+        W, X, GEMV_M, GEMV_K, S_PREFILL, js=[(i0 + i) * 977 % GEMV_M for i in range(c)], threads=threads),
+        seconds_each, threads, GEMV_M)
     out["prefill_4096x34816x5120"] = {"tflops": 2.0 * S_PREFILL * GEMV_K * feats / el / 1e12,
                                       "sample": f"{feats} of {GEMV_M} output features", "s": round(el, 2)}
     for v in out.values():
+        v["threads"] = threads
         for key in ("tflops", "gbs"):
             if key in v:
                 v[key] = round(v[key], 5)
@@ -372,11 +374,11 @@ def oracle_configs(seconds_each: float):
 
 def cpu_baseline(A, B, seconds: float, seconds_each: float = 2.5):
     flops, elapsed, cols, threads = oracle_gemm_sample(A, B, seconds)
+    configs = oracle_configs(seconds_each, threads)
     return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{cols} output columns of the 8192x8192x16384 GEMM (each 8192x16384 FMAs, FP64), "
                       f"{elapsed:.1f} s",
-            "cpu": cpu_model(), "single_thread": single_thread_rates(),
-            "configs": oracle_configs(seconds_each)}
+            "cpu": cpu_model(), "configs": configs, "single_thread": single_thread_rates()}
 
 
 # ---------------------------------------------------------------------------
@@ -774,7 +776,7 @@ def run_ours(args):
             "single_launch_us": round(single_ms[n] * 1e3, 2),
             "single_launch_frac": round(gemv_bytes(n) / (single_ms[n] * 1e-3) / 1e9 / hbm_peak, 4),
             "kernel": ("gemv_bf16_kernel (CUDA cores, register streaming)" if n <= 3 else
-                       "gemm_tcgen05_kernel<BN 32, K-major A, BF16> (tensor cores, balanced tile heights)"),
+                       "gemm_tcgen05_kernel<BN 32, K-major A, BF16> (tensor cores, 128 x 32 tiles)"),
             "cuda_core_best": {"kernel": kernel_names[kc], "us": round(ms_cc * 1e3, 2),
                                "frac": round(gemv_bytes(n) / (ms_cc * 1e-3) / 1e9 / hbm_peak, 4)},
             "e2e_gbs": round(world * gemv_bytes(n) / e2e_gemv_s[n] / 1e9, 1)}

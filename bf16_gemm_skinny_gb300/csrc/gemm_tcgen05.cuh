@@ -373,12 +373,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmB);
         if (p.tma_store) prefetch_tmap(&tmC);
         if (p.sk == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
-            // The first tile's first stages into L2 while the kernel before this
-            // one may still be running (a prefetch is coherent: nothing reaches
-            // shared memory before griddep_wait below).
+            // The first tile's first two stages into L2 while the kernel before
+            // this one may still be running (a prefetch is coherent: nothing
+            // reaches shared memory before griddep_wait below).  Two, not the
+            // whole ring: the TMA unit works through the prefetches before the
+            // real loads, and a launch with nothing to overlap waits for them.
+            // Measured on the 34816 x 5120 decode shape (n = 4 and 8), first data
+            // after the prologue 4.5-5.6 us with the whole ring prefetched, 1.9-2.4
+            // us with two stages, kernel span 61-62 -> 59-60 us.
             int pm, pn;
             tile_coord(static_cast<int>(blockIdx.x), p.num_m, p.num_n, p.group_m, &pm, &pn);
-            const int kbs = p.num_kb < S ? p.num_kb : S;
+            constexpr int kPrefetchStages = S < 2 ? S : 2;
+            const int kbs = p.num_kb < kPrefetchStages ? p.num_kb : kPrefetchStages;
             for (int kb = 0; kb < kbs; ++kb) {
                 const int k0 = kb * Ty::kBK;
                 if constexpr (A_MN) {
