@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdio>
+#include <type_traits>
 
 #include "bsk_internal.h"
 #include "ptx.cuh"
@@ -237,22 +238,41 @@ __device__ __forceinline__ uint16_t round_out(uint32_t acc_bits)
 }
 
 // Masked column-major stores of one lane's row m, columns n0..n0+31 (rows at
-// or past m_end -- the end of C or of the tile -- store nothing).
+// or past m_end -- the end of C or of the tile -- store nothing).  The lanes of
+// a warp hold consecutive rows, so each store instruction writes 32 adjacent
+// elements of one column.  The column address advances by a running pointer
+// and the column bound is tested once per 32 columns: the epilogue warps share
+// their schedulers with the producer and the MMA issuer, and per-element
+// 64-bit index arithmetic (about 15 instructions per element) slowed the
+// tensor pipe's feed (measured on 4096^3: 99 us against 88 us with TMA stores;
+// the tensor pipe busy 74% instead of 85% of active cycles).
 template <int OUT>
 __device__ __forceinline__ void store_row(const uint32_t (&r)[32], const Params& p, int m, int n0, int m_end)
 {
     if (m >= m_end) return;
-    if constexpr (OUT == kOutF32) {
-        uint32_t* Cg = reinterpret_cast<uint32_t*>(p.C);
+    const int ncols = p.N - n0;
+    using E = typename std::conditional<OUT == kOutF32, uint32_t, uint16_t>::type;
+    E* q = reinterpret_cast<E*>(p.C) + (static_cast<long long>(m) + static_cast<long long>(n0) * p.ldc);
+    const long long step = p.ldc;
+    auto value = [&](int j) -> E {
+        if constexpr (OUT == kOutF32) {
+            return r[j];
+        } else {
+            return round_out<OUT>(r[j]);
+        }
+    };
+    if (ncols >= 32) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (n0 + j < p.N) Cg[static_cast<long long>(m) + static_cast<long long>(n0 + j) * p.ldc] = r[j];
+        for (int j = 0; j < 32; ++j) {
+            *q = value(j);
+            q += step;
+        }
     } else {
-        uint16_t* Cg = reinterpret_cast<uint16_t*>(p.C);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (n0 + j < p.N)
-                Cg[static_cast<long long>(m) + static_cast<long long>(n0 + j) * p.ldc] = round_out<OUT>(r[j]);
+        for (int j = 0; j < 32; ++j) {
+            if (j < ncols) *q = value(j);
+            q += step;
+        }
     }
 }
 
