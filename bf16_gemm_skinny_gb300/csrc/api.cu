@@ -280,7 +280,8 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     // 13 us of host and device time per call on GB300) outweigh the gain on
     // short problems and when the waves are already nearly full (measured: 272
     // tiles on 152 SMs 8% slower split; 4096 x 256 x 8192 13% faster split than
-    // on CTA pairs; 256^3 and 1024^3 twice as slow).  A 256-wide shape whose
+    // on CTA pairs before each tile's split was capped at four CTAs, 32.6 against
+    // 47 us after; 256^3 and 1024^3 twice as slow).  A 256-wide shape whose
     // CTA-pair tiles would fill under three quarters of the pairs runs split on
     // single CTAs instead.
     const long long kbs = (op.K + (fp8 ? 127LL : 63LL)) / (fp8 ? 128 : 64);
@@ -294,12 +295,15 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     // call's time is latency -- launch, first loads, one tile's MMAs, the
     // epilogue -- so narrower tiles on single CTAs spread it over more SMs.
     // 256^3 on GB300, calls back to back: 7.9 us per call on one CTA pair,
-    // 5.2 us on 128 x 128 tiles, 4.6 us on 128 x 64 tiles (8 CTAs).
+    // 5.2 us on 128 x 128 tiles, 4.5 us on 128 x 64 tiles (8 CTAs), 4.2 us on
+    // 128 x 32 tiles (16 CTAs).  128 x 32 tiles are taken while they fit in one
+    // wave (0.3 us faster than 128 x 64 from 256^3 to 640^3 and 1024 x 256 x
+    // 1024; 1024^3 would need two waves of them: 12.3 against 8.3 us).
     if (pair && gemm_kernel == 0 && bn_opt == 0 && kbs < 32) {
         const long long pair_tiles = ((op.M + 255LL) / 256) * ((op.N + 255LL) / 256);
         if (pair_tiles * 4 <= (sms / 2 > 0 ? sms / 2 : 1)) {
             pair = false;
-            block_n = op.N <= 32 && !op.b_mn_major ? 32 : 64;
+            block_n = !op.b_mn_major && m_tiles * ((op.N + 31LL) / 32) <= sms ? 32 : 64;
         }
     }
     if (pair && gemm_kernel == 0 && sk_opt != 1 && kbs >= 32) {

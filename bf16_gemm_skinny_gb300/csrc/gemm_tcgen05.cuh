@@ -179,6 +179,33 @@ __device__ __forceinline__ int sk_unit_of(const Params& p, long long i, int unit
     return static_cast<int>(((i + 1) * static_cast<long long>(units) + p.sk_iters - 1) / p.sk_iters) - 1;
 }
 
+// Stream-K fix-up: adds to r[j] the FP32 partials that CTAs first .. last left
+// for this lane's row, column j of the current 32-column chunk (p0 points at
+// CTA 0's slot entry for the chunk's first column; slots are `slot` floats
+// apart, columns 128 floats).  The slots are read four at a time so that
+// their loads are in flight together; the sums are taken in slot order.
+__device__ __forceinline__ void add_partials(uint32_t (&r)[32], const float* p0, long long slot, int first, int last)
+{
+    for (int q = first; q <= last; q += 4) {
+        float v[4][32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (q + u <= last) {
+                const float* pq = p0 + static_cast<long long>(q + u) * slot;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[u][j] = pq[j * kBM];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (q + u <= last) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + v[u][j]);
+            }
+        }
+    }
+}
+
 // Identifiers of the waits, reported in the status word on a timeout.
 enum WaitSite {
     kSiteProducerEmpty = 1,
@@ -612,11 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 32; ++j) ps[j * kBM] = __uint_as_float(r[j]);
                     continue;
                 }
-                for (int q = static_cast<int>(blockIdx.x) + 1; q <= q_last; ++q) {
-                    const float* pq = p.sk_part + static_cast<long long>(q) * BN * kBM + slot_col;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + pq[j * kBM]);
-                }
+                add_partials(r, p.sk_part + slot_col, static_cast<long long>(BN) * kBM, static_cast<int>(blockIdx.x) + 1,
+                             q_last);
                 finish_acc<IN, OUT>(r, p, m0 + lane, n0 + c * 32);
                 if (Ty::kOutBytes == 2 && p.tma_store && whole_quarter) {
                     uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
@@ -993,11 +1017,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 32; ++j) ps[j * kBM] = __uint_as_float(r[j]);
                     continue;
                 }
-                for (int q = pair + 1; q <= q_last; ++q) {
-                    const float* pq = p.sk_part + static_cast<long long>(q * 2 + static_cast<int>(rank)) * T * kBM + slot_col;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + pq[j * kBM]);
-                }
+                // slot of CTA (pair q, rank): (q * 2 + rank) * T * kBM
+                add_partials(r, p.sk_part + static_cast<long long>(rank) * T * kBM + slot_col, 2LL * T * kBM, pair + 1,
+                             q_last);
                 finish_acc<IN, OUT>(r, p, m0 + lane, n0 + c * 32);
                 if (Ty::kOutBytes == 2 && p.tma_store) {
                     uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
@@ -1155,6 +1177,15 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
         if (p.sk_dp_tiles == p.num_tiles) p.sk_dp_tiles -= grid;   // keep one wave to share
         p.sk_iters = static_cast<long long>(p.num_tiles - p.sk_dp_tiles) * p.num_kb;
         if (grid > p.sk_iters) grid = static_cast<int>(p.sk_iters);
+        if (p.sk_dp_tiles == 0) {
+            // Few tiles: the CTA that finishes a split tile adds the others' FP32
+            // partials one after another, so each tile is shared by at most four
+            // CTAs, each with at least 8 k-blocks.  256 x 256 x 2048 (2 tiles of
+            // 32 k-blocks): 64 CTAs of one k-block each took 114 us per call.
+            const long long split = p.num_kb / 8 < 1 ? 1 : (p.num_kb / 8 > 4 ? 4 : p.num_kb / 8);
+            const long long cap = static_cast<long long>(p.num_tiles) * split;
+            if (grid > cap) grid = static_cast<int>(cap);
+        }
         p.sk_part = g.sk_part;
         p.sk_flag = g.sk_flag;
         cudaLaunchAttribute attr[1];

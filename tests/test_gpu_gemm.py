@@ -287,6 +287,23 @@ def test_stream_k_on_cta_pairs(M, N, K, sms):
     sampled_check(got, A, B, M, N, K, cols, rows, True)
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 256, 2048), (128, 128, 16384), (300, 517, 2048), (512, 512, 4096),
+                                   (129, 33, 4160)])
+def test_few_tiles_long_k_default_schedule(M, N, K):
+    """Few tiles with a long k loop: the default plan shares each tile's k-blocks
+    between at most four CTAs (stream-K), whose owner adds the others' partials.
+    Integer inputs give the oracle's bits; random inputs stay within tolerance
+    and repeat bit for bit."""
+    A, B = operands(M, N, K, "int2")
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    assert np.array_equal(run(A, B, M, N, K), want)
+    Ar, Br = operands(M, N, K, "normal0.5")
+    got = run(Ar, Br, M, N, K)
+    assert np.array_equal(run(Ar, Br, M, N, K), got)
+    ref, _ = oracle.gemm_f16_colmajor(Ar, Br, M, N, K)
+    check_tolerance(got, ref, "f16", K, absmax_f16(Ar), absmax_f16(Br), f"few tiles {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("M,N,K", [(1000, 777, 1030), (256, 256, 64), (300, 517, 200), (2304, 2560, 1024),
                                    (4095, 4097, 4100)])
 def test_dynamic_tile_order_on_cta_pairs(M, N, K):
