@@ -42,6 +42,7 @@ OPTIONS = {
     "pdl": 12,
     "tile_sched": 13,
     "block_m": 14,
+    "split_k": 15,
 }
 
 # Every symbol include/bsk.h (the C ABI) declares.

@@ -46,7 +46,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 15;
+constexpr int kNumOpts = 16;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -275,15 +275,15 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     const long long gemm_kernel = opt_or(BSK_OPT_GEMM_KERNEL, 0);
     bool pair = block_n == 256 && gemm_kernel != 1;
     // Stream-K (one-CTA-per-tile kernel) when whole tiles would leave more than
-    // a quarter of the SM slots idle and each tile has at least 32 k-blocks to
-    // share.  Its fixed costs (workspace, flag reset, cooperative launch: about
+    // a quarter of the SM slots idle and each tile has at least 64 k-blocks to
+    // share (below that, whole tiles of the narrowest width that fits one wave).
+    // A 256-wide shape whose CTA-pair tiles would fill under three quarters of
+    // the pairs leaves the pairs for single CTAs from 32 k-blocks on.  Its fixed costs (workspace, flag reset, cooperative launch: about
     // 13 us of host and device time per call on GB300) outweigh the gain on
     // short problems and when the waves are already nearly full (measured: 272
     // tiles on 152 SMs 8% slower split; 4096 x 256 x 8192 13% faster split than
     // on CTA pairs before each tile's split was capped at four CTAs, 32.6 against
-    // 47 us after; 256^3 and 1024^3 twice as slow).  A 256-wide shape whose
-    // CTA-pair tiles would fill under three quarters of the pairs runs split on
-    // single CTAs instead.
+    // 47 us after; 256^3 and 1024^3 twice as slow).
     const long long kbs = (op.K + (fp8 ? 127LL : 63LL)) / (fp8 ? 128 : 64);
     const long long sk_opt = opt_or(BSK_OPT_STREAM_K, 0);
     auto fill = [&](long long tiles, long long slots) {
@@ -306,6 +306,16 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
             block_n = !op.b_mn_major && m_tiles * ((op.N + 31LL) / 32) <= sms ? 32 : 64;
         }
     }
+    // Short k loops: one CTA per 128 x 256 tile finishes before CTA pairs when a
+    // tile has at most 8 k-blocks, or at most 32 with all single-CTA tiles in one
+    // wave (GB300, calls back to back, pairs / single CTAs: 8192^2 x 256 57.2 /
+    // 50.5 us, 8192^2 x 512 63.1 / 57.0, 4096^2 x 512 22.0 / 19.6, 2048^2 x 1024
+    // 11.8 / 10.6, 2048^2 x 2048 16.7 / 15.5; 8192^2 x 1024 84.0 / 89.5 and
+    // 4096^2 x 1024 27.4 / 27.4 stay on pairs).
+    if (pair && gemm_kernel == 0 && bn_opt == 0) {
+        const long long single_tiles = m_tiles * ((op.N + 255LL) / 256);
+        if (kbs <= 8 || (kbs <= 32 && single_tiles <= sms)) pair = false;
+    }
     if (pair && gemm_kernel == 0 && sk_opt != 1 && kbs >= 32) {
         const long long pair_tiles = ((op.M + 255LL) / 256) * ((op.N + 255LL) / 256);
         if (fill(pair_tiles, sms / 2 > 0 ? sms / 2 : 1) < 0.75) pair = false;
@@ -313,7 +323,22 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     bool stream_k = false;
     if (!pair && sk_opt != 1) {
         const long long tiles = m_tiles * ((op.N + block_n - 1LL) / block_n);
-        stream_k = sk_opt == 2 || (fill(tiles, sms) < 0.75 && kbs >= 32);
+        const bool starved = fill(tiles, sms) < 0.75;
+        // Split only k loops of 64 k-blocks or more: at 32 its fixed costs and the
+        // owners' fix-up outweigh the gain (calls back to back on GB300, split
+        // against whole narrow tiles: 128 x 512 x 2048 20.6 / 12.0 us, 512 x 512 x
+        // 2048 21.4 / 12.1, 2048 x 512 x 2048 24.9 / 12.9, 8192 x 128 x 2048 21.1 /
+        // 12.9; at K = 4096 they are even, from K = 8192 on the split wins).
+        stream_k = sk_opt == 2 || (starved && kbs >= 64);
+        if (!stream_k && starved && bn_opt == 0 && gemm_kernel == 0) {
+            // whole tiles: the narrowest whose grid still fits in one wave
+            for (int bn = op.b_mn_major ? 64 : 32; bn < block_n; bn *= 2) {
+                if (m_tiles * ((op.N + bn - 1LL) / bn) <= sms) {
+                    block_n = bn;
+                    break;
+                }
+            }
+        }
     } else if (pair && sk_opt != 1) {
         // CTA pairs: whole waves first, the last (partial) wave shared -- on
         // request only.  The pair kernel runs under the power cap, so idle SMs in
@@ -323,6 +348,46 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
         // 4096 x 1024 x 4096 1.43 (fixed costs); inside a benchmark step of
         // GEMM + GEMVs the 8192^2 x 16384 gain did not show.
         stream_k = sk_opt == 2;
+    }
+    // Split-K over a cluster (one-CTA kernel): each tile's k loop is cut among a
+    // cluster of 2..16 CTAs that sum their FP32 partials through distributed
+    // shared memory -- no workspace, no flags, no cooperative launch.  For a
+    // tile-starved problem the plan with the least estimated time wins, from a
+    // model fitted to calls back to back on GB300: one CTA streams (128 + BN)
+    // 128-byte operand rows per k-block at about 80 GB/s (1.6 ns a row); a
+    // whole-tile launch costs about 4.3 us beyond that, a split one 5.6 us plus
+    // 31 ns per column of its tile (the partial, the barriers, the sums) and
+    // 0.5 us more for clusters of 16.  The largest cluster whose tiles all fit
+    // on the device at once is taken for each width.  Measured (us, plan
+    // chosen / best measured / whole tiles or stream-K): 128 x 128 x 16384
+    // 11.8 / 11.8 / 31.0, 128 x 512 x 16384 15.6 / 15.6 / 39.3, 256 x 1024 x
+    // 8192 16.9 / 16.9 / 29.3, 1024 x 256 x 4096 12.3 / 12.3 / 24.0, 128 x 512
+    // x 2048 8.6 / 8.6 / 12.5; 128 x 8192 x 2048 stays on whole tiles (13.4).
+    int skc = 0;
+    const long long skc_opt = opt_or(BSK_OPT_SPLIT_K, 0);
+    if (!pair && skc_opt >= 2) {
+        skc = static_cast<int>(skc_opt);
+        stream_k = false;
+    } else if (!pair && skc_opt == 0 && sk_opt == 0 && gemm_kernel == 0 && bn_opt == 0 && op.M > 0 && op.N > 0) {
+        const long long tiles_now = m_tiles * ((op.N + block_n - 1LL) / block_n);
+        if (fill(tiles_now, sms) < 0.75) {
+            auto row_ns = [](long long bn) { return (128 + bn) * 16 / 10; };   // per k-block
+            long long best = stream_k ? -1 : 4300 + kbs * ((tiles_now + sms - 1) / sms) * row_ns(block_n);
+            for (int bn = op.b_mn_major ? 64 : 32; bn <= 256; bn *= 2) {
+                const long long tiles = m_tiles * ((op.N + bn - 1LL) / bn);
+                for (int sz = 16; sz >= 2; sz /= 2) {
+                    if (kbs / sz < 2 || tiles > bsk::split_k_capacity(sz)) continue;
+                    const long long est = 5600 + 31LL * bn + (sz == 16 ? 500 : 0) + (kbs + sz - 1) / sz * row_ns(bn);
+                    if (best < 0 || est < best) {
+                        best = est;
+                        block_n = bn;
+                        skc = sz;
+                    }
+                    break;
+                }
+            }
+            if (skc > 1) stream_k = false;
+        }
     }
     // Tile order on CTA pairs (whole tiles): fixed unless the dynamic order --
     // one cluster per tile launched, a free pair taking the tile of a cluster
@@ -417,6 +482,7 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     g.stream_k = stream_k;
     g.sk_part = sk_part;
     g.sk_flag = sk_flag;
+    g.skc = skc;
     // Tile-row group ("Hygon 优化", section 分组调度).  CTA pairs: 8.  Measured on
     // GB300 on 8192^2 x 16384, one launch (cold L2): DRAM reads 4.54 / 4.35 /
     // 2.34 / 3.46 GB for GROUP_M 2 / 4 / 8 / 16, 1.235 / 1.238 / 1.169 / 1.204
@@ -1127,6 +1193,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_PDL: ok = value == 0 || value == 1; break;
     case BSK_OPT_TILE_SCHED: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_BLOCK_M: ok = value >= 0 && value <= 128 && value % 8 == 0; break;
+    case BSK_OPT_SPLIT_K: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

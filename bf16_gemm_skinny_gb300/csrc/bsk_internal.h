@@ -137,10 +137,15 @@ struct GemmLaunch {
     unsigned long long wait_limit_ns = 2000000000ull;
     bool pdl = true;         // whole-tile launches: programmatic dependent of the previous kernel
     bool dyn = false;        // CTA pairs, whole tiles: dynamic tile order (one cluster per tile launched)
+    int skc = 0;             // one-CTA kernel: split-K over clusters of skc CTAs (2..16, a power of two
+                             // dividing block_n); 0 = off
 };
 
 // Returns 0 on success; otherwise an error message is written to `msg`.
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
+// Clusters of `skc` CTAs of the one-CTA GEMM kernel that fit on the current
+// device at once (0 if the size is not available).
+int split_k_capacity(int skc);
 // The FP8 part of launch_gemm (gemm_fp8.cu).
 int launch_gemm_fp8(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
 

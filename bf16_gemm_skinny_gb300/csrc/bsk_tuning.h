@@ -67,6 +67,9 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_BLOCK_M          rows per tile of the one-CTA GEMM kernel with a K-major A and a
  *                            single tile column (the skinny decode shapes): 8..128, a
  *                            multiple of 8 (default 128; other shapes always use 128)
+ *   BSK_OPT_SPLIT_K          split-K over a cluster of the one-CTA GEMM kernel: 0 automatic
+ *                            (tile-starved problems), 1 off, 2 / 4 / 8 / 16 force that cluster
+ *                            size (one-CTA kernel, whole tiles; 16 needs a non-portable cluster)
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
@@ -83,7 +86,8 @@ enum {
     BSK_OPT_STREAM_K = 11,
     BSK_OPT_PDL = 12,
     BSK_OPT_TILE_SCHED = 13,
-    BSK_OPT_BLOCK_M = 14
+    BSK_OPT_BLOCK_M = 14,
+    BSK_OPT_SPLIT_K = 15
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);

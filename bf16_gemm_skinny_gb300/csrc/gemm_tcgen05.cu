@@ -73,6 +73,48 @@ int preload_gemm_f16_colmajor_kernels(char* msg, size_t msg_len)
     return 0;
 }
 
+int split_k_capacity(int skc)
+{
+    // Every instance of the one-CTA kernel takes one SM (its ring fills the
+    // shared memory), so the count is the same for all: queried once per device
+    // and size on one instance.
+    static std::atomic<int> cache[SmemOptIn::kMaxDevices][5];
+    if (skc < 1 || skc > 16 || (skc & (skc - 1)) != 0) return 0;
+    int lg = 0;
+    while ((1 << lg) < skc) ++lg;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= SmemOptIn::kMaxDevices) dev = -1;
+    int n = dev >= 0 ? cache[dev][lg].load(std::memory_order_acquire) : 0;
+    if (n > 0) return n;
+    using Cf = Cfg<32>;
+    auto kern = gemm_tcgen05_kernel<32, true, false, kInF16, kOutF16>;
+    static SmemOptIn smem_opt;
+    if (smem_opt.ensure(reinterpret_cast<const void*>(kern), Cf::kSmemBytes) != cudaSuccess ||
+        (skc > 8 && cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(skc);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(skc), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cf::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (n > 0 && dev >= 0) cache[dev][lg].store(n, std::memory_order_release);
+    return n;
+}
+
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
     if (g.in_type == kInE4M3 || g.in_type == kInE5M2) return launch_gemm_fp8(g, stream, msg, msg_len);

@@ -131,6 +131,12 @@ struct Params {
     // CTA pairs, whole tiles: 1 = dynamic tile order (the grid holds one cluster
     // per tile; later tiles come from clusters whose launch is cancelled)
     int dyn;
+    // One-CTA kernel: split-K over a cluster of skc CTAs (0 = off).  CTA r of
+    // the cluster takes k-blocks [r*kb/skc, (r+1)*kb/skc) of tile blockIdx.x /
+    // skc, leaves its FP32 partial in its own shared memory, and after a
+    // cluster barrier sums columns [r*BN/skc, (r+1)*BN/skc) of the tile over
+    // all skc partials (in rank order) and stores them.
+    int skc;
 };
 
 // The work of one unit (a CTA, or a CTA pair) of `units` as a sequence of
@@ -144,6 +150,11 @@ struct SegCursor {
 
 __device__ __forceinline__ SegCursor seg_first(const Params& p, int unit, int units)
 {
+    if (p.skc > 1) {
+        const long long base = static_cast<long long>(unit / p.skc) * p.num_kb;
+        const long long r = unit % p.skc;
+        return {0, 0, base + r * p.num_kb / p.skc, base + (r + 1) * p.num_kb / p.skc, 1};
+    }
     if (p.sk) {
         return {static_cast<long long>(unit), static_cast<long long>(p.sk_dp_tiles),
                 static_cast<long long>(unit) * p.sk_iters / units,
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         if (p.tma_store) prefetch_tmap(&tmC);
-        if (p.sk == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
+        if (p.sk == 0 && p.skc <= 1 && static_cast<int>(blockIdx.x) < p.num_tiles) {
             // The first tile's first two stages into L2 while the kernel before
             // this one may still be running (a prefetch is coherent: nothing
             // reaches shared memory before griddep_wait below).  Two, not the
@@ -633,6 +644,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
                 }
                 const long long slot_col = static_cast<long long>(c * 32) * kBM + quarter * 32 + lane;
+                if (p.skc > 1) {
+                    // split-K over the cluster: the partial stays in this CTA's shared
+                    // memory ([column][128 rows] FP32 over the ring, whose stages the
+                    // MMAs have finished reading)
+                    if (c == 0) fence_proxy_async_smem();
+                    float* part = reinterpret_cast<float*>(smem) + slot_col;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) part[j * kBM] = __uint_as_float(r[j]);
+                    continue;
+                }
                 if (to_slot) {
                     float* ps = p.sk_part + static_cast<long long>(blockIdx.x) * BN * kBM + slot_col;
 #pragma unroll
@@ -668,6 +689,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
+    }
+
+    if (p.skc > 1) {
+        // Split-K over the cluster.  A CTA whose share of k-blocks is empty holds
+        // a zero partial.  Barrier 1: every CTA's partial is in its shared memory.
+        SegCursor cur = seg_first(p, blockIdx.x, gridDim.x);
+        if (cur.pos >= cur.end && warp >= 2) {
+            float* part = reinterpret_cast<float*>(smem);
+            for (int i = threadIdx.x - 64; i < BN * kBM; i += kEpiWarps * 32) part[i] = 0.f;
+        }
+        cluster_sync();
+        if (warp >= 2) {
+            // Columns [rank * BN/skc, (rank+1) * BN/skc) of the tile, summed over the
+            // cluster's partials in rank order.  Work items are 4 rows of one column
+            // (16 bytes of each partial); a thread takes every 128th item, four items
+            // at a time, and keeps 4 items x 4 partials of loads in flight.
+            const int rank = static_cast<int>(cluster_ctarank());
+            const int cols = BN / p.skc;
+            const int items = cols * (kBM / 4);
+            const int t = threadIdx.x - 64;
+            int pm, pn;
+            tile_coord(static_cast<int>(blockIdx.x) / p.skc, p.num_m, p.num_n, p.group_m, &pm, &pn);
+            const uint32_t part0 = smem_u32(smem);
+            using E = typename std::conditional<OUT == kOutF32, uint32_t, uint16_t>::type;
+            for (int i0 = t; i0 < items; i0 += 4 * kEpiWarps * 32) {
+                float4 acc[4];
+                uint32_t off[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int i = i0 + u * kEpiWarps * 32;
+                    const int col = rank * cols + i / (kBM / 4);
+                    const int row = (i % (kBM / 4)) * 4;
+                    off[u] = static_cast<uint32_t>((col * kBM + row) * 4);
+                }
+                for (int q0 = 0; q0 < p.skc; q0 += 4) {
+                    float4 x[4][4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (i0 + u * kEpiWarps * 32 < items && q0 + q < p.skc)
+                                x[u][q] = ld_shared_cluster_v4(mapa_shared(part0 + off[u], q0 + q));
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (i0 + u * kEpiWarps * 32 < items && q0 + q < p.skc) {
+                                acc[u].x += x[u][q].x;
+                                acc[u].y += x[u][q].y;
+                                acc[u].z += x[u][q].z;
+                                acc[u].w += x[u][q].w;
+                            }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kEpiWarps * 32;
+                    if (i >= items) continue;
+                    const int n = pn * BN + rank * cols + i / (kBM / 4);
+                    const int m_first = pm * kBM + (i % (kBM / 4)) * 4;
+                    const float v4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+                    if (n >= p.N) continue;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = m_first + e;
+                        if (m >= p.M) break;
+                        float v = v4[e];
+                        if constexpr (Ty::kFp8) {
+                            if (p.alpha != 1.0f) v *= p.alpha;
+                        } else {
+                            if (p.bias_mode == 1) v += bias_value<OUT>(p.bias, m);
+                            else if (p.bias_mode == 2) v += bias_value<OUT>(p.bias, n);
+                        }
+                        E* dst = reinterpret_cast<E*>(p.C) + (static_cast<long long>(m) + static_cast<long long>(n) * p.ldc);
+                        if constexpr (OUT == kOutF32) {
+                            *dst = __float_as_uint(v);
+                        } else {
+                            *dst = round_out<OUT>(__float_as_uint(v));
+                        }
+                    }
+                }
+            }
+        }
+        // Barrier 2: no CTA leaves while a peer may still read its shared memory.
+        cluster_sync();
     }
 
     tc_fence_before_sync();
@@ -1129,8 +1235,9 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     using Ty = Types<IN, OUT>;
     // Tile rows: 128, or the balanced height the planner chose (K-major A,
     // whole tiles only).
-    const int bm = (!A_MN && !g.stream_k && g.block_m >= 8 && g.block_m <= kBM && g.block_m % 8 == 0) ? g.block_m
-                                                                                                       : kBM;
+    const int bm = (!A_MN && !g.stream_k && g.skc <= 1 && g.block_m >= 8 && g.block_m <= kBM && g.block_m % 8 == 0)
+                       ? g.block_m
+                       : kBM;
     CUtensorMap tmA, tmB, tmC;
     if (!encode_operands<IN, OUT, A_MN, B_MN>(g, bm, BN, &tmA, &tmB, &tmC, msg, msg_len)) return 1;
 
@@ -1153,6 +1260,7 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
     p.dyn = 0;
+    p.skc = 0;
 
     auto kern = gemm_tcgen05_kernel<BN, A_MN, B_MN, IN, OUT>;
     static SmemOptIn smem_opt;
@@ -1160,6 +1268,67 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 1;
+    }
+    if (g.skc > 1) {
+        // Split-K: one cluster of skc CTAs per tile (no workspace, no flags).
+        int skc = g.skc;
+        p.sk = 0;
+        p.sk_dp_tiles = 0;
+        p.sk_iters = 0;
+        p.sk_part = nullptr;
+        p.sk_flag = nullptr;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cf::kSmemBytes;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // Clusters of this kernel that fit on the device at once, per cluster size
+        // (queried once per device).  A size whose clusters would not all fit in
+        // one wave is halved while that makes them fit: one wave of smaller
+        // clusters finishes before two waves of larger ones (GB300, one CTA per
+        // SM: 76 clusters of 2, 36 of 4, 15 of 8, 7 of 16).
+        static std::atomic<int> fit_cache[SmemOptIn::kMaxDevices][5];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= SmemOptIn::kMaxDevices) dev = -1;
+        auto fits = [&](int size) {
+            int lg = 0;
+            while ((1 << lg) < size) ++lg;
+            int n = dev >= 0 ? fit_cache[dev][lg].load(std::memory_order_acquire) : 0;
+            if (n > 0) return n;
+            if (size > 8 && cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+                cudaGetLastError();
+                return 0;
+            }
+            attr[0].val.clusterDim.x = static_cast<unsigned>(size);
+            cfg.gridDim = dim3(static_cast<unsigned>(size), 1, 1);
+            n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            if (n > 0 && dev >= 0) fit_cache[dev][lg].store(n, std::memory_order_release);
+            return n;
+        };
+        while (skc > 2 && fits(skc) < p.num_tiles) skc /= 2;
+        p.skc = skc;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(skc);
+        cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles) * static_cast<unsigned>(skc), 1, 1);
+        cfg.numAttrs = g.pdl ? 2 : 1;
+        e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "GEMM (split-K, clusters of %d) launch failed: %s", skc, cudaGetErrorString(e));
+            return 1;
+        }
+        return 0;
     }
     int grid = 0;
     p.sk = 0;
@@ -1249,6 +1418,7 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.status = g.status;
     p.wait_limit_ns = g.wait_limit_ns;
     p.dyn = 0;
+    p.skc = 0;
 
     auto kern = gemm_tcgen05_pair_kernel<A_MN, B_MN, IN, OUT>;
     static SmemOptIn smem_opt;

@@ -174,6 +174,18 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     return r;
 }
 
+// 16-byte load from the shared memory of another CTA of the cluster (address
+// from mapa_shared, 16-byte aligned).
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // All threads of all CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync()
 {

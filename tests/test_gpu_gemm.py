@@ -290,8 +290,9 @@ def test_stream_k_on_cta_pairs(M, N, K, sms):
 @pytest.mark.parametrize("M,N,K", [(256, 256, 2048), (128, 128, 16384), (300, 517, 2048), (512, 512, 4096),
                                    (129, 33, 4160)])
 def test_few_tiles_long_k_default_schedule(M, N, K):
-    """Few tiles with a long k loop: the default plan shares each tile's k-blocks
-    between at most four CTAs (stream-K), whose owner adds the others' partials.
+    """Few tiles with a long k loop: the default plan splits each tile's k loop
+    over a cluster of CTAs that add their partials through distributed shared
+    memory.
     Integer inputs give the oracle's bits; random inputs stay within tolerance
     and repeat bit for bit."""
     A, B = operands(M, N, K, "int2")
@@ -302,6 +303,34 @@ def test_few_tiles_long_k_default_schedule(M, N, K):
     assert np.array_equal(run(Ar, Br, M, N, K), got)
     ref, _ = oracle.gemm_f16_colmajor(Ar, Br, M, N, K)
     check_tolerance(got, ref, "f16", K, absmax_f16(Ar), absmax_f16(Br), f"few tiles {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,block_n,skc", [
+    (1000, 777, 1030, 32, 2), (1000, 777, 1030, 64, 4), (1000, 777, 1030, 128, 8), (1000, 777, 1030, 256, 16),
+    (129, 257, 65, 32, 8),        # 2 k-blocks over 8 CTAs: six hold empty (zero) partials
+    (300, 517, 2048, 32, 16), (4095, 40, 4100, 32, 4), (64, 20, 96, 32, 2)])
+def test_split_k_over_clusters(M, N, K, block_n, skc):
+    """Split-K over a cluster of the one-CTA kernel (forced): every CTA leaves its
+    partial in shared memory, the cluster sums each column slice in rank order
+    through distributed shared memory.  Integer inputs give the oracle's bits;
+    random inputs stay within tolerance and repeat bit for bit."""
+    A, B = operands(M, N, K, "int2")
+    Ar, Br = operands(M, N, K, "normal0.5")
+    opts = {"gemm_kernel": 1, "block_n": block_n, "split_k": skc}
+    for k, v in opts.items():
+        bsk.set_option(k, v)
+    try:
+        got = run(A, B, M, N, K)
+        got_r = run(Ar, Br, M, N, K)
+        again = run(Ar, Br, M, N, K)
+    finally:
+        for k in opts:
+            bsk.set_option(k, 0)
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    assert np.array_equal(got, want)
+    assert np.array_equal(got_r, again)
+    ref, _ = oracle.gemm_f16_colmajor(Ar, Br, M, N, K)
+    check_tolerance(got_r, ref, "f16", K, absmax_f16(Ar), absmax_f16(Br), f"split-K {skc} {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("M,N,K", [(1000, 777, 1030), (256, 256, 64), (300, 517, 200), (2304, 2560, 1024),

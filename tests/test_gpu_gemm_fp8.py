@@ -159,21 +159,45 @@ def test_random_inputs_within_tolerance(fmt, out):
     check(got, ref, out, K, absmax(A2, fmt), absmax(B2, fmt), alpha, f"{fmt}->{out}")
 
 
-@pytest.mark.parametrize("kernel,block_n,group_m", [
-    (2, 256, 2), (2, 256, 5), (1, 256, 3), (1, 128, 1), (1, 64, 7), (1, 32, 2)])
-def test_result_independent_of_tile_config(kernel, block_n, group_m):
+@pytest.mark.parametrize("kernel,block_n,group_m,skc", [
+    (2, 256, 2, 0), (2, 256, 5, 0), (1, 256, 3, 0), (1, 128, 1, 0), (1, 64, 7, 0), (1, 32, 2, 0),
+    (1, 32, 2, 4), (1, 256, 1, 16)])
+def test_result_independent_of_tile_config(kernel, block_n, group_m, skc):
     M, N, K = 1000, 777, 1030
     A2, B2 = operands(M, N, K, "int2", "e4m3")
-    bsk.set_option("gemm_kernel", kernel)
-    bsk.set_option("block_n", block_n)
-    bsk.set_option("group_m", group_m)
+    opts = {"gemm_kernel": kernel, "block_n": block_n, "group_m": group_m, "split_k": skc}
+    for k, v in opts.items():
+        bsk.set_option(k, v)
     try:
         got, Af, lda, Bf, ldb = run(A2, B2, "e4m3", "bf16")
     finally:
-        for k in ("gemm_kernel", "block_n", "group_m"):
+        for k in opts:
             bsk.set_option(k, 0)
     _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", "bf16")
     assert np.array_equal(got, bits)
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_split_k_scale_and_outputs(out):
+    """Split-K over clusters (forced) applies alpha once, after the partials are
+    summed: integer codes with alpha 1 give the oracle's bits; random codes
+    with alpha 1/32 stay within tolerance."""
+    M, N, K = 700, 300, 2304
+    opts = {"gemm_kernel": 1, "block_n": 64, "split_k": 8}
+    for k, v in opts.items():
+        bsk.set_option(k, v)
+    try:
+        A2, B2 = operands(M, N, K, "int2", "e4m3")
+        got, Af, lda, Bf, ldb = run(A2, B2, "e4m3", out)
+        _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", out)
+        assert np.array_equal(got, bits)
+        A2, B2 = operands(M, N, K, "normal1", "e4m3")
+        got, Af, lda, Bf, ldb = run(A2, B2, "e4m3", out, 0.03125)
+    finally:
+        for k in opts:
+            bsk.set_option(k, 0)
+    ref, _ = want(Af, lda, Bf, ldb, M, N, K, "e4m3", out, 0.03125)
+    check(got, ref, out, K, absmax(A2, "e4m3"), absmax(B2, "e4m3"), 0.03125, f"split-K e4m3->{out}")
 
 
 @pytest.mark.parametrize("N", [1, 8, 16, 33, 64, 100, 128, 129])

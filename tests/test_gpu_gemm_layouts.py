@@ -269,7 +269,8 @@ def test_ragged_m_with_aligned_ldc_leaves_padding_alone(M, pad_c):
     assert np.array_equal(got, out)
 
 
-@pytest.mark.parametrize("sched", [{"stream_k": 2}, {"stream_k": 2, "gemm_kernel": 1}, {"tile_sched": 2}])
+@pytest.mark.parametrize("sched", [{"stream_k": 2}, {"stream_k": 2, "gemm_kernel": 1}, {"tile_sched": 2},
+                                   {"split_k": 8, "gemm_kernel": 1}, {"split_k": 4, "gemm_kernel": 1, "block_n": 64}])
 @pytest.mark.parametrize("order,transa,transb,mode", [
     (0, 0, 0, 1), (0, 1, 1, 2), (1, 0, 1, 2), (1, 1, 0, 1), (0, 0, 1, 0)])
 def test_schedules_with_layouts_and_bias(sched, order, transa, transb, mode):
