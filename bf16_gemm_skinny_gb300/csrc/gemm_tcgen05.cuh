@@ -90,7 +90,8 @@ struct Cfg {
     static constexpr int kBBytes = BN * kRowBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kEpiBufBytes = kEpiBox * kEpiBox * 2;
-    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int kEpiBufs = 2;   // staging buffers per epilogue warp
+    static constexpr int kEpiBytes = kEpiWarps * kEpiBufs * kEpiBufBytes;
     static constexpr int kTmemCols = 2 * BN;
     static constexpr int kNumBars = 2 * kStages + 5;
     static constexpr int kBarBytes = 256;
@@ -598,8 +599,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Epilogue: TMEM -> registers -> 16-bit -> C
         // ------------------------------------------------------------------
         const int quarter = warp & 3;             // TMEM lanes this warp may read
-        const int ew = warp - 2;                  // owner of a staging buffer pair
-        uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
+        const int ew = warp - 2;                  // owner of kEpiBufs staging buffers
+        uint8_t* ebuf = sEpi + ew * Cf::kEpiBufs * Cf::kEpiBufBytes;
+        // Staging buffers are taken in turn over all of this warp's TMA stores,
+        // tiles included (a 32-wide tile has one store per tile): the buffer of
+        // the store kEpiBufs before is free once at most kEpiBufs - 1 stores are
+        // still reading.
+        int staged = 0;
         SegCursor cur = seg_first(p, blockIdx.x, gridDim.x);
         int tile, kb0, kb1;
         for (int it = 0; seg_next(p, cur, tile, kb0, kb1); ++it) {
@@ -664,8 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              q_last);
                 finish_acc<IN, OUT>(r, p, m0 + lane, n0 + c * 32);
                 if (Ty::kOutBytes == 2 && p.tma_store && whole_quarter) {
-                    uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
-                    if (lane == 0) bulk_wait_group_read<1>();   // the store that used `buf` has read it
+                    uint8_t* buf = ebuf + (staged++ % Cf::kEpiBufs) * Cf::kEpiBufBytes;
+                    if (lane == 0) bulk_wait_group_read<Cf::kEpiBufs - 1>();   // the store that used `buf` has read it
                     __syncwarp();
                     uint16_t* b16 = reinterpret_cast<uint16_t*>(buf);
 #pragma unroll
@@ -1067,6 +1073,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int ew = warp - 2;
         uint8_t* ebuf = sEpi + ew * 2 * Cf::kEpiBufBytes;
+        int staged = 0;   // TMA stores of this warp so far: buffer staged % 2
         SegCursor cur = seg_first(p, pair, num_pairs);
         int tile = 0, kb0 = 0, kb1 = 0;
         for (int it = 0;; ++it) {
@@ -1128,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              q_last);
                 finish_acc<IN, OUT>(r, p, m0 + lane, n0 + c * 32);
                 if (Ty::kOutBytes == 2 && p.tma_store) {
-                    uint8_t* buf = ebuf + (c & 1) * Cf::kEpiBufBytes;
+                    uint8_t* buf = ebuf + (staged++ & 1) * Cf::kEpiBufBytes;
                     if (lane == 0) bulk_wait_group_read<1>();
                     __syncwarp();
                     uint16_t* b16 = reinterpret_cast<uint16_t*>(buf);
