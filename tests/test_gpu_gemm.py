@@ -305,6 +305,24 @@ def test_few_tiles_long_k_default_schedule(M, N, K):
     check_tolerance(got, ref, "f16", K, absmax_f16(Ar), absmax_f16(Br), f"few tiles {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (2048, 2048, 256),     # short k loop on many tiles: one CTA per 128 x 256 tile instead of CTA pairs
+    (2304, 2560, 512),
+    (2048, 2048, 2048),    # 32 k-blocks, all 128 single-CTA tiles in one wave
+    (128, 8192, 2048),     # tile-starved, k loop too short to split: whole 128 x 64 tiles
+    (8192, 128, 2048)])
+def test_planner_regimes(M, N, K):
+    """The default plan in each regime the planner tells apart gives the oracle's
+    bits on integer inputs and stays within tolerance on random ones."""
+    A, B = operands(M, N, K, "int2")
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    assert np.array_equal(run(A, B, M, N, K), want)
+    Ar, Br = operands(M, N, K, "normal0.5")
+    got = run(Ar, Br, M, N, K)
+    ref, _ = oracle.gemm_f16_colmajor(Ar, Br, M, N, K)
+    check_tolerance(got, ref, "f16", K, absmax_f16(Ar), absmax_f16(Br), f"plan {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("M,N,K,block_n,skc", [
     (1000, 777, 1030, 32, 2), (1000, 777, 1030, 64, 4), (1000, 777, 1030, 128, 8), (1000, 777, 1030, 256, 16),
     (129, 257, 65, 32, 8),        # 2 k-blocks over 8 CTAs: six hold empty (zero) partials
