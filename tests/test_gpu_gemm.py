@@ -323,6 +323,32 @@ def test_planner_regimes(M, N, K):
     check_tolerance(got, ref, "f16", K, absmax_f16(Ar), absmax_f16(Br), f"plan {M}x{N}x{K}")
 
 
+def _random_shapes(count, seed, min_work, max_work):
+    """Seeded shapes over every regime of the planner: each of M, N, K drawn
+    log-uniformly from 1..8192 (K up to 16384), half of them rounded to a
+    multiple of 8 (aligned C, TMA stores), with min_work..max_work multiply-adds."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        M, N = (int(np.exp(rng.uniform(0, np.log(8192)))) for _ in range(2))
+        K = int(np.exp(rng.uniform(0, np.log(16384))))
+        if rng.random() < 0.5:
+            M, N, K = (max(8, (v + 7) // 8 * 8) for v in (M, N, K))
+        if min_work <= M * N * K <= max_work:
+            out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", _random_shapes(40, 2026, 1, 6e8) + _random_shapes(20, 2027, 3e8, 4e9))
+def test_random_shapes_default_plan(M, N, K):
+    """Whatever plan the planner picks for a shape (CTA pairs, one-CTA tiles of
+    any width, split-K over clusters, stream-K, the pack for unaligned leading
+    dimensions), integer inputs give the oracle's bits in every element."""
+    A, B = operands(M, N, K, "int2")
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    assert np.array_equal(run(A, B, M, N, K), want), f"{M}x{N}x{K}"
+
+
 @pytest.mark.parametrize("M,N,K,block_n,skc", [
     (1000, 777, 1030, 32, 2), (1000, 777, 1030, 64, 4), (1000, 777, 1030, 128, 8), (1000, 777, 1030, 256, 16),
     (129, 257, 65, 32, 8),        # 2 k-blocks over 8 CTAs: six hold empty (zero) partials
