@@ -333,3 +333,31 @@ def test_pack_every_byte_offset(offset):
     got, Af, lda, Bf, ldb = run(A2, B2, "e4m3", "f32", pad_a=3, pad_b=5, offset=offset)
     _, bits = want(Af, lda, Bf, ldb, M, N, K, "e4m3", "f32")
     assert np.array_equal(got, bits)
+
+
+def _random_cases(count, seed):
+    """Seeded shapes (M, N, K log-uniform in 1..3000, at most 2e8 multiply-adds),
+    formats, output types and paddings."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        M, N, K = (int(np.exp(rng.uniform(0, np.log(3000)))) for _ in range(3))
+        if M * N * K > 2e8:
+            continue
+        fmt = ("e4m3", "e5m2")[int(rng.integers(0, 2))]
+        o = ("f32", "bf16")[int(rng.integers(0, 2))]
+        pads = tuple(int(v) for v in rng.choice([0, 0, 1, 16, 5], 3))
+        out.append((M, N, K, fmt, o, pads))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,fmt,out,pads", _random_cases(30, 88))
+def test_random_shapes_default_plan(M, N, K, fmt, out, pads):
+    """Random shapes, formats, output types and leading dimensions through the
+    default plan (the pack for unaligned ones): integer codes give the oracle's
+    bits, and no padding of C is written."""
+    A, B = inputs.fp8_operands(M, N, K, "int2", fmt, M + 3, N + 9)
+    A2, B2 = A.reshape(M, K), B.reshape(N, K)
+    got, Af, lda, Bf, ldb = run(A2, B2, fmt, out, pad_a=pads[0], pad_b=pads[1], pad_c=pads[2])
+    _, bits = want(Af, lda, Bf, ldb, M, N, K, fmt, out)
+    assert np.array_equal(got, bits), f"{int((got != bits).sum())} of {got.size} entries differ"

@@ -294,3 +294,34 @@ def test_schedules_with_layouts_and_bias(sched, order, transa, transb, mode):
             bsk.set_option(k, 0)
     _, out = want(order, transa, transb, Af, lda, Bf, ldb, M, N, K, bias=bias, mode=mode)
     assert np.array_equal(got, out), f"{int((got != out).sum())} of {got.size} entries differ"
+
+
+def _random_cases(count, seed):
+    """Seeded shapes, storage forms, paddings and bias modes, M, N, K log-uniform
+    in 1..3000 with at most 2e8 multiply-adds."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        M, N, K = (int(np.exp(rng.uniform(0, np.log(3000)))) for _ in range(3))
+        if M * N * K > 2e8:
+            continue
+        order, transa, transb = (int(v) for v in rng.integers(0, 2, 3))
+        pads = tuple(int(v) for v in rng.choice([0, 0, 1, 3, 8], 3))
+        out.append((M, N, K, order, transa, transb, pads, int(rng.integers(0, 3))))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,order,transa,transb,pads,mode", _random_cases(40, 77))
+def test_random_layouts_default_plan(M, N, K, order, transa, transb, pads, mode):
+    """Random shapes in every storage form, with padded leading dimensions and
+    each bias mode, through the default plan: integer inputs and bias give the
+    oracle's bits, and no padding of C is written."""
+    A2, B2 = operands(M, N, K, "int2", seeds=(M + 5, N + 7))
+    bias = None
+    if mode:
+        vals = np.random.default_rng(K).integers(-40, 41, max(M, N))
+        bias = enc(vals)[:M if mode == 1 else N]
+    got, Af, lda, Bf, ldb = run(order, transa, transb, A2, B2, pad_a=pads[0], pad_b=pads[1], pad_c=pads[2],
+                                bias=bias, mode=mode)
+    _, out = want(order, transa, transb, Af, lda, Bf, ldb, M, N, K, bias=bias, mode=mode)
+    assert np.array_equal(got, out), f"{int((got != out).sum())} of {got.size} entries differ"
