@@ -251,20 +251,20 @@ GemmOp colmajor_op(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int
     return op;
 }
 
-// Runs the tcgen05 GEMM on operands in any layout TMA may not take directly:
-// an operand whose base is not 16-byte aligned or whose leading dimension is
-// not a multiple of 16 bytes is packed into a stream-ordered workspace (or
-// into `fixed`, when given).
-int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch* fixed = nullptr)
-{
-    const PackPlan pp = plan_pack(op);
-    const bool fp8 = op.in_type == bsk::kInE4M3 || op.in_type == bsk::kInE5M2;
-    const int eb = pp.eb;
-    const int a_inner = pp.a_inner, a_outer = pp.a_outer, b_inner = pp.b_inner, b_outer = pp.b_outer;
-    const bool a_ok = pp.a_ok, b_ok = pp.b_ok;
-    const long long lda_p = pp.lda_p, ldb_p = pp.ldb_p;
-    const size_t a_bytes = pp.a_bytes, b_bytes = pp.b_bytes;
+// The kernel, tile and schedule of one GEMM.  Every choice below was measured on
+// GB300; the comments give the figures.
+struct GemmPlan {
+    int block_n = 256;      // tile width: 32, 64, 128 or 256
+    int block_m = 128;      // one-CTA kernel, K-major A, one tile column: rows per tile
+    bool pair = true;       // CTA-pair kernel (256 x 256 tiles over two SMs)
+    bool stream_k = false;  // one-CTA kernel: stream-K schedule (workspace partials)
+    int skc = 0;            // one-CTA kernel: split-K over clusters of skc CTAs
+    bool dyn = false;       // CTA pairs: dynamic tile order
+};
 
+GemmPlan plan_gemm(const GemmOp& op, int sms)
+{
+    const bool fp8 = op.in_type == bsk::kInE4M3 || op.in_type == bsk::kInE5M2;
     // Tile width: the smallest of 32 / 64 / 128 covering a skinny N (one CTA per
     // tile, deep ring: the weight stream sets the pace), else 256 on CTA pairs.
     // An MN-major B is staged in 64-column swizzle atoms: at least 64 wide.
@@ -406,6 +406,33 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     const long long bm_opt = opt_or(BSK_OPT_BLOCK_M, 0);
     if (!pair && !stream_k && !op.a_mn_major && (op.N + block_n - 1LL) / block_n == 1 && bm_opt > 0)
         block_m = static_cast<int>(bm_opt);
+    GemmPlan plan;
+    plan.block_n = block_n;
+    plan.block_m = block_m;
+    plan.pair = pair;
+    plan.stream_k = stream_k;
+    plan.skc = skc;
+    plan.dyn = dyn;
+    return plan;
+}
+
+// Runs the tcgen05 GEMM on operands in any layout TMA may not take directly:
+// an operand whose base is not 16-byte aligned or whose leading dimension is
+// not a multiple of 16 bytes is packed into a stream-ordered workspace (or
+// into `fixed`, when given).
+int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch* fixed = nullptr)
+{
+    const PackPlan pp = plan_pack(op);
+    const int eb = pp.eb;
+    const int a_inner = pp.a_inner, a_outer = pp.a_outer, b_inner = pp.b_inner, b_outer = pp.b_outer;
+    const bool a_ok = pp.a_ok, b_ok = pp.b_ok;
+    const long long lda_p = pp.lda_p, ldb_p = pp.ldb_p;
+    const size_t a_bytes = pp.a_bytes, b_bytes = pp.b_bytes;
+
+    const GemmPlan plan = plan_gemm(op, sms);
+    const int block_n = plan.block_n;
+    const bool stream_k = plan.stream_k;
+
     // one slot per CTA: block_n x 128 FP32 (CTA pairs: each CTA's 128 rows of a 256-wide tile)
     const size_t sk_part_bytes = stream_k ? static_cast<size_t>(sms) * block_n * 128 * sizeof(float) : 0;
     const size_t sk_flag_bytes = stream_k ? static_cast<size_t>(sms) * sizeof(int) : 0;
@@ -476,13 +503,13 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     g.alpha = op.alpha;
     g.bias = op.bias_mode != 0 ? op.bias : nullptr;
     g.bias_mode = op.bias_mode;
-    g.block_n = block_n;
-    g.block_m = block_m;
-    g.pair = pair;
-    g.stream_k = stream_k;
+    g.block_n = plan.block_n;
+    g.block_m = plan.block_m;
+    g.pair = plan.pair;
+    g.stream_k = plan.stream_k;
     g.sk_part = sk_part;
     g.sk_flag = sk_flag;
-    g.skc = skc;
+    g.skc = plan.skc;
     // Tile-row group ("Hygon 优化", section 分组调度).  CTA pairs: 8.  Measured on
     // GB300 on 8192^2 x 16384, one launch (cold L2): DRAM reads 4.54 / 4.35 /
     // 2.34 / 3.46 GB for GROUP_M 2 / 4 / 8 / 16, 1.235 / 1.238 / 1.169 / 1.204
@@ -500,7 +527,7 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     g.status = fixed != nullptr ? fixed->status : g_status_dev;
     g.wait_limit_ns = static_cast<unsigned long long>(opt_or(BSK_OPT_WAIT_LIMIT_US, kDefaultWaitLimitUs)) * 1000ull;
     g.pdl = opt_or(BSK_OPT_PDL, 0) != 1;
-    g.dyn = dyn;
+    g.dyn = plan.dyn;
     if (bsk::launch_gemm(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
     return BSK_OK;
 }
