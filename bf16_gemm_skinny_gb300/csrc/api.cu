@@ -355,14 +355,14 @@ GemmPlan plan_gemm(const GemmOp& op, int sms)
     // tile-starved problem the plan with the least estimated time wins, from a
     // model fitted to calls back to back on GB300: one CTA streams (128 + BN)
     // 128-byte operand rows per k-block at about 80 GB/s (1.6 ns a row); a
-    // whole-tile launch costs about 4.3 us beyond that, a split one 5.6 us plus
+    // whole-tile launch costs about 4.3 us beyond that, a split one 5.0 us plus
     // 31 ns per column of its tile (the partial, the barriers, the sums) and
     // 0.5 us more for clusters of 16.  The largest cluster whose tiles all fit
     // on the device at once is taken for each width.  Measured (us, plan
-    // chosen / best measured / whole tiles or stream-K): 128 x 128 x 16384
-    // 11.8 / 11.8 / 31.0, 128 x 512 x 16384 15.6 / 15.6 / 39.3, 256 x 1024 x
-    // 8192 16.9 / 16.9 / 29.3, 1024 x 256 x 4096 12.3 / 12.3 / 24.0, 128 x 512
-    // x 2048 8.6 / 8.6 / 12.5; 128 x 8192 x 2048 stays on whole tiles (13.4).
+    // chosen / whole tiles or stream-K): 128 x 128 x 16384 10.6 / 31.0, 128 x
+    // 512 x 16384 13.1 / 39.3, 256 x 1024 x 8192 16.9 / 29.3, 1024 x 256 x 4096
+    // 11.8 / 24.0, 128 x 512 x 2048 8.1 / 12.5; 128 x 8192 x 2048 stays on
+    // whole tiles (13.4; the best split 15.1).
     int skc = 0;
     const long long skc_opt = opt_or(BSK_OPT_SPLIT_K, 0);
     if (!pair && skc_opt >= 2) {
@@ -377,7 +377,7 @@ GemmPlan plan_gemm(const GemmOp& op, int sms)
                 const long long tiles = m_tiles * ((op.N + bn - 1LL) / bn);
                 for (int sz = 16; sz >= 2; sz /= 2) {
                     if (kbs / sz < 2 || tiles > bsk::split_k_capacity(sz)) continue;
-                    const long long est = 5600 + 31LL * bn + (sz == 16 ? 500 : 0) + (kbs + sz - 1) / sz * row_ns(bn);
+                    const long long est = 5000 + 31LL * bn + (sz == 16 ? 500 : 0) + (kbs + sz - 1) / sz * row_ns(bn);
                     if (best < 0 || est < best) {
                         best = est;
                         block_n = bn;

@@ -709,8 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp >= 2) {
             // Columns [rank * BN/skc, (rank+1) * BN/skc) of the tile, summed over the
             // cluster's partials in rank order.  Work items are 4 rows of one column
-            // (16 bytes of each partial); a thread takes every 128th item, four items
-            // at a time, and keeps 4 items x 4 partials of loads in flight.
+            // (16 bytes of each partial); a thread takes every 128th item and keeps 16
+            // loads in flight: 4 items x 4 partials at a time in clusters of 2 or 4,
+            // one item x all partials in clusters of 8 or 16 (fewer items, more
+            // partials each).
             const int rank = static_cast<int>(cluster_ctarank());
             const int cols = BN / p.skc;
             const int items = cols * (kBM / 4);
@@ -719,61 +721,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coord(static_cast<int>(blockIdx.x) / p.skc, p.num_m, p.num_n, p.group_m, &pm, &pn);
             const uint32_t part0 = smem_u32(smem);
             using E = typename std::conditional<OUT == kOutF32, uint32_t, uint16_t>::type;
-            for (int i0 = t; i0 < items; i0 += 4 * kEpiWarps * 32) {
-                float4 acc[4];
-                uint32_t off[4];
+            auto offset = [&](int i) {
+                return static_cast<uint32_t>(((rank * cols + i / (kBM / 4)) * kBM + (i % (kBM / 4)) * 4) * 4);
+            };
+            auto add4 = [](float4& a, const float4& x) {
+                a.x += x.x;
+                a.y += x.y;
+                a.z += x.z;
+                a.w += x.w;
+            };
+            // bias or FP8 scale, one rounding, and the four rows' stores of item i
+            auto emit = [&](int i, const float4& acc) {
+                const int n = pn * BN + rank * cols + i / (kBM / 4);
+                const int m_first = pm * kBM + (i % (kBM / 4)) * 4;
+                const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+                if (n >= p.N) return;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const int i = i0 + u * kEpiWarps * 32;
-                    const int col = rank * cols + i / (kBM / 4);
-                    const int row = (i % (kBM / 4)) * 4;
-                    off[u] = static_cast<uint32_t>((col * kBM + row) * 4);
+                for (int e = 0; e < 4; ++e) {
+                    const int m = m_first + e;
+                    if (m >= p.M) break;
+                    float v = v4[e];
+                    if constexpr (Ty::kFp8) {
+                        if (p.alpha != 1.0f) v *= p.alpha;
+                    } else {
+                        if (p.bias_mode == 1) v += bias_value<OUT>(p.bias, m);
+                        else if (p.bias_mode == 2) v += bias_value<OUT>(p.bias, n);
+                    }
+                    E* dst = reinterpret_cast<E*>(p.C) + (static_cast<long long>(m) + static_cast<long long>(n) * p.ldc);
+                    if constexpr (OUT == kOutF32) {
+                        *dst = __float_as_uint(v);
+                    } else {
+                        *dst = round_out<OUT>(__float_as_uint(v));
+                    }
                 }
-                for (int q0 = 0; q0 < p.skc; q0 += 4) {
+            };
+            if (p.skc >= 8) {
+                for (int i = t; i < items; i += kEpiWarps * 32) {
+                    const uint32_t off = offset(i);
+                    float4 x[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (q < p.skc) x[q] = ld_shared_cluster_v4(mapa_shared(part0 + off, q));
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (q < p.skc) add4(acc, x[q]);
+                    emit(i, acc);
+                }
+            } else {
+                for (int i0 = t; i0 < items; i0 += 4 * kEpiWarps * 32) {
+                    float4 acc[4];
+                    uint32_t off[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        off[u] = offset(i0 + u * kEpiWarps * 32);
+                    }
                     float4 x[4][4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            if (i0 + u * kEpiWarps * 32 < items && q0 + q < p.skc)
-                                x[u][q] = ld_shared_cluster_v4(mapa_shared(part0 + off[u], q0 + q));
+                            if (i0 + u * kEpiWarps * 32 < items && q < p.skc)
+                                x[u][q] = ld_shared_cluster_v4(mapa_shared(part0 + off[u], q));
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < 4; ++u) {
+                        if (i0 + u * kEpiWarps * 32 >= items) continue;
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            if (i0 + u * kEpiWarps * 32 < items && q0 + q < p.skc) {
-                                acc[u].x += x[u][q].x;
-                                acc[u].y += x[u][q].y;
-                                acc[u].z += x[u][q].z;
-                                acc[u].w += x[u][q].w;
-                            }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = i0 + u * kEpiWarps * 32;
-                    if (i >= items) continue;
-                    const int n = pn * BN + rank * cols + i / (kBM / 4);
-                    const int m_first = pm * kBM + (i % (kBM / 4)) * 4;
-                    const float v4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
-                    if (n >= p.N) continue;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int m = m_first + e;
-                        if (m >= p.M) break;
-                        float v = v4[e];
-                        if constexpr (Ty::kFp8) {
-                            if (p.alpha != 1.0f) v *= p.alpha;
-                        } else {
-                            if (p.bias_mode == 1) v += bias_value<OUT>(p.bias, m);
-                            else if (p.bias_mode == 2) v += bias_value<OUT>(p.bias, n);
-                        }
-                        E* dst = reinterpret_cast<E*>(p.C) + (static_cast<long long>(m) + static_cast<long long>(n) * p.ldc);
-                        if constexpr (OUT == kOutF32) {
-                            *dst = __float_as_uint(v);
-                        } else {
-                            *dst = round_out<OUT>(__float_as_uint(v));
-                        }
+                            if (q < p.skc) add4(acc[u], x[u][q]);
+                        emit(i0 + u * kEpiWarps * 32, acc[u]);
                     }
                 }
             }
