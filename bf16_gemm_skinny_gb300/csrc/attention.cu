@@ -207,6 +207,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
 
     __shared__ float s_m[kAttnWarps][G];
     __shared__ float s_l[kAttnWarps][G];
+    __shared__ float s_f[kAttnWarps][G];   // combine: each warp's weight per head
+    __shared__ float s_hm[G], s_hl[G];      // combine: each head's max and sum
     // weights of the chunk and rescale factors, each stored twice ({w, w}): the
     // packed FMAs of the output update take them as pairs straight from memory
     __shared__ __align__(16) float2 s_p[kAttnWarps][T][G];
@@ -417,12 +419,36 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
         s_l[warp][gq] = l_h;
     }
 #pragma unroll
-    for (int j = 0; j < G; ++j)
+    for (int j = 0; j < G; ++j) {
+        // this lane's EPL consecutive values of head j, in 16-byte (or 8-byte) stores
+        float* dst = s_o + (warp * G + j) * HD + lane * EPL;
+        if constexpr (EPL % 4 == 0) {
 #pragma unroll
-        for (int e = 0; e < P; ++e) {
-            s_o[(warp * G + j) * HD + lane * EPL + 2 * e] = o[j][e].x;
-            s_o[(warp * G + j) * HD + lane * EPL + 2 * e + 1] = o[j][e].y;
+            for (int e = 0; e < P; e += 2)
+                *reinterpret_cast<float4*>(dst + 2 * e) = make_float4(o[j][e].x, o[j][e].y, o[j][e + 1].x, o[j][e + 1].y);
+        } else {
+#pragma unroll
+            for (int e = 0; e < P; ++e) *reinterpret_cast<float2*>(dst + 2 * e) = o[j][e];
         }
+    }
+    __syncthreads();
+    // per head: M = max_w m_w, the warps' weights 2^(m_w - M) and L = sum_w w l_w,
+    // once (G threads), for the CTA's outputs below
+    if (threadIdx.x < G) {
+        const int j = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][j]);
+        float Lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+            const float f = M == -INFINITY ? 0.f : exp2f(s_m[w][j] - M);
+            s_f[w][j] = f;
+            Lsum = fmaf(f, s_l[w][j], Lsum);
+        }
+        s_hm[j] = M;
+        s_hl[j] = Lsum;
+    }
     __syncthreads();
 
     float* out = p.partial +
@@ -431,23 +457,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
     for (int i = threadIdx.x; i < G * HD; i += blockDim.x) {
         const int j = i / HD;
         const int e = i - j * HD;
-        float M = -INFINITY;
+        float O = 0.f;
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][j]);
-        float O = 0.f, Lsum = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) {
-                const float f = exp2f(s_m[w][j] - M);
-                O = fmaf(f, s_o[(w * G + j) * HD + e], O);
-                Lsum = fmaf(f, s_l[w][j], Lsum);
-            }
-        }
+        for (int w = 0; w < kAttnWarps; ++w) O = fmaf(s_f[w][j], s_o[(w * G + j) * HD + e], O);
         float* dst = out + j * head_stride;
         dst[2 + e] = O;
         if (e == 0) {
-            dst[0] = M;
-            dst[1] = Lsum;
+            dst[0] = s_hm[j];
+            dst[1] = s_hl[j];
         }
     }
 }
