@@ -1,7 +1,7 @@
 """Seeded fuzz through the default plans: hundreds of random problems (the
 FP16 column-major GEMM, gemm_f16 in every storage form with each bias mode,
-and the FP8 GEMM in both formats and outputs), integer-valued inputs, every
-element compared with the oracle bit for bit.  Shapes are drawn log-uniform
+the FP8 GEMM in both formats and outputs, and gemv_bf16 for 1..160 tokens),
+integer-valued inputs, every element compared with the oracle bit for bit.  Shapes are drawn log-uniform
 (M, N up to 8192, K up to 16384, half of them rounded to multiples of 8), so
 most are small and odd: the unaligned pack, ragged tails, every tile width,
 split-K over clusters and the CTA-pair kernel all come up."""
@@ -91,6 +91,36 @@ def _layout(rng, M, N, K):
     got = C.cpu().numpy().view(np.uint16)
     got = got.reshape(M, N) if order else got.reshape(N, M).T
     return np.array_equal(got, np.asarray(want).reshape(N, M).T)
+
+
+def _gemv(rng):
+    """y = x W^T through gemv_bf16 (CUDA cores for n <= 3, the tensor-core GEMM
+    beyond), M up to 40000, K up to 8192, n up to 160 tokens."""
+    import torch
+
+    while True:
+        M = int(np.exp(rng.uniform(0, np.log(40000))))
+        K = int(np.exp(rng.uniform(0, np.log(8192))))
+        n = int(np.exp(rng.uniform(0, np.log(160))))
+        if M * K * n <= MAX_WORK:
+            break
+    W, x = inputs.linear_operands(M, K, n, "int2", "int2", int(rng.integers(1, 1000)), int(rng.integers(1, 1000)))
+    y = torch.empty(n * M, dtype=torch.int16, device="cuda")
+    bsk.gemv_bf16(torch.from_numpy(W.view(np.int16)).cuda(), torch.from_numpy(x.view(np.int16)).cuda(), y, M, K, n)
+    _, want = oracle.linear_bf16(W, x, M, K, n)
+    return np.array_equal(y.cpu().numpy().view(np.uint16), want.reshape(-1)), (M, K, n)
+
+
+@pytest.mark.parametrize("seed", [303])
+def test_fuzz_gemv(seed):
+    rng = np.random.default_rng(seed)
+    fails = []
+    for _ in range(150):
+        ok, shape = _gemv(rng)
+        if not ok:
+            fails.append(shape)
+    bsk.stream_check()
+    assert not fails, f"{len(fails)} problems differ from the oracle, e.g. {fails[:5]}"
 
 
 @pytest.mark.parametrize("seed", [101, 202])
