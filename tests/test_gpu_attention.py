@@ -155,3 +155,38 @@ def test_out_of_range_block_is_reported_not_read():
     assert exc.value.status == 1
     # the library keeps working
     test_batch_with_empty_sequence_and_determinism()
+
+
+def _random_configs(count, seed):
+    """Seeded attention problems: head_dim, query heads per KV head, page size,
+    batch, per-sequence lengths (some empty) and segment counts at random."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        hd = int(rng.choice([64, 128, 256]))
+        group = int(rng.choice([1, 2, 4, 8]))
+        nkv = int(rng.choice([1, 2, 4]))
+        bs = int(rng.choice([8, 16, 31, 64, 784]))
+        num_seqs = int(rng.integers(1, 4))
+        lens = [int(v) for v in np.exp(rng.uniform(0, np.log(6000), num_seqs)).astype(int)]
+        if rng.random() < 0.2:
+            lens[0] = 0
+        segs = int(rng.choice([0, 0, 1, 5, 16, 32, 100]))
+        out.append((hd, group * nkv, nkv, bs, lens, segs, int(rng.integers(0, 1 << 20))))
+    return out
+
+
+@pytest.mark.parametrize("hd,nqh,nkv,bs,lens,segs,seed", _random_configs(24, 1234))
+def test_random_configurations(hd, nqh, nkv, bs, lens, segs, seed):
+    """Random head shapes, page sizes, batches with uneven (and empty) sequences
+    and segment counts: within the derived tolerance of the oracle, empty
+    sequences give zeros."""
+    q, k, v, bt, sl, nb, mb = make_problem(seed, len(lens), lens, nqh, nkv, hd, bs)
+    scale = 1.0 / math.sqrt(hd)
+    got = run(q, k, v, bt, sl, nqh, nkv, hd, bs, nb, mb, scale, segs)
+    ref, _ = oracle.decode_attention_bf16(q, k.reshape(nb, bs, nkv, hd), v.reshape(nb, bs, nkv, hd), bt, sl,
+                                          nqh, nkv, hd, bs, scale)
+    for s, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[s] == 0)
+    check(got, ref, q, k, v, hd, scale, max(max(lens), 1), f"hd={hd} {nqh}/{nkv} bs={bs} lens={lens} segs={segs}")
