@@ -43,6 +43,7 @@ OPTIONS = {
     "tile_sched": 13,
     "block_m": 14,
     "split_k": 15,
+    "prefetch_kb": 16,
 }
 
 # Every symbol include/bsk.h (the C ABI) declares.

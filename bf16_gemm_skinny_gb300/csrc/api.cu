@@ -46,7 +46,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 16;
+constexpr int kNumOpts = 17;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -528,6 +528,16 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     g.wait_limit_ns = static_cast<unsigned long long>(opt_or(BSK_OPT_WAIT_LIMIT_US, kDefaultWaitLimitUs)) * 1000ull;
     g.pdl = opt_or(BSK_OPT_PDL, 0) != 1;
     g.dyn = plan.dyn;
+    // One-CTA kernel with a K-major A (the skinny decode weight): while a launch
+    // waits for the kernel before it, its epilogue warps prefetch 16 more
+    // k-blocks of their first tile's rows into L2, using the DRAM bandwidth the
+    // earlier kernel's last CTAs leave idle.  34816 x 5120 on GB300, per launch
+    // (off / 4 / 8 / 16 / 32 k-blocks), chains of 24 back to back: n = 4 57.3-57.8
+    // / 57.4-57.5 / 57.0-57.3 / 56.7 / 56.5-56.8 us, n = 8 57.7-58.2 / 57.7-57.9 /
+    // 57.2-57.4 / 56.3-56.5 / 57.0; one launch after a GEMM: the same within 1 us
+    // up to 16, 1-2 us slower at 32 (the prefetches then delay the first loads).
+    const long long pf_opt = opt_or(BSK_OPT_PREFETCH_KB, 0);
+    g.prefetch_kb = static_cast<int>(pf_opt == 0 ? 16 : pf_opt == 1 ? 0 : pf_opt);
     if (bsk::launch_gemm(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
     return BSK_OK;
 }
@@ -1221,6 +1231,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_TILE_SCHED: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_BLOCK_M: ok = value >= 0 && value <= 128 && value % 8 == 0; break;
     case BSK_OPT_SPLIT_K: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16; break;
+    case BSK_OPT_PREFETCH_KB: ok = value >= 0 && value <= 64; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

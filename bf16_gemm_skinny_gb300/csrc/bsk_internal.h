@@ -139,6 +139,8 @@ struct GemmLaunch {
     bool dyn = false;        // CTA pairs, whole tiles: dynamic tile order (one cluster per tile launched)
     int skc = 0;             // one-CTA kernel: split-K over clusters of skc CTAs (2..16, a power of two
                              // dividing block_n); 0 = off
+    int prefetch_kb = 0;     // one-CTA kernel, K-major A, whole tiles: extra k-blocks of the first
+                             // tile's rows prefetched into L2 in the prologue
 };
 
 // Returns 0 on success; otherwise an error message is written to `msg`.

@@ -70,6 +70,11 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_SPLIT_K          split-K over a cluster of the one-CTA GEMM kernel: 0 automatic
  *                            (tile-starved problems), 1 off, 2 / 4 / 8 / 16 force that cluster
  *                            size (one-CTA kernel, whole tiles; 16 needs a non-portable cluster)
+ *   BSK_OPT_PREFETCH_KB      one-CTA GEMM kernel with a K-major A (the skinny decode shapes):
+ *                            k-blocks of the first tile's A rows that the epilogue warps
+ *                            prefetch into L2 while the launch waits for the kernel before
+ *                            it, beyond the two stages the producer prefetches: 0 automatic
+ *                            (16), 1 none, 2..64 that many
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
@@ -87,7 +92,8 @@ enum {
     BSK_OPT_PDL = 12,
     BSK_OPT_TILE_SCHED = 13,
     BSK_OPT_BLOCK_M = 14,
-    BSK_OPT_SPLIT_K = 15
+    BSK_OPT_SPLIT_K = 15,
+    BSK_OPT_PREFETCH_KB = 16
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);

@@ -138,6 +138,11 @@ struct Params {
     // cluster barrier sums columns [r*BN/skc, (r+1)*BN/skc) of the tile over
     // all skc partials (in rank order) and stores them.
     int skc;
+    // One-CTA kernel, K-major A, whole tiles: the epilogue warps prefetch k-blocks
+    // [2, 2 + pf_kb) of their first tile's A rows into L2 before the dependency wait.
+    const uint8_t* a_rows;  // A's first row
+    long long a_ld_bytes;   // bytes between A's rows
+    int pf_kb;
 };
 
 // The work of one unit (a CTA, or a CTA pair) of `units` as a sequence of
@@ -469,6 +474,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    if constexpr (!A_MN) {
+        // K-major A (the skinny decode weight): the epilogue warps, idle until the
+        // first accumulator, prefetch the next pf_kb k-blocks of their first
+        // tile's rows into L2 -- one 128-byte line per row and k-block, by the
+        // load units, so the TMA unit's queue stays free for the real loads.
+        // Like the producer's prefetch above this reads nothing into the SM.
+        if (warp >= 2 && p.pf_kb > 0 && p.sk == 0 && p.skc <= 1 && static_cast<int>(blockIdx.x) < p.num_tiles) {
+            int pm, pn;
+            tile_coord(static_cast<int>(blockIdx.x), p.num_m, p.num_n, p.group_m, &pm, &pn);
+            const int row = pm * p.bm + (static_cast<int>(threadIdx.x) - 64);
+            constexpr int kFirst = S < 2 ? S : 2;
+            const int kb_end = p.num_kb < kFirst + p.pf_kb ? p.num_kb : kFirst + p.pf_kb;
+            if (row < p.M && row < (pm + 1) * p.bm) {
+                const uint8_t* r = p.a_rows + static_cast<long long>(row) * p.a_ld_bytes;
+                for (int kb = kFirst; kb < kb_end; ++kb) prefetch_l2(r + static_cast<long long>(kb) * kRowBytes);
+            }
+        }
+    }
     // The prologue touched only shared memory, TMEM and the parameters; global
     // memory is read and written only once the kernel before this one in the
     // stream has completed (a no-op unless launched as its dependent).
@@ -1285,6 +1308,9 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     p.wait_limit_ns = g.wait_limit_ns;
     p.dyn = 0;
     p.skc = 0;
+    p.a_rows = static_cast<const uint8_t*>(g.A);
+    p.a_ld_bytes = g.lda * Ty::kElemBytes;
+    p.pf_kb = A_MN ? 0 : g.prefetch_kb;
 
     auto kern = gemm_tcgen05_kernel<BN, A_MN, B_MN, IN, OUT>;
     static SmemOptIn smem_opt;
@@ -1443,6 +1469,9 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.wait_limit_ns = g.wait_limit_ns;
     p.dyn = 0;
     p.skc = 0;
+    p.a_rows = nullptr;
+    p.a_ld_bytes = 0;
+    p.pf_kb = 0;
 
     auto kern = gemm_tcgen05_pair_kernel<A_MN, B_MN, IN, OUT>;
     static SmemOptIn smem_opt;

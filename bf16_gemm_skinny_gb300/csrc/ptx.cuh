@@ -208,6 +208,12 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)
 
 // Prefetch of the box at (x, y) into L2 (no shared memory, no completion signal;
 // coherent with any writes that reach L2 later).
+// A hint: brings the 128-byte line holding `addr` into L2; delivers nothing.
+__device__ __forceinline__ void prefetch_l2(const void* addr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y)
 {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

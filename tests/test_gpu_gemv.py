@@ -216,6 +216,25 @@ def test_skinny_tile_heights(block_m, M, K, n):
         bsk.set_option("gemv_kernel", 0)
 
 
+@pytest.mark.parametrize("prefetch_kb", [1, 2, 64])
+@pytest.mark.parametrize("M,K,n,offset,block_m", [(34816, 5120, 4, 0, 0), (1003, 1032, 8, 1, 0), (4095, 200, 16, 0, 0),
+                                                  (777, 2048, 100, 0, 0), (4095, 1032, 8, 0, 40)])
+def test_skinny_prologue_prefetch_depths(prefetch_kb, M, K, n, offset, block_m):
+    """The L2 prefetch of the first tile's weight rows in the prologue is a hint:
+    none, the shortest and the deepest setting -- on the decode shape, a packed
+    (unaligned) W, a k loop shorter than the prefetch, a ragged M and a forced
+    tile height -- give the oracle's bits on integer inputs."""
+    bsk.set_option("prefetch_kb", prefetch_kb)
+    bsk.set_option("block_m", block_m)
+    try:
+        W, x = operands(M, K, n, True)
+        _, want = oracle.linear_bf16(W, x, M, K, n)
+        assert np.array_equal(run(W, x, M, K, n, offset), want)
+    finally:
+        bsk.set_option("prefetch_kb", 0)
+        bsk.set_option("block_m", 0)
+
+
 def test_k_zero_and_empty():
     got = run(np.zeros(0, np.uint16), np.zeros(0, np.uint16), 50, 0, 3)
     assert np.all(got == 0)

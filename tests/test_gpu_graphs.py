@@ -3,7 +3,9 @@
 One graph captures every kind of launch the library makes: the CTA-pair GEMM
 (with programmatic dependent launch), the GEMM on unaligned operands (pack
 kernels into a stream-ordered workspace), stream-K (flag reset + cooperative
-launch), the dynamic tile order (cluster launch control), the CUDA-core GEMV,
+launch), split-K over a thread-block cluster (clusters of 2 to 16, the largest
+with the non-portable size attribute), the dynamic tile order (cluster launch
+control), the CUDA-core GEMV,
 the tensor-core skinny GEMM, the FP8 GEMM and split-KV decode attention
 (workspace + the merge kernel as a programmatic dependent).  The graph is
 replayed on new input contents, written in place between replays: every
@@ -43,6 +45,7 @@ class Problem:
     RAGGED = (300, 517, 200)       # unaligned leading dimensions: pack path
     SK = (1000, 777, 1030)         # stream-K forced
     DYN = (1000, 777, 1030)        # dynamic tile order forced
+    SPLITK = (128, 128, 4096)      # one tile, 64 k-blocks: split-K over a cluster (automatic, and 16 forced)
     GEMV = (1000, 1024)            # M, K; n = 1 (CUDA cores) and n = 8 (tensor cores)
     FP8 = (256, 160, 384)
     ATTN = dict(nqh=16, nkv=4, hd=256, bs=784, L=1500)
@@ -60,6 +63,10 @@ class Problem:
         self.sA, self.sB = self._pair(M * K, N * K)
         self.sC = torch.zeros(M * N, dtype=torch.int16, device="cuda")
         self.dC = torch.zeros(M * N, dtype=torch.int16, device="cuda")
+        M, N, K = self.SPLITK
+        self.kA, self.kB = self._pair(M * K, N * K)
+        self.kC = torch.zeros(M * N, dtype=torch.int16, device="cuda")
+        self.k16C = torch.zeros(M * N, dtype=torch.int16, device="cuda")
         M, K = self.GEMV
         self.W = torch.zeros(M * K, dtype=torch.int16, device="cuda")
         self.x1 = torch.zeros(K, dtype=torch.int16, device="cuda")
@@ -96,7 +103,7 @@ class Problem:
                                                                      else np.uint8)))
 
         for (M, N, K), A, B, s in ((self.GEMM, self.gA, self.gB, 0), (self.RAGGED, self.rA, self.rB, 2),
-                                   (self.SK, self.sA, self.sB, 4)):
+                                   (self.SK, self.sA, self.sB, 4), (self.SPLITK, self.kA, self.kB, 13)):
             a, b = inputs.gemm_operands(M, N, K, "int2", seed + s, seed + s + 1)
             put(A, a)
             put(B, b)
@@ -132,6 +139,13 @@ class Problem:
             bsk.gemm_f16_colmajor_enqueue(self.sA, self.sB, self.dC, M, N, K)
         finally:
             bsk.set_option("tile_sched", 0)
+        M, N, K = self.SPLITK
+        bsk.gemm_f16_colmajor_enqueue(self.kA, self.kB, self.kC, M, N, K)
+        bsk.set_option("split_k", 16)
+        try:
+            bsk.gemm_f16_colmajor_enqueue(self.kA, self.kB, self.k16C, M, N, K)
+        finally:
+            bsk.set_option("split_k", 0)
         M, K = self.GEMV
         bsk.gemv_bf16_enqueue(self.W, self.x1, self.y1, M, K, 1)
         bsk.gemv_bf16_enqueue(self.W, self.x8, self.y8, M, K, 8)
@@ -143,7 +157,7 @@ class Problem:
 
     def outputs(self):
         return [from_dev(t) for t in (self.gC, self.rC, self.sC, self.dC, self.y1, self.y8, self.o)] + \
-            [self.f8C.cpu().numpy().view(np.uint32)]
+            [self.f8C.cpu().numpy().view(np.uint32)] + [from_dev(t) for t in (self.kC, self.k16C)]
 
 
 def check_integer_outputs(prob, outs):
@@ -167,6 +181,10 @@ def check_integer_outputs(prob, outs):
     M, N, K = prob.FP8
     _, want = oracle.gemm_fp8(prob.f8A.cpu().numpy(), prob.f8B.cpu().numpy(), M, N, K, K, K, "e4m3", 0.5, "f32")
     assert np.array_equal(outs[7], want), "FP8 GEMM"
+    M, N, K = prob.SPLITK
+    _, want = oracle.gemm_f16_colmajor(from_dev(prob.kA), from_dev(prob.kB), M, N, K)
+    assert np.array_equal(outs[8], want), "split-K GEMM (automatic plan)"
+    assert np.array_equal(outs[9], want), "split-K GEMM (cluster of 16)"
 
 
 def test_graph_replay_matches_eager_calls():
@@ -192,7 +210,7 @@ def test_graph_replay_matches_eager_calls():
 
     for seed in (200, 300):
         prob.refill(seed)
-        for t in (prob.gC, prob.rC, prob.sC, prob.dC, prob.y1, prob.y8, prob.o, prob.f8C):
+        for t in (prob.gC, prob.rC, prob.sC, prob.dC, prob.y1, prob.y8, prob.o, prob.f8C, prob.kC, prob.k16C):
             t.fill_(0x5A5A)
         graph.replay()
         torch.cuda.synchronize()

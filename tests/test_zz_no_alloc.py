@@ -8,7 +8,8 @@ device array instead.
 The GPU tests call it through the C ABI:
   * twice in a row on each of several problems -- both operands packed (the
     4095 x 4097 x 4100 workload), unaligned base pointers, 16-byte-aligned
-    operands that need no scratch, a skinny shape, and K = 0 -- and check
+    operands that need no scratch, a skinny shape, stream-K partials in the
+    array, and K = 0 -- and check
     every result against the oracle (integer-valued inputs bit for bit,
     random ones within the tolerance the parity tests use) and against the
     regular gemm_f16_colmajor (the same planner and kernels: bit-identical);
@@ -104,6 +105,36 @@ def test_matches_oracle_and_regular_entry_point_on_two_calls_in_a_row(lib, M, N,
         # same planner, same kernels: the regular entry point's bits (so within its tolerance too)
         assert np.array_equal(got, regular), f"call {call}: differs from gemm_f16_colmajor"
     assert np.array_equal(from_dev(Ad), A) and np.array_equal(from_dev(Bd), B), "an input was modified"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K,offset", [(512, 256, 8192, 0), (1000, 24, 2056, 3)])
+def test_stream_k_partials_in_the_fixed_array(lib, M, N, K, offset):
+    """Stream-K forced: its FP32 partials and flags come from the fixed array (after
+    the packed operands, for the unaligned problem).  Integer inputs match the
+    oracle bit for bit and the regular entry point under the same option, and
+    calls after the first leave device free memory unchanged."""
+    import torch
+
+    torch.cuda.init()
+    oracle.build()
+    A, B = inputs.gemm_operands(M, N, K, "int2", 11, 12)
+    Ad, Bd, buf = _device_operands(A, B, M, N, offset)
+    _, want = oracle.gemm_f16_colmajor(A, B, M, N, K)
+    bsk.set_option("stream_k", 2)
+    try:
+        regular = _call(bsk.gemm_f16_colmajor, Ad, Bd, buf, M, N, K, offset)
+        assert np.array_equal(regular, want), "regular entry point, stream-K"
+        _call(bsk.gemm_f16_colmajor_noalloc, Ad, Bd, buf, M, N, K, offset)   # set-up call
+        DefaultPool(torch.cuda.current_device()).reset_marks()   # returns the regular call's workspace
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        for call in range(2):
+            got = _call(bsk.gemm_f16_colmajor_noalloc, Ad, Bd, buf, M, N, K, offset)
+            assert torch.cuda.mem_get_info()[0] == free0, f"call {call}: device free memory moved"
+            assert np.array_equal(got, want), f"call {call}: differs from the oracle"
+    finally:
+        bsk.set_option("stream_k", 0)
 
 
 @pytest.mark.gpu
