@@ -44,6 +44,7 @@ OPTIONS = {
     "block_m": 14,
     "split_k": 15,
     "prefetch_kb": 16,
+    "k_order": 17,
 }
 
 # Every symbol include/bsk.h (the C ABI) declares.

@@ -46,7 +46,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 17;
+constexpr int kNumOpts = 18;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -538,6 +538,14 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     // up to 16, 1-2 us slower at 32 (the prefetches then delay the first loads).
     const long long pf_opt = opt_or(BSK_OPT_PREFETCH_KB, 0);
     g.prefetch_kb = static_cast<int>(pf_opt == 0 ? 16 : pf_opt == 1 ? 0 : pf_opt);
+    // CTA pairs: odd rounds of whole tiles run their k loop from the top, so a
+    // round starts on the A panels' k-slices the round before it read last (still
+    // in L2).  8192^2 x 16384 on GB300, back to back for 3 s under the 1.4 kW
+    // cap, two interleaved pairs of runs: 1612.7 / 1616.5 TFLOP/s at 1447 / 1455
+    // MHz against 1597.7 / 1598.8 at 1425 / 1432 always ascending; DRAM reads of
+    // one launch 2.23 / 2.28 GB against 2.31 / 2.54; single launches the same
+    // within their spread.  Each tile still has one fixed summation order.
+    g.k_alternate = opt_or(BSK_OPT_K_ORDER, 0) != 1;
     if (bsk::launch_gemm(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
     return BSK_OK;
 }
@@ -1232,6 +1240,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_BLOCK_M: ok = value >= 0 && value <= 128 && value % 8 == 0; break;
     case BSK_OPT_SPLIT_K: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16; break;
     case BSK_OPT_PREFETCH_KB: ok = value >= 0 && value <= 64; break;
+    case BSK_OPT_K_ORDER: ok = value == 0 || value == 1; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

@@ -141,6 +141,7 @@ struct GemmLaunch {
                              // dividing block_n); 0 = off
     int prefetch_kb = 0;     // one-CTA kernel, K-major A, whole tiles: extra k-blocks of the first
                              // tile's rows prefetched into L2 in the prologue
+    bool k_alternate = false;  // CTA pairs, whole tiles: odd rounds run their k loop downwards
 };
 
 // Returns 0 on success; otherwise an error message is written to `msg`.

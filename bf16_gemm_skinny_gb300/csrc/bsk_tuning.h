@@ -75,6 +75,9 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *                            prefetch into L2 while the launch waits for the kernel before
  *                            it, beyond the two stages the producer prefetches: 0 automatic
  *                            (16), 1 none, 2..64 that many
+ *   BSK_OPT_K_ORDER          k order of the CTA-pair GEMM's whole tiles: 0 automatic (odd
+ *                            rounds of tiles descending, so a round starts on the k-slices
+ *                            the round before it left in L2), 1 always ascending
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
@@ -93,7 +96,8 @@ enum {
     BSK_OPT_TILE_SCHED = 13,
     BSK_OPT_BLOCK_M = 14,
     BSK_OPT_SPLIT_K = 15,
-    BSK_OPT_PREFETCH_KB = 16
+    BSK_OPT_PREFETCH_KB = 16,
+    BSK_OPT_K_ORDER = 17
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);

@@ -140,6 +140,11 @@ struct Params {
     int skc;
     // One-CTA kernel, K-major A, whole tiles: the epilogue warps prefetch k-blocks
     // [2, 2 + pf_kb) of their first tile's A rows into L2 before the dependency wait.
+    // CTA pairs, whole tiles: with rev_round = R > 0 the tiles of odd rounds
+    // (tile / R odd; R = the pairs of the fixed order) run their k loop from the
+    // last k-block down, so that a round starts on the A panels' k-slices the
+    // round before it read last, which are still in L2.
+    int rev_round;
     const uint8_t* a_rows;  // A's first row
     long long a_ld_bytes;   // bytes between A's rows
     int pf_kb;
@@ -992,6 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
                 const int m0 = pm * T + static_cast<int>(rank) * kBM;
                 const int n0 = pn * T + static_cast<int>(rank) * kBM;
+                const bool rev = p.rev_round > 0 && kb0 == 0 && kb1 == p.num_kb && ((tile / p.rev_round) & 1);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
                         ok = false;
@@ -1001,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = leader_full0 + 8 * stage;
                     const uint32_t a_dst = smem_u32(sA + stage * Cf::kABytes);
                     const uint32_t b_dst = smem_u32(sB + stage * Cf::kBBytes);
-                    const int k0 = kb * Ty::kBK;
+                    const int k0 = (rev ? kb0 + kb1 - 1 - kb : kb) * Ty::kBK;
                     if constexpr (A_MN) {
                         tma_load_2d_pair(a_dst, &tmA, fb, m0, k0);
                         tma_load_2d_pair(a_dst + Cf::kABytes / 2, &tmA, fb, m0 + 64, k0);
@@ -1308,6 +1314,7 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     p.wait_limit_ns = g.wait_limit_ns;
     p.dyn = 0;
     p.skc = 0;
+    p.rev_round = 0;
     p.a_rows = static_cast<const uint8_t*>(g.A);
     p.a_ld_bytes = g.lda * Ty::kElemBytes;
     p.pf_kb = A_MN ? 0 : g.prefetch_kb;
@@ -1469,6 +1476,7 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.wait_limit_ns = g.wait_limit_ns;
     p.dyn = 0;
     p.skc = 0;
+    p.rev_round = 0;
     p.a_rows = nullptr;
     p.a_ld_bytes = 0;
     p.pf_kb = 0;
@@ -1516,6 +1524,7 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
         if (p.sk_dp_tiles == p.num_tiles) p.sk_dp_tiles -= clusters;   // keep one wave to share
         p.sk_iters = static_cast<long long>(p.num_tiles - p.sk_dp_tiles) * p.num_kb;
         const int pairs = static_cast<long long>(clusters) < p.sk_iters ? clusters : static_cast<int>(p.sk_iters);
+        p.rev_round = g.k_alternate ? pairs : 0;
         p.sk_part = g.sk_part;
         p.sk_flag = g.sk_flag;
         cudaLaunchAttribute attr2[2];
@@ -1535,6 +1544,7 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     }
     const int per_pair = (p.num_tiles + clusters - 1) / clusters;
     const int pairs = (p.num_tiles + per_pair - 1) / per_pair;
+    p.rev_round = g.k_alternate ? pairs : 0;   // the dynamic order keeps the fixed order's rounds
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     if (g.dyn) {
         // one cluster per tile: the resident clusters take the tiles of those

@@ -405,6 +405,31 @@ def test_dynamic_tile_order_on_cta_pairs(M, N, K):
     assert np.array_equal(outs[1], outs[2])
 
 
+@pytest.mark.parametrize("M,N,K,sms", [(4095, 4097, 4100, 0), (2304, 2560, 1024, 0), (1000, 777, 1030, 8),
+                                       (300, 517, 2048, 9)])
+def test_k_order_of_rounds_on_cta_pairs(M, N, K, sms):
+    """CTA pairs over two or more rounds of tiles, with odd rounds running their
+    k loop downwards (the default) and with every k loop ascending: integer inputs
+    give the oracle's bits either way, and random inputs stay within tolerance
+    and repeat bit for bit."""
+    A, B = operands(M, N, K, "int2")
+    Ar, Br = operands(M, N, K, "normal0.5")
+    cols = sorted(c for c in {0, 1, 255, 256, 511, 512, N // 2, N - 1} if c < N)
+    rows = sorted(r for r in {0, 127, 128, 255, 256, M // 2, M - 1} if r < M)
+    outs = {}
+    for order in (0, 1):
+        bsk.set_option("num_sms", sms)
+        bsk.set_option("k_order", order)
+        try:
+            sampled_check(run(A, B, M, N, K), A, B, M, N, K, cols, rows, True)
+            outs[order] = run(Ar, Br, M, N, K)
+            assert np.array_equal(run(Ar, Br, M, N, K), outs[order])
+        finally:
+            bsk.set_option("k_order", 0)
+            bsk.set_option("num_sms", 0)
+        sampled_check(outs[order], Ar, Br, M, N, K, cols, rows, False)
+
+
 @pytest.mark.parametrize("sms,offset", [(1, 3), (2, 0), (5, 7)])
 def test_pack_on_few_sms(sms, offset):
     """The pack on a grid capped to a few SMs: each warp streams hundreds of
