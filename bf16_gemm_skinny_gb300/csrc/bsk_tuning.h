@@ -45,13 +45,14 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *                            tensor-core skinny GEMM (default: 1 for n <= 3, 5 for
  *                            n >= 4; a CUDA-core kernel whose buffers do not fit in
  *                            shared memory falls back to another)
- *   BSK_OPT_STREAM_K         GEMM schedule: 1 whole tiles, 2 stream-K (every SM -- or CTA
- *                            pair -- an equal share of the tile x k-block iterations of the
- *                            last wave; split tiles are summed in FP32 by the unit that
- *                            holds their first k-block), 0 automatic: stream-K on the
- *                            one-CTA-per-tile kernel when whole tiles would fill under three
- *                            quarters of the SMs and a tile has at least 32 k-blocks; whole
- *                            tiles on CTA pairs
+ *   BSK_OPT_STREAM_K         GEMM schedule: 1 whole tiles (no automatic split of any kind),
+ *                            2 stream-K (every SM -- or CTA pair -- an equal share of the
+ *                            tile x k-block iterations of the last wave; split tiles are
+ *                            summed in FP32 by the unit that holds their first k-block),
+ *                            0 automatic: on the one-CTA-per-tile kernel, when whole tiles
+ *                            would fill under three quarters of the SMs, split-K over a
+ *                            cluster where its estimated time is lowest, else stream-K if a
+ *                            tile has at least 64 k-blocks; whole tiles on CTA pairs
  *   BSK_OPT_PDL              1: launch the GEMM, GEMV and attention kernels in plain stream
  *                            order; 0 (default): as programmatic dependents of the kernel
  *                            before them in the stream, so that their launch and prologue
