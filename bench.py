@@ -798,8 +798,8 @@ def run_ours(args):
         "dtype": "f16/bf16 in, f32 accumulate",
         "data": "synthetic (seeded PCG64: GEMM A,B uniform[-1,1] FP16; W N(0,0.02), x N(0,1) BF16)",
         "config": {"workload": WORKLOAD, "gemm": [GEMM_M, GEMM_N, GEMM_K], "gemv": [GEMV_M, GEMV_K, list(GEMV_NS)],
-                   "parallelism": f"replicas x{world}", "gemm_tile": [256, 256, 64],
-                   "gemm_stage_bytes_per_sm": tile_stage_bytes(128, 128, 64),
+                   "parallelism": f"replicas x{world}", "gemm_tile": [512, 256, 64],
+                   "gemm_stage_bytes_per_sm": tile_stage_bytes(256, 128, 64),
                    "l2": "inputs larger than L2 (GEMM operands 537 MB; consecutive GEMV launches read different "
                          "356 MB weight copies, three in rotation)",
                    "gemv_timing": f"per-launch average over a chain of {GEMV_CHAIN} back-to-back launches per n "
@@ -819,7 +819,7 @@ def run_ours(args):
                          peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])), 4),
                      "traffic": committed_traffic("gemm_f16_8192x8192x16384"),
                      "peak_source": f"{peak_src} bf16_tflops (FP16 dense rate = BF16 on this part)",
-                     "kernel": "gemm_tcgen05_pair_kernel<MN-major A, FP16> (CTA pairs, 256x256 tiles)"},
+                     "kernel": "gemm_tcgen05_pair_kernel<MN-major A, FP16, 2 row blocks> (CTA pairs, 512x256 tiles)"},
         "gpu_launches": args.steps * (1 + GEMV_CHAIN * len(GEMV_NS)),
         "clocks": clocks,
     }

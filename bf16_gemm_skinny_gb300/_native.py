@@ -45,6 +45,7 @@ OPTIONS = {
     "split_k": 15,
     "prefetch_kb": 16,
     "k_order": 17,
+    "pair_m": 18,
 }
 
 # Every symbol include/bsk.h (the C ABI) declares.

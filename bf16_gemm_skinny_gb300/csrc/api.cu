@@ -46,7 +46,7 @@ int fail_cuda(cudaError_t e, const char* what)
 // ----------------------------------------------------------------------------
 // options
 // ----------------------------------------------------------------------------
-constexpr int kNumOpts = 18;
+constexpr int kNumOpts = 19;
 std::atomic<long long> g_opt[kNumOpts];
 
 long long opt_or(int key, long long dflt)
@@ -260,6 +260,7 @@ struct GemmPlan {
     bool stream_k = false;  // one-CTA kernel: stream-K schedule (workspace partials)
     int skc = 0;            // one-CTA kernel: split-K over clusters of skc CTAs
     bool dyn = false;       // CTA pairs: dynamic tile order
+    int pair_m = 1;         // CTA pairs: 256-row blocks per tile (1: 256 x 256, 2: 512 x 256)
 };
 
 GemmPlan plan_gemm(const GemmOp& op, int sms)
@@ -402,6 +403,28 @@ GemmPlan plan_gemm(const GemmOp& op, int sms)
     // CTAs -- measured 1.2 us slower per launch on GB300 (n = 4 and 8, chains of
     // 24 launches: 59.2 / 58.6 us against 57.8 / 57.4), so they are not the
     // default.
+    // CTA pairs on 512 x 256 tiles (16-bit inputs, K-major B, whole tiles in the
+    // fixed order): each CTA stages 256 rows of A, so every B slice in shared
+    // memory feeds two MMAs and a k step moves 48 KB per SM for twice the MMAs of
+    // a 256 x 256 tile's 32 KB, which relieves the shared memory (at 256 x 256 its
+    // bandwidth is the limit).  The one accumulator leaves the epilogue of a tile
+    // unhidden, so long k loops only.  GB300, 16-bit, calls back to back (256 x
+    // 256 / 512 x 256 tiles): 8192^2 x 16384 1853-1856 / 1924-1926 TFLOP/s, for 3 s
+    // under the power cap 1610-1611 / 1672-1673 (SM clock 1470-1477 / 1530 MHz);
+    // 8192^3 1829-1841 / 1869-1874; 34816 x 4096 x 5120 (80 k-blocks) 0.753 / 0.783 ms.
+    int pair_m = 1;
+    const long long pm_opt = opt_or(BSK_OPT_PAIR_M, 0);
+    if (pair && !stream_k && !dyn && !op.b_mn_major && !fp8 && pm_opt != 1) {
+        if (pm_opt == 2) {
+            pair_m = 2;
+        } else if (kbs >= 128) {
+            const long long pairs = sms / 2 > 0 ? sms / 2 : 1;
+            const long long n_tiles = (op.N + 255LL) / 256;
+            const double fill256 = fill(((op.M + 255LL) / 256) * n_tiles, pairs);
+            const double fill512 = fill(((op.M + 511LL) / 512) * n_tiles, pairs);
+            if (fill512 >= fill256 - 0.02) pair_m = 2;
+        }
+    }
     int block_m = 128;
     const long long bm_opt = opt_or(BSK_OPT_BLOCK_M, 0);
     if (!pair && !stream_k && !op.a_mn_major && (op.N + block_n - 1LL) / block_n == 1 && bm_opt > 0)
@@ -413,6 +436,7 @@ GemmPlan plan_gemm(const GemmOp& op, int sms)
     plan.stream_k = stream_k;
     plan.skc = skc;
     plan.dyn = dyn;
+    plan.pair_m = pair_m;
     return plan;
 }
 
@@ -546,6 +570,7 @@ int run_gemm(const GemmOp& op, int sms, cudaStream_t s, const bsk::FixedScratch*
     // one launch 2.23 / 2.28 GB against 2.31 / 2.54; single launches the same
     // within their spread.  Each tile still has one fixed summation order.
     g.k_alternate = opt_or(BSK_OPT_K_ORDER, 0) != 1;
+    g.pair_m = plan.pair_m;
     if (bsk::launch_gemm(g, s, msg, sizeof(msg))) return fail(BSK_ERR_CUDA, "%s", msg);
     return BSK_OK;
 }
@@ -1241,6 +1266,7 @@ int bsk_set_option(int key, long long value)
     case BSK_OPT_SPLIT_K: ok = value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16; break;
     case BSK_OPT_PREFETCH_KB: ok = value >= 0 && value <= 64; break;
     case BSK_OPT_K_ORDER: ok = value == 0 || value == 1; break;
+    case BSK_OPT_PAIR_M: ok = value >= 0 && value <= 2; break;
     case BSK_OPT_WAIT_LIMIT_US: ok = value >= 0 && value <= 60000000; break;
     case BSK_OPT_NUM_SMS: ok = value >= 0 && value <= 100000; break;
     default: ok = false;

@@ -142,6 +142,8 @@ struct GemmLaunch {
     int prefetch_kb = 0;     // one-CTA kernel, K-major A, whole tiles: extra k-blocks of the first
                              // tile's rows prefetched into L2 in the prologue
     bool k_alternate = false;  // CTA pairs, whole tiles: odd rounds run their k loop downwards
+    int pair_m = 1;          // CTA pairs, 16-bit inputs, K-major B, whole tiles in the fixed order:
+                             // 256-row blocks per pair tile (1 or 2)
 };
 
 // Returns 0 on success; otherwise an error message is written to `msg`.
@@ -151,6 +153,10 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_
 int split_k_capacity(int skc);
 // The FP8 part of launch_gemm (gemm_fp8.cu).
 int launch_gemm_fp8(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
+// CTA pairs on 512 x 256 tiles (gemm_tcgen05_m512.cu), and its column-major FP16
+// instance (for loading its code ahead of time).
+int launch_gemm_pair_m512(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len);
+const void* gemm_pair_m512_colmajor_kernel();
 
 // Decode GEMV / skinny GEMM on the CUDA cores: y[t, j] = sum_k x[t, k] W[j, k]
 // for t < n <= 8, W [M, K] row-major, x [n, K], y [n, M] row-major, BF16.

@@ -79,6 +79,11 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
  *   BSK_OPT_K_ORDER          k order of the CTA-pair GEMM's whole tiles: 0 automatic (odd
  *                            rounds of tiles descending, so a round starts on the k-slices
  *                            the round before it left in L2), 1 always ascending
+ *   BSK_OPT_PAIR_M           rows of a CTA-pair tile (16-bit inputs, K-major B, whole tiles in
+ *                            the fixed order): 0 automatic, 1 256 x 256 tiles, 2 512 x 256
+ *                            tiles (each CTA stages 256 rows of A; every B slice feeds two
+ *                            MMAs; one accumulator, so the epilogue no longer overlaps the
+ *                            next tile's MMAs)
  * Returns BSK_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 enum {
@@ -98,7 +103,8 @@ enum {
     BSK_OPT_BLOCK_M = 14,
     BSK_OPT_SPLIT_K = 15,
     BSK_OPT_PREFETCH_KB = 16,
-    BSK_OPT_K_ORDER = 17
+    BSK_OPT_K_ORDER = 17,
+    BSK_OPT_PAIR_M = 18
 };
 int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);

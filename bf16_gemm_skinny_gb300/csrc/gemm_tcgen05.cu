@@ -56,7 +56,8 @@ int preload_gemm_f16_colmajor_kernels(char* msg, size_t msg_len)
     // the instances gemm_f16_colmajor may pick: MN-major A, K-major B, FP16 in
     // and out, on CTA pairs or one CTA per 128 x BN tile
     const void* kernels[] = {
-        reinterpret_cast<const void*>(gemm_tcgen05_pair_kernel<true, false, kInF16, kOutF16>),
+        reinterpret_cast<const void*>(gemm_tcgen05_pair_kernel<true, false, kInF16, kOutF16, 1>),
+        gemm_pair_m512_colmajor_kernel(),
         reinterpret_cast<const void*>(gemm_tcgen05_kernel<256, true, false, kInF16, kOutF16>),
         reinterpret_cast<const void*>(gemm_tcgen05_kernel<128, true, false, kInF16, kOutF16>),
         reinterpret_cast<const void*>(gemm_tcgen05_kernel<64, true, false, kInF16, kOutF16>),
@@ -126,6 +127,8 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_
         snprintf(msg, msg_len, "16-bit GEMMs produce their input type");
         return 1;
     }
+    if (g.block_n == 256 && g.pair && g.pair_m == 2 && !g.stream_k && !g.dyn && !g.b_mn_major)
+        return launch_gemm_pair_m512(g, stream, msg, msg_len);
     switch (g.block_n) {
     case 256: return g.pair ? dispatch_pair(g, stream, msg, msg_len) : dispatch_single<256>(g, stream, msg, msg_len);
     case 128: return dispatch_single<128>(g, stream, msg, msg_len);

@@ -850,14 +850,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   * each CTA's epilogue warps hand the accumulator back by arriving on the even
 //     CTA's "accumulator empty" barrier (8 arrivals).
 // ---------------------------------------------------------------------------
+template <int MB>
 struct PairCfg {
-    static constexpr int kStages = 6;
-    static constexpr int kABytes = kBM * kRowBytes;        // this CTA's 128 rows of A
+    static_assert(MB == 1 || MB == 2, "one or two 256-row blocks per pair tile");
+    static constexpr int kStages = MB == 1 ? 6 : 4;
+    static constexpr int kBlockABytes = kBM * kRowBytes;   // this CTA's 128 rows of one A block
+    static constexpr int kABytes = MB * kBlockABytes;
     static constexpr int kBBytes = kBM * kRowBytes;        // this CTA's 128 rows of B
-    static constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB; the pair moves 64 KB per stage
+    static constexpr int kStageBytes = kABytes + kBBytes;  // 32 / 48 KB; the pair moves twice that per stage
     static constexpr int kEpiBufBytes = kEpiBox * kEpiBox * 2;
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
-    static constexpr int kTile = 256;                      // pair tile is 256 x 256
+    static constexpr int kTile = 256;                      // pair tile is 256 * MB rows x 256 columns
+    // MB = 1: two 256-column accumulators (the epilogue of one tile overlaps the
+    // next tile's MMAs); MB = 2: one accumulator of two 256-column blocks
+    static constexpr int kAccBufs = MB == 1 ? 2 : 1;
     static constexpr int kTmemCols = 2 * kTile;
     static constexpr int kNumBars = 2 * kStages + 5;
     // barriers, TMEM slot + abort flag, then the dynamic order's 2 x kSched
@@ -870,14 +876,15 @@ struct PairCfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
 };
 
-template <bool A_MN, bool B_MN, int IN, int OUT>
+template <bool A_MN, bool B_MN, int IN, int OUT, int MB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const Params p)
 {
-    using Cf = PairCfg;
+    using Cf = PairCfg<MB>;
     constexpr int S = Cf::kStages;
     constexpr int T = Cf::kTile;
+    constexpr int TM = T * MB;   // rows of C per pair tile
     using Ty = Types<IN, OUT>;
     constexpr uint32_t kIdesc = Ty::idesc(A_MN, B_MN, 2 * kBM, T);
     static_assert(!Ty::kFp8 || (!A_MN && !B_MN), "FP8 operands are K-major");
@@ -995,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 int pm, pn;
                 tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
-                const int m0 = pm * T + static_cast<int>(rank) * kBM;
+                const int m0 = pm * TM + static_cast<int>(rank) * kBM;   // this CTA's rows of A block 0
                 const int n0 = pn * T + static_cast<int>(rank) * kBM;
                 const bool rev = p.rev_round > 0 && kb0 == 0 && kb1 == p.num_kb && ((tile / p.rev_round) & 1);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -1008,11 +1015,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_dst = smem_u32(sA + stage * Cf::kABytes);
                     const uint32_t b_dst = smem_u32(sB + stage * Cf::kBBytes);
                     const int k0 = (rev ? kb0 + kb1 - 1 - kb : kb) * Ty::kBK;
-                    if constexpr (A_MN) {
-                        tma_load_2d_pair(a_dst, &tmA, fb, m0, k0);
-                        tma_load_2d_pair(a_dst + Cf::kABytes / 2, &tmA, fb, m0 + 64, k0);
-                    } else {
-                        tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
+#pragma unroll
+                    for (int b = 0; b < MB; ++b) {   // A block b: rows m0 + b * 256 of this CTA's half
+                        const uint32_t ab = a_dst + b * Cf::kBlockABytes;
+                        if constexpr (A_MN) {
+                            tma_load_2d_pair(ab, &tmA, fb, m0 + b * T, k0);
+                            tma_load_2d_pair(ab + Cf::kBlockABytes / 2, &tmA, fb, m0 + b * T + 64, k0);
+                        } else {
+                            tma_load_2d_pair(ab, &tmA, fb, k0, m0 + b * T);
+                        }
                     }
                     if constexpr (B_MN) {
                         tma_load_2d_pair(b_dst, &tmB, fb, n0, k0);            // 64(n) x 64(k)
@@ -1072,13 +1083,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else if (!seg_next(p, cur, tile, kb0, kb1)) {
                     break;
                 }
-                const int acc = it & 1;
-                const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+                const int acc = it % Cf::kAccBufs;
+                const uint32_t aph = static_cast<uint32_t>(it / Cf::kAccBufs) & 1u;
                 if (!mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
+                // accumulator of A block b: TMEM columns (acc + b) * 256 (one of acc, b is 0)
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * T);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
@@ -1090,11 +1102,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_base = smem_u32(sB + stage * Cf::kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < kRowBytes / kMmaBytes; ++kk) {
-                        const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, Cf::kABytes / 2, 1024)
-                                                 : smem_desc_sw128(a_base + kk * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
                                                  : smem_desc_sw128(b_base + kk * 32, 16, 1024);
-                        mma_issue_pair<Ty::kFp8>(d_tmem, ad, bd, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+#pragma unroll
+                        for (int b = 0; b < MB; ++b) {   // the blocks share this k-step's B slice
+                            const uint32_t ab = a_base + b * Cf::kBlockABytes;
+                            const uint64_t ad = A_MN ? smem_desc_sw128(ab + kk * 2048, Cf::kBlockABytes / 2, 1024)
+                                                     : smem_desc_sw128(ab + kk * 32, 16, 1024);
+                            mma_issue_pair<Ty::kFp8>(d_tmem + static_cast<uint32_t>(b * T), ad, bd, kIdesc,
+                                                     (kb != kb0 || kk != 0) ? 1u : 0u);
+                        }
                     }
                     mma_commit_pair_multicast(empty0 + 8 * stage, 0x3);
                     issued_any = true;
@@ -1114,7 +1131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------------
-        // Epilogue (both CTAs): this CTA's 128 rows of the 256 x 256 tile
+        // Epilogue (both CTAs): this CTA's 128 rows of each 256-row block of the tile
         // ------------------------------------------------------------------
         const int quarter = warp & 3;
         const int ew = warp - 2;
@@ -1135,15 +1152,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (!seg_next(p, cur, tile, kb0, kb1)) {
                 break;
             }
-            const int acc = it & 1;
-            const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+            const int acc = it % Cf::kAccBufs;
+            const uint32_t aph = static_cast<uint32_t>(it / Cf::kAccBufs) & 1u;
             bool ok = mbar_wait(tfull0 + 8 * acc, aph, wc, kSiteEpilogueTmemFull);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after_sync();
             int pm, pn;
             tile_coord(tile, p.num_m, p.num_n, p.group_m, &pm, &pn);
-            const int m0 = pm * T + static_cast<int>(rank) * kBM + quarter * 32;
+            const int m0 = pm * TM + static_cast<int>(rank) * kBM + quarter * 32;   // in A block 0
             const int n0 = pn * T;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * T);
@@ -1160,11 +1177,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)__all_sync(0xffffffffu, fok);   // on a timeout the status word is set; the output is undefined
             }
 #pragma unroll 1
-            for (int c = 0; c < T / 32; ++c) {
+            for (int cb = 0; cb < MB * (T / 32); ++cb) {
+                const int b = cb / (T / 32);   // A block of the chunk (stream-K runs with MB = 1)
+                const int c = cb % (T / 32);
+                const int mb = m0 + b * T;
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c * 32, r);
+                tmem_ld_32x32b_x32(t_row + b * T + c * 32, r);
                 tmem_ld_wait();
-                if (c == T / 32 - 1) {
+                if (cb == MB * (T / 32) - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_remote(leader_tempty0 + 8 * acc);
@@ -1176,10 +1196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 32; ++j) ps[j * kBM] = __uint_as_float(r[j]);
                     continue;
                 }
+                if (mb >= p.M) continue;   // all 32 rows past the end of C: nothing to store
                 // slot of CTA (pair q, rank): (q * 2 + rank) * T * kBM
                 add_partials(r, p.sk_part + static_cast<long long>(rank) * T * kBM + slot_col, 2LL * T * kBM, pair + 1,
                              q_last);
-                finish_acc<IN, OUT>(r, p, m0 + lane, n0 + c * 32);
+                finish_acc<IN, OUT>(r, p, mb + lane, n0 + c * 32);
                 if (Ty::kOutBytes == 2 && p.tma_store) {
                     uint8_t* buf = ebuf + (staged++ & 1) * Cf::kEpiBufBytes;
                     if (lane == 0) bulk_wait_group_read<1>();
@@ -1190,11 +1211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, smem_u32(buf), m0, n0 + c * 32);
+                        tma_store_2d(&tmC, smem_u32(buf), mb, n0 + c * 32);
                         bulk_commit_group();
                     }
                 } else {
-                    store_row<OUT>(r, p, m0 + lane, n0 + c * 32, p.M);
+                    store_row<OUT>(r, p, mb + lane, n0 + c * 32, p.M);
                 }
             }
             if (to_slot) {
@@ -1444,11 +1465,15 @@ int launch_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t 
     return 0;
 }
 
-template <bool A_MN, bool B_MN, int IN, int OUT>
+template <bool A_MN, bool B_MN, int IN, int OUT, int MB = 1>
 int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, size_t msg_len)
 {
-    using Cf = PairCfg;
+    using Cf = PairCfg<MB>;
     using Ty = Types<IN, OUT>;
+    if (MB != 1 && (g.stream_k || g.dyn)) {
+        snprintf(msg, msg_len, "GEMM (CTA pair): 512-row tiles run whole tiles in the fixed order only");
+        return 1;
+    }
     CUtensorMap tmA, tmB, tmC;
     if (!encode_operands<IN, OUT, A_MN, B_MN>(g, kBM, kBM, &tmA, &tmB, &tmC, msg, msg_len)) return 1;
     Params p;
@@ -1456,7 +1481,7 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.bm = kBM;
     p.N = g.N;
     p.K = g.K;
-    p.num_m = (g.M + Cf::kTile - 1) / Cf::kTile;
+    p.num_m = (g.M + Cf::kTile * MB - 1) / (Cf::kTile * MB);
     p.num_n = (g.N + Cf::kTile - 1) / Cf::kTile;
     p.num_tiles = p.num_m * p.num_n;
     p.num_kb = (g.K + Ty::kBK - 1) / Ty::kBK;
@@ -1481,7 +1506,7 @@ int launch_pair_instance(const GemmLaunch& g, cudaStream_t stream, char* msg, si
     p.a_ld_bytes = 0;
     p.pf_kb = 0;
 
-    auto kern = gemm_tcgen05_pair_kernel<A_MN, B_MN, IN, OUT>;
+    auto kern = gemm_tcgen05_pair_kernel<A_MN, B_MN, IN, OUT, MB>;
     static SmemOptIn smem_opt;
     cudaError_t e = smem_opt.ensure(reinterpret_cast<const void*>(kern), Cf::kSmemBytes);
     if (e != cudaSuccess) {

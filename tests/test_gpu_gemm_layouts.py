@@ -325,3 +325,49 @@ def test_random_layouts_default_plan(M, N, K, order, transa, transb, pads, mode)
                                 bias=bias, mode=mode)
     _, out = want(order, transa, transb, Af, lda, Bf, ldb, M, N, K, bias=bias, mode=mode)
     assert np.array_equal(got, out), f"{int((got != out).sum())} of {got.size} entries differ"
+
+
+@pytest.mark.parametrize("order,transa,transb,M,N,K,sms,mode", [
+    (0, 0, 0, 1000, 777, 1030, 8, 0),     # MN-major A; four pairs, several rounds of 512 x 256 tiles
+    (0, 0, 0, 600, 517, 640, 8, 0),       # the second tile row's second block lies wholly past M
+    (0, 1, 0, 1536, 512, 640, 6, 1),      # K-major A, per-row bias, three pairs
+    (1, 0, 1, 700, 1100, 1024, 8, 2),     # the row-major linear layer X W^T + b (K-major after the swap)
+    (0, 0, 0, 2304, 2560, 1024, 0, 0),
+])
+def test_pair_512_row_tiles(order, transa, transb, M, N, K, sms, mode):
+    """CTA pairs on 512 x 256 tiles (BSK_OPT_PAIR_M = 2: two 256-row blocks per
+    pair tile sharing each B slice; grids capped where needed so that the
+    planner keeps CTA pairs): integer inputs, with an integer bias where
+    given, match the oracle bit for bit; with every k loop ascending, random
+    inputs give the bits of the 256 x 256 tiles (each output sums the same
+    products in the same order)."""
+    A2, B2 = operands(M, N, K, "int2")
+    bias = None
+    if mode:
+        vals = np.random.default_rng(5).integers(-40, 41, max(M, N))
+        bias = enc(vals[:M] if mode == 1 else vals[:N])
+    bsk.set_option("pair_m", 2)
+    bsk.set_option("num_sms", sms)
+    try:
+        got, Af, lda, Bf, ldb = run(order, transa, transb, A2, B2, pad_a=8, pad_b=16, pad_c=8, bias=bias, mode=mode)
+    finally:
+        bsk.set_option("pair_m", 0)
+        bsk.set_option("num_sms", 0)
+    rows = np.unique(np.r_[np.arange(0, M, 37), M - 1]) if M * N > 1 << 20 else None
+    cols = np.unique(np.r_[np.arange(0, N, 41), N - 1]) if M * N > 1 << 20 else None
+    _, out = want(order, transa, transb, Af, lda, Bf, ldb, M, N, K, bias=bias, mode=mode, rows=rows, cols=cols)
+    sub = got if rows is None else got[np.ix_(rows, cols)]
+    assert np.array_equal(sub, out), f"{int((sub != out).sum())} of {sub.size} entries differ"
+    Ar, Br = operands(M, N, K, "normal0.5")
+    outs = {}
+    for pm in (1, 2):
+        bsk.set_option("pair_m", pm)
+        bsk.set_option("k_order", 1)
+        bsk.set_option("num_sms", sms)
+        try:
+            outs[pm] = run(order, transa, transb, Ar, Br, pad_a=8, pad_b=16, pad_c=8)[0]
+        finally:
+            bsk.set_option("pair_m", 0)
+            bsk.set_option("k_order", 0)
+            bsk.set_option("num_sms", 0)
+    assert np.array_equal(outs[1], outs[2])

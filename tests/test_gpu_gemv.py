@@ -235,6 +235,22 @@ def test_skinny_prologue_prefetch_depths(prefetch_kb, M, K, n, offset, block_m):
         bsk.set_option("block_m", 0)
 
 
+@pytest.mark.parametrize("M,K,n", [(1100, 640, 600), (2048, 1032, 1024)])
+def test_prefill_on_512_row_pair_tiles(M, K, n):
+    """The BF16 prefill product (K-major W and x) on CTA pairs with 512 x 256
+    tiles forced (on 8 SMs, so that the planner keeps CTA pairs for these
+    short k loops): integer inputs give the oracle's bits."""
+    bsk.set_option("pair_m", 2)
+    bsk.set_option("num_sms", 8)
+    try:
+        W, x = operands(M, K, n, True)
+        _, want = oracle.linear_bf16(W, x, M, K, n)
+        assert np.array_equal(run(W, x, M, K, n), want)
+    finally:
+        bsk.set_option("pair_m", 0)
+        bsk.set_option("num_sms", 0)
+
+
 def test_k_zero_and_empty():
     got = run(np.zeros(0, np.uint16), np.zeros(0, np.uint16), 50, 0, 3)
     assert np.all(got == 0)

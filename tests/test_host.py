@@ -222,7 +222,7 @@ def test_options_round_trip_and_range_checks(lib):
     with pytest.raises(bsk.BskError):
         bsk.set_option("gemv_rows", 3)
     for name, good, bad in (("pdl", 1, 2), ("tile_sched", 2, 3), ("stream_k", 2, 3), ("split_k", 16, 3),
-                            ("prefetch_kb", 64, 65), ("k_order", 1, 2)):
+                            ("prefetch_kb", 64, 65), ("k_order", 1, 2), ("pair_m", 2, 3)):
         bsk.set_option(name, good)
         assert bsk.get_option(name) == good
         bsk.set_option(name, 0)
