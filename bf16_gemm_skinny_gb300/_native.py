@@ -57,7 +57,7 @@ EXPORTS = (
 )
 # Tuning options and test hooks (csrc/bsk_tuning.h): exported for the tests and
 # the benchmark, not part of the C ABI.
-TUNING_EXPORTS = ("bsk_tile_coord", "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout")
+TUNING_EXPORTS = ("bsk_tile_coord", "bsk_set_option", "bsk_get_option", "bsk_test_wait_timeout", "bsk_plan_gemm")
 
 COL_MAJOR, ROW_MAJOR = 0, 1
 BIAS_NONE, BIAS_ROW, BIAS_COLUMN = 0, 1, 2
@@ -121,6 +121,8 @@ def load():
         lib.bsk_get_option.restype = ctypes.c_longlong
         lib.bsk_test_wait_timeout.argtypes = [ctypes.c_uint, p]
         lib.bsk_test_wait_timeout.restype = i
+        lib.bsk_plan_gemm.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(i)]
+        lib.bsk_plan_gemm.restype = i
         _lib = lib
         return lib
 
@@ -270,6 +272,14 @@ def tile_coord(t: int, num_m: int, num_n: int, group_m: int):
     pm, pn = ctypes.c_int(), ctypes.c_int()
     load().bsk_tile_coord(t, num_m, num_n, group_m, ctypes.byref(pm), ctypes.byref(pn))
     return pm.value, pn.value
+
+
+def plan_gemm(M: int, N: int, K: int, a_mn_major: bool = True, b_mn_major: bool = False, fp8: bool = False,
+              sms: int = 152) -> dict:
+    """The plan a GEMM of this shape would take (test hook; launches nothing)."""
+    out = (ctypes.c_int * 7)()
+    _check(load().bsk_plan_gemm(M, N, K, int(a_mn_major), int(b_mn_major), int(fp8), sms, out))
+    return dict(zip(("block_n", "block_m", "pair", "stream_k", "split_k", "pair_m", "dyn"), list(out)))
 
 
 def set_option(name: str, value: int) -> None:

@@ -1246,6 +1246,29 @@ void bsk_tile_coord(int t, int num_m, int num_n, int group_m, int* pid_m, int* p
     if (pid_n) *pid_n = pn;
 }
 
+int bsk_plan_gemm(int M, int N, int K, int a_mn_major, int b_mn_major, int fp8, int sms, int* plan)
+{
+    if (plan == nullptr || M < 1 || N < 1 || K < 1 || sms < 2)
+        return fail(BSK_ERR_INVALID_ARG, "plan query: sizes and SM count must be positive (sms >= 2), plan non-NULL");
+    GemmOp op;
+    op.M = M;
+    op.N = N;
+    op.K = K;
+    op.a_mn_major = a_mn_major != 0;
+    op.b_mn_major = b_mn_major != 0;
+    op.in_type = fp8 ? bsk::kInE4M3 : bsk::kInF16;
+    op.out_type = fp8 ? bsk::kOutBF16 : bsk::kOutF16;
+    const GemmPlan p = plan_gemm(op, sms);
+    plan[0] = p.block_n;
+    plan[1] = p.block_m;
+    plan[2] = p.pair ? 1 : 0;
+    plan[3] = p.stream_k ? 1 : 0;
+    plan[4] = p.skc;
+    plan[5] = p.pair_m;
+    plan[6] = p.dyn ? 1 : 0;
+    return BSK_OK;
+}
+
 int bsk_set_option(int key, long long value)
 {
     if (key < 1 || key >= kNumOpts) return fail(BSK_ERR_INVALID_ARG, "unknown option key %d", key);

@@ -110,6 +110,18 @@ int bsk_set_option(int key, long long value);
 long long bsk_get_option(int key);
 
 /*
+ * Test hook: the plan gemm_f16 / gemm_fp8 would take for an M x N x K product
+ * (column-major storage; a_mn_major / b_mn_major as the kernels see the
+ * operands; fp8 nonzero for E4M3 inputs) on `sms` SMs under the current
+ * options, written to plan[0..6]: tile width, tile height of the one-CTA
+ * kernel, CTA pairs (0/1), stream-K (0/1), split-K cluster size (0 = none),
+ * 256-row blocks per pair tile (1/2), dynamic tile order (0/1).  Split-K plans
+ * depend on how many clusters fit on the current device: without a device
+ * none is considered.  Launches nothing.
+ */
+int bsk_plan_gemm(int M, int N, int K, int a_mn_major, int b_mn_major, int fp8, int sms, int* plan);
+
+/*
  * Test hook for the watchdog: launches one CTA that waits on a barrier that
  * nothing completes, using the GEMM's bounded wait with a limit of
  * `limit_us` microseconds (1 .. 10,000,000).  Returns BSK_ERR_TIMEOUT when the

@@ -232,6 +232,52 @@ def test_options_round_trip_and_range_checks(lib):
     assert lib.bsk_set_option(len(bsk.OPTIONS) + 1, 1) == 1
 
 
+@pytest.mark.parametrize("shape,kw,want", [
+    # the headline product: CTA pairs on 512 x 256 tiles (a k loop of 256 blocks)
+    ((8192, 8192, 16384), {}, dict(pair=1, block_n=256, pair_m=2)),
+    ((6144, 6144, 8192), {}, dict(pair=1, pair_m=2)),
+    # 80 k-blocks: the unhidden epilogue of 512-row tiles would cost more than they save
+    ((34816, 4096, 5120), dict(a_mn_major=False), dict(pair=1, pair_m=1)),
+    ((4095, 4097, 4100), {}, dict(pair=1, pair_m=1)),
+    # 512-row tiles would fill the pairs worse (80 tiles in two waves against 144)
+    ((2304, 4096, 8192), {}, dict(pair=1, pair_m=1)),
+    # a transposed B and FP8 inputs keep 256 x 256 tiles
+    ((8192, 8192, 16384), dict(b_mn_major=True), dict(pair=1, pair_m=1)),
+    ((8192, 8192, 8192), dict(a_mn_major=False, fp8=True), dict(pair=1, pair_m=1)),
+    # latency-bound and short-k shapes run one CTA per tile
+    ((256, 256, 256), {}, dict(pair=0, block_n=32, pair_m=1)),
+    ((8192, 8192, 256), {}, dict(pair=0, block_n=256)),
+    # skinny decode: the tile width follows N
+    ((34816, 16, 5120), dict(a_mn_major=False), dict(pair=0, block_n=32, split_k=0)),
+    ((34816, 100, 5120), dict(a_mn_major=False), dict(pair=0, block_n=128)),
+])
+def test_planner_rules(lib, shape, kw, want):
+    """The tile plan the GEMM planner picks on 152 SMs (no launch; split-K plans,
+    which need the device's cluster capacity, are not considered here)."""
+    plan = bsk.plan_gemm(*shape, **kw)
+    assert {k: plan[k] for k in want} == want, plan
+
+
+def test_planner_follows_forcing_options(lib):
+    try:
+        bsk.set_option("pair_m", 1)
+        assert bsk.plan_gemm(8192, 8192, 16384)["pair_m"] == 1
+        bsk.set_option("pair_m", 2)
+        assert bsk.plan_gemm(34816, 4096, 5120, a_mn_major=False)["pair_m"] == 2
+        bsk.set_option("pair_m", 0)
+        bsk.set_option("tile_sched", 2)    # the dynamic order runs 256 x 256 tiles only
+        plan = bsk.plan_gemm(8192, 8192, 16384)
+        assert plan["dyn"] == 1 and plan["pair_m"] == 1
+        bsk.set_option("tile_sched", 0)
+        bsk.set_option("gemm_kernel", 1)   # one CTA per 128 x 256 tile
+        assert bsk.plan_gemm(8192, 8192, 16384)["pair"] == 0
+    finally:
+        for k in ("pair_m", "tile_sched", "gemm_kernel"):
+            bsk.set_option(k, 0)
+    with pytest.raises(bsk.BskError):
+        bsk.plan_gemm(0, 8, 8)
+
+
 def test_watchdog_probe_validates_limit(lib):
     assert lib.bsk_test_wait_timeout(0, None) == 1
     assert lib.bsk_test_wait_timeout(20_000_000, None) == 1
