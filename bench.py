@@ -154,13 +154,16 @@ def load_peaks():
 
 
 # The code each measured launch is built from: (file, text that starts the
-# file's host-only part or None).  Host-side launch code does not change the
-# kernel, so it is left out of the digest -- except the GEMM's planner
-# (api.cu), whose choices (tile order, tile width, schedule) change the
-# kernel's DRAM traffic.
+# file's host-only part or None), or (file, (first, end)) for the part of a
+# file from the text `first` up to the text `end`.  Host-side launch code does
+# not change the kernel, so it is left out of the digest -- except the GEMM's
+# planning and launch set-up in api.cu (pack, tile width and height, schedule,
+# tile order, k order), whose choices change the kernel's DRAM traffic.
 KERNEL_SOURCES = {
     "gemm": (("gemm_tcgen05.cuh", "inline CUtensorMapDataType tmap_type("), ("ptx.cuh", None),
-             ("bsk_internal.h", "using TmapEncodeFn"), ("api.cu", None)),
+             ("bsk_internal.h", "using TmapEncodeFn"),
+             ("api.cu", ("// Which operands must be packed before the TMA can read them",
+                         "// Elements a stored matrix"))),
     "gemv": (("gemv.cu", "int launch_vec(const GemvLaunch& g"), ("bsk_internal.h", "using TmapEncodeFn")),
 }
 
@@ -174,7 +177,12 @@ def source_digest(kernel: str) -> str:
     for name, host_start in KERNEL_SOURCES[kernel]:
         with open(os.path.join(cdir, name), "rb") as f:
             text = f.read()
-        if host_start is not None:
+        if isinstance(host_start, tuple):
+            first, end = (text.find(m.encode()) for m in host_start)
+            if first < 0 or end < first:
+                raise RuntimeError(f"{name}: markers {host_start!r} not found in order")
+            text = text[first:end]
+        elif host_start is not None:
             cut = text.find(host_start.encode())
             if cut < 0:
                 raise RuntimeError(f"{name}: host-code marker {host_start!r} not found")
