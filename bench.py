@@ -168,12 +168,13 @@ KERNEL_SOURCES = {
 }
 
 
-def source_digest(kernel: str) -> str:
+def source_digest(kernel: str, cdir: str | None = None) -> str:
     """Hash of one kernel's device code (comments and whitespace left out); a
     committed traffic figure is only reported while that code is unchanged
-    since it was measured."""
+    since it was measured.  `cdir`: the source directory (default: the
+    package's csrc/)."""
     h = hashlib.sha256()
-    cdir = os.path.join(ROOT, "bf16_gemm_skinny_gb300", "csrc")
+    cdir = cdir or os.path.join(ROOT, "bf16_gemm_skinny_gb300", "csrc")
     for name, host_start in KERNEL_SOURCES[kernel]:
         with open(os.path.join(cdir, name), "rb") as f:
             text = f.read()
